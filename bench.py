@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Throughput of the TurboQuant KV-cache hot path on GB300.
+
+One step = one decode step of one attention layer for the whole batch: the
+fused store of every sequence's new token (tq_store) followed by decode
+attention over the compressed paged cache (tq_decode_attention), on seeded
+synthetic data with the workload's shapes.  Default workload: the
+Llama-3.1-8B-shaped decode layer (32 query / 8 KV heads, d=128, batch 16,
+8,192-token contexts, 3-bit keys + QJL, 4-bit group-32 values).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is KV tokens attended per second over
+the whole job (sum of context lengths / step time, summed over ranks; every
+rank runs its own replica: weak scaling).  The reference arm (--impl
+reference) times the CPU oracle on a bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+DEFAULT_WORKLOAD = "llama8b_gqa4_b16_8k"
+METRIC = "decode-attn KV tokens/s & achieved HBM GB/s vs peak; store tokens/s"
+UNIT = "KV tokens/s"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--split-blocks", type=int, default=0, help="KV blocks per decode split (0: per workload)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-store-workload", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "turboquant_bit_kv_tq_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)
+        e = rec.get(f"{kernel}:{workload}")
+        if e and e.get("source_hash") == _kernel_source_hash():
+            return e.get("dram_bytes_per_launch_scaled", e.get("dram_bytes_per_launch"))
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ CPU baseline
+_CPU_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle import paged
+from turboquant_bit_kv_tq_gb300 import workloads as wl
+w = wl.config({name!r})
+cap = {cap}
+P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl)
+n = min(w.compressed_lens()[0], cap)
+nb = (n + 15) // 16
+cache = np.zeros((nb, w.kv_heads, P.layout.page_bytes), np.uint8)
+K, V = wl.kv_tokens(w, 0, 0, n)
+t = np.arange(n)
+paged.store(cache, P, K[:-1], V[:-1], t[:-1])
+Q = wl.queries(w, 1).astype(np.float64)
+tail = min(w.tail, w.seq_lens[0]) if w.tail else 0
+kw = {{}}
+if tail:
+    tk, tv = wl.kv_tokens(w, 0, w.compressed_lens()[0], tail)
+    kw = dict(tail_k=tk.transpose(1, 0, 2)[None], tail_v=tv.transpose(1, 0, 2)[None], tail_lens=[tail])
+steps, t0 = 0, time.perf_counter()
+while True:
+    paged.store(cache, P, K[-1:], V[-1:], t[-1:])           # the step's new token
+    paged.decode_attention(cache, P, Q, np.arange(nb)[None], [n], **kw)
+    steps += 1
+    el = time.perf_counter() - t0
+    if el >= {seconds} or steps >= {max_steps}:
+        break
+print(json.dumps(dict(steps=steps, seconds=el, tokens=(n + tail) * steps, seq_tokens=n + tail)))
+"""
+
+
+def cpu_oracle_run(name, seconds, max_steps=10**6, cap=8192):
+    """Time the oracle (single thread, spawned process) on one sequence of the
+    workload (its first `cap` compressed tokens + tail, all heads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = _CPU_SNIPPET.format(root=ROOT, name=name, cap=cap, seconds=seconds, max_steps=max_steps)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["value"] = res["tokens"] / res["seconds"]
+    res["cores"] = 1
+    res["sample"] = (f"oracle (numpy fp64, 1 thread) on sequence 0 of {name}: first {res['seq_tokens']} tokens "
+                     f"(compressed + tail), all {wl_heads(name)} query heads, store of the step's new token + "
+                     f"decode, {res['steps']} steps in {res['seconds']:.1f} s")
+    return res
+
+
+def wl_heads(name):
+    from turboquant_bit_kv_tq_gb300 import workloads as wl
+
+    return wl.config(name).q_heads
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from turboquant_bit_kv_tq_gb300 import workloads as wl
+
+    w = wl.config(args.workload)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    cpu_oracle_run(args.workload, per_step, max_steps=max(1, args.warmup))  # warm-up steps
+    res = cpu_oracle_run(args.workload, per_step * args.steps, max_steps=args.steps)
+    ms = 1e3 * res["seconds"] / res["steps"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": args.gpus,
+        "steps": res["steps"], "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": res["sample"]},
+        "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"]},
+        "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- our arm
+def _setup_decode(w, split_blocks, torch, tq, wl, device):
+    import numpy as np
+
+    table, num_blocks = wl.block_table(w)
+    comp = w.compressed_lens()
+    kw = wl.cache_config_kwargs(w, num_blocks=num_blocks, max_blocks=table.shape[1], split_blocks=split_blocks)
+    c = tq.TQCache(device=device, **kw)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    for b in range(w.batch):
+        for s0 in range(0, comp[b], 65536):
+            n = min(65536, comp[b] - s0)
+            t = np.arange(s0, s0 + n)
+            slots = torch.from_numpy(table[b, t // 16].astype(np.int64) * 16 + t % 16).to(device)
+            K, V = wl.kv_tokens_device(w, n, gen, device)
+            c.store(K, V, slots)
+    torch.cuda.synchronize()
+    if c.device_error():
+        raise RuntimeError("device error while filling the cache")
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    st = dict(
+        q=torch.from_numpy(wl.queries(w)).to(device, dt),
+        table=torch.from_numpy(table).to(device),
+        lens=torch.tensor(comp, dtype=torch.int32, device=device),
+        out=torch.empty((w.batch, w.q_heads, w.d), dtype=torch.bfloat16, device=device),
+    )
+    # the step's new token per sequence overwrites the newest compressed slot,
+    # so the context length stays fixed from step to step
+    last = [max(0, n - 1) for n in comp]
+    st["new_slots"] = torch.tensor([int(table[b, p // 16]) * 16 + p % 16 if comp[b] else -1
+                                    for b, p in enumerate(last)], dtype=torch.int64, device=device)
+    K, V = wl.kv_tokens_device(w, w.batch, gen, device)
+    st["new_k"], st["new_v"] = K, V
+    if w.tail:
+        tl = w.tail_lens()
+        st["tail_k"] = (torch.randn((w.batch, w.kv_heads, w.tail, w.d), generator=gen, device=device)).to(
+            torch.bfloat16)
+        st["tail_v"] = (torch.randn((w.batch, w.kv_heads, w.tail, w.d), generator=gen, device=device)).to(
+            torch.bfloat16)
+        st["tail_lens"] = torch.tensor(tl, dtype=torch.int32, device=device)
+    return c, st, table
+
+
+def _step(c, st, stream):
+    c.store(st["new_k"], st["new_v"], st["new_slots"], stream=stream)
+    c.decode(st["q"], st["table"], st["lens"], out=st["out"], tail_k=st.get("tail_k"), tail_v=st.get("tail_v"),
+             tail_lens=st.get("tail_lens"), stream=stream)
+
+
+def _events(torch, n, stream):
+    """n timing-event pairs, each recorded once so that its CUDA handle exists
+    before the library is given it."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in ev:
+        a.record(stream)
+        b.record(stream)
+    return ev
+
+
+def _time_steps(torch, tq, c, st, stream, steps, flush, split_events=True):
+    """Per-step CUDA events on `stream`, L2 flushed between steps (outside the
+    events).  Returns (step_ms list, split_ms list)."""
+    ev = _events(torch, steps, stream)
+    sev = _events(torch, steps, stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            if split_events:
+                tq.tq_set_profile_events(c.handle, tq.TQ_PROF_DECODE_SPLIT, sev[i][0], sev[i][1])
+            ev[i][0].record(stream)
+            _step(c, st, stream)
+            ev[i][1].record(stream)
+    tq.tq_set_profile_events(c.handle, tq.TQ_PROF_DECODE_SPLIT, None, None)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    split_ms = [a.elapsed_time(b) for a, b in sev] if split_events else []
+    return step_ms, split_ms
+
+
+def _e2e(torch, c, st, w, stream, steps, warmup, flush):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in, result copied out, inside the timed region."""
+    names = ["q", "new_k", "new_v", "new_slots", "lens", "table"] + (["tail_lens"] if w.tail else [])
+    host = {k: st[k].cpu().pin_memory() for k in names}
+    out_h = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+    dev = {k: torch.empty_like(st[k]) for k in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    st2 = dict(st)
+    st2.update(dev)
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            flush.zero_()
+            if i >= warmup:
+                ev[i - warmup][0].record(stream)
+            for k in names:
+                dev[k].copy_(host[k], non_blocking=True)
+            _step(c, st2, stream)
+            out_h.copy_(st2["out"], non_blocking=True)
+            if i >= warmup:
+                ev[i - warmup][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, h2d, d2h
+
+
+def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak):
+    """Store throughput on the 65,536-token scattered append (context line)."""
+    w = wl.config("store_64seq_65536tok")
+    lens, prior, table, slots = wl.store_layout(w)
+    c = tq.TQCache(device=device, **wl.cache_config_kwargs(w, num_blocks=w.pool_blocks, max_blocks=4, max_batch=1))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    K, V = wl.kv_tokens_device(w, w.store_tokens, gen, device)
+    s = torch.from_numpy(slots).to(device)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        c.store(K, V, s)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        c.store(K, V, s)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    read = K.numel() * 2 * 2 + s.numel() * 8
+    written = w.store_tokens * w.kv_heads * c.page_bytes // 16
+    gbs = (read + written) / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "tokens_per_s": w.store_tokens / (ms * 1e-3), "ms": ms,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "algorithmic_bytes": read + written,
+            "launches": steps}
+
+
+def run_ours(args):
+    import torch
+
+    import turboquant_bit_kv_tq_gb300 as tq
+    from turboquant_bit_kv_tq_gb300 import workloads as wl
+
+    ws, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    tq.load_library()
+    w = wl.config(args.workload)
+    split_blocks = args.split_blocks or (64 if max(w.seq_lens) > 16384 else 32)
+    c, st, table = _setup_decode(w, split_blocks, torch, tq, wl, device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device=device)
+    peak, peak_kind = _peaks()
+
+    # warm-up, then the timed steps (barrier + sync on both sides)
+    _time_steps(torch, tq, c, st, stream, max(3, args.warmup), flush, split_events=False)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms, split_ms = _time_steps(torch, tq, c, st, stream, args.steps, flush)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    if c.device_error():
+        raise RuntimeError("device error during the timed steps")
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    attended = sum(w.compressed_lens()) + sum(w.tail_lens())
+    value = ws * attended / (ms * 1e-3)
+    # algorithmic bytes of the split-KV kernel: the compressed bytes of every
+    # attended token-head, the block-table entries and the exact tail K/V
+    per_token_head = c.page_bytes // 16
+    token_heads = sum(w.compressed_lens()) * w.kv_heads
+    blocks = sum((n + 15) // 16 for n in w.compressed_lens())
+    tail_bytes = sum(w.tail_lens()) * w.kv_heads * w.d * 2 * 2
+    split_bytes = token_heads * per_token_head + blocks * 4 + tail_bytes
+    split_avg = statistics.mean(split_ms)
+    achieved = split_bytes / (split_avg * 1e-3) / 1e9
+    # whole-step algorithmic bytes: decode's bytes + q read + out written +
+    # the store's bf16 read and packed write
+    step_bytes = (split_bytes + w.batch * w.q_heads * w.d * (2 + 2) +
+                  w.batch * w.kv_heads * w.d * 2 * 2 + w.batch * w.kv_heads * per_token_head)
+
+    e2e_ms, h2d, d2h = _e2e(torch, c, st, w, stream, args.steps, max(3, args.warmup), flush)
+    e2e_ms_max = e2e_ms
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms_max = float(t.item())
+
+    store_line = None
+    if not args.no_store_workload and rank == 0:
+        store_line = _store_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush, peak)
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            try:
+                r = cpu_oracle_run(args.workload, args.cpu_seconds)
+                cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+            except Exception as e:  # reported, not fatal
+                cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"[:300]}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
+                       "head_dim": w.d, "context_lens": sorted(set(w.seq_lens)), "tail": w.tail,
+                       "k_bits": w.k_bits, "k_qjl": w.k_qjl, "v_mode": w.v_mode, "v_bits": w.v_bits,
+                       "split_blocks": split_blocks, "out_dtype": "bf16",
+                       "l2": "flushed: 256 MiB buffer written between timed steps (outside the events)",
+                       "step": "tq_store of each sequence's new token + tq_decode_attention"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": _ncu_traffic("split_kernel", w.name),
+                         "kernel": "tq::split_kernel (decode split-KV)", "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": split_bytes, "bytes_per_token_head": per_token_head,
+                         "units_per_launch": token_heads, "avg_launch_ms": split_avg,
+                         "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9},
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+            "e2e": {"value": ws * attended / (e2e_ms_max * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+            "gpu_launches": 4 * args.steps,
+            "store_workload": store_line,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,89 @@
+"""CPU checks of the C-ABI library: it loads, exports every function
+include/tq_kv.h declares, and its host-side tables (codebooks, rotation signs,
+QJL matrix, page sizes) equal the oracle's independently generated ones.  No
+compute call needs a GPU here."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import turboquant_bit_kv_tq_gb300 as tq
+from oracle import codebook, paged, prng
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(tq.library_path()):
+        from turboquant_bit_kv_tq_gb300 import _build
+
+        _build.build()
+    tq.load_library()
+
+
+def test_header_functions_all_exported():
+    with open(os.path.join(ROOT, "include", "tq_kv.h")) as f:
+        text = f.read()
+    declared = sorted(set(re.findall(r"^\s*(?:tq_status|const char\*)\s+(tq_\w+)\s*\(", text, re.M)))
+    assert declared == sorted(tq.EXPORTED)
+    lib = tq.load_library()
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert tq.tq_status_string(0) == "ok"
+    for s in (-1, -2, -3, -4, -5):
+        assert tq.tq_status_string(s) != "unknown status"
+
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_codebook_matches_oracle(d, bits):
+    c, b, mse = tq.tq_make_codebook(d, bits)
+    oc, ob = codebook.sphere_codebook(d, bits)
+    assert np.max(np.abs(c - oc)) < 1e-11
+    assert np.max(np.abs(b - ob)) < 1e-11
+    # the fp32 tables the kernels use are then identical
+    assert np.array_equal(c.astype(np.float32), oc.astype(np.float32))
+    assert np.array_equal(b.astype(np.float32), ob.astype(np.float32))
+    assert abs(mse - codebook.per_vector_mse(d, oc)) < 1e-10
+
+
+@pytest.mark.parametrize("d,seed", [(128, 2), (256, 2), (128, 12345)])
+def test_rotation_signs_match_oracle(d, seed):
+    assert np.array_equal(tq.tq_make_rotation_signs(d, seed), prng.rotation_signs(d, seed).astype(np.float32))
+
+
+@pytest.mark.parametrize("d,seed", [(128, 1), (256, 1), (128, 99)])
+def test_qjl_matrix_matches_oracle(d, seed):
+    bits = tq.tq_make_qjl_matrix(d, seed).astype(np.uint32) << 16
+    lib_vals = bits.view(np.float32).astype(np.float64)
+    assert np.array_equal(lib_vals, prng.qjl_matrix(d, seed))
+
+
+@pytest.mark.parametrize("d,kb,vm,vb", [(128, 2, 0, 2), (128, 3, 1, 4), (256, 2, 0, 2), (128, 4, 1, 2),
+                                        (256, 3, 1, 3)])
+def test_page_bytes_match_oracle_layout(d, kb, vm, vb):
+    cfg = tq.tq_cache_config(head_dim=d, num_kv_heads=8, num_q_heads=32, num_blocks=10, k_bits=kb, v_mode=vm,
+                             v_bits=vb, max_blocks_per_seq=4)
+    sizes = tq.tq_cache_sizes(cfg)
+    lay = paged.PageLayout(d, kb, True, "mse" if vm == 0 else "g32", vb)
+    assert sizes["page_bytes"] == lay.page_bytes
+    assert sizes["cache_bytes"] == 10 * 8 * lay.page_bytes
+    assert sizes["page_bytes"] % 16 == 0
+
+
+def test_bad_configs_are_rejected_on_the_host():
+    ok = dict(head_dim=128, num_kv_heads=8, num_q_heads=32, num_blocks=10, k_bits=3, v_mode=1, v_bits=4,
+              max_blocks_per_seq=4)
+    tq.tq_cache_sizes(tq.tq_cache_config(**ok))
+    for bad, status in [(dict(head_dim=64), -2), (dict(k_bits=5), -2), (dict(v_bits=1), -2), (dict(block_size=32), -2),
+                        (dict(num_q_heads=30), -1), (dict(num_blocks=0), -1), (dict(v_mode=7), -2),
+                        (dict(split_blocks=0), -1), (dict(tail_cap=-1), -1)]:
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_cache_sizes(tq.tq_cache_config(**{**ok, **bad}))
+        assert e.value.status == status, bad

@@ -1,0 +1,74 @@
+// Private to the library: the cache handle, page layout and the kernel
+// launchers shared between tq_host.cpp, tq_store.cu and tq_decode.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "tq_kv.h"
+
+namespace tq {
+
+constexpr int kBlock = 16;  // tokens per cache block
+constexpr int kMaxLevels = 16;
+
+// Byte offsets of the planes of one (block, KV head) page; see tq_kv.h.
+struct Layout {
+    int d, k_bits, v_bits, k_qjl, v_mode;
+    int k_code_row, k_sign_row, v_code_row, v_meta_row;  // bytes per token row
+    int k_codes, k_signs, k_norm, k_rnorm, v_codes, v_meta;  // plane offsets
+    int page_bytes;
+};
+
+// Device pointers into the caller's params buffer.
+struct DeviceParams {
+    const float* signs;      // [d] +-1
+    const float* s_f32;      // S row-major [d][d]
+    const float* st_f32;     // S^T [d][d] (st[i*d + j] = S[j][i])
+    const uint16_t* s_bf16;  // S row-major, bf16 bits
+    const float* k_cent;     // [16] key centroids (padded)
+    const float* k_bound;    // [16] key boundaries
+    const float* v_cent;     // [16] value centroids (MSE)
+    const float* v_bound;    // [16]
+    uint32_t* err;           // device error word
+};
+
+// Split-KV geometry of a configuration.
+struct Splits {
+    int n_chunks;  // ceil(max_blocks_per_seq / split_blocks)
+    int n_splits;  // n_chunks + (tail_cap > 0)
+};
+
+struct ParamsLayout {
+    size_t signs, s_f32, st_f32, s_bf16, k_cent, k_bound, v_cent, v_bound, err, total;
+};
+
+struct WorkspaceLayout {
+    size_t q, acc, ml, total;  // q: [B][Hq][3][d]; acc: [B][Hq][S][d]; ml: [B][Hq][S][2]
+};
+
+tq_status compute_layout(const tq_cache_config& c, Layout* lay);
+Splits compute_splits(const tq_cache_config& c);
+ParamsLayout params_layout(const tq_cache_config& c);
+WorkspaceLayout workspace_layout(const tq_cache_config& c);
+
+}  // namespace tq
+
+struct tq_cache {
+    tq_cache_config cfg;
+    tq::Layout lay;
+    tq::Splits splits;
+    tq::DeviceParams dp;
+    float* ws_q;
+    float* ws_acc;
+    float* ws_ml;
+    // profiling events (cudaEvent_t) around the store / decode-split kernels
+    void* prof_start[2] = {nullptr, nullptr};
+    void* prof_stop[2] = {nullptr, nullptr};
+    // host copies of the tables
+    std::vector<float> signs;
+    std::vector<uint16_t> s_bf16;
+    std::vector<double> k_cent, k_bound, v_cent, v_bound;
+};

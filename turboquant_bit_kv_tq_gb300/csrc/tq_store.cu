@@ -1,0 +1,250 @@
+// Fused TurboQuant KV-cache store: norm, rotation, Lloyd-Max codes, key
+// residual + QJL signs, value codes, bit packing and the scattered write into
+// the paged cache, in one launch ([Roadmap] §3.1 "rotation fused into the
+// quantise kernel"; [Paged] "Which path vLLM takes": the store kernel
+// quantises, packs and writes the paged KV cache).
+//
+// One warp encodes one (token, KV head) vector at a time; lane l holds
+// coordinates l + 32k.  The QJL projection S r runs on CUDA cores from a
+// shared-memory copy of S^T.
+
+#include <algorithm>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+struct StoreArgs {
+    const void* k;
+    const void* v;
+    const int64_t* slots;
+    uint8_t* cache;
+    int64_t num_tokens;
+    int64_t num_slots;  // num_blocks * 16
+    int heads;
+    Layout lay;
+    DeviceParams dp;
+};
+
+// Pack codes[0..d) (one byte each, b bits used) into the row's LSB-first
+// bitstream; lanes write whole 32-bit words.
+__device__ __forceinline__ void pack_row(const uint8_t* codes, int d, int b, uint8_t* dst, int lane) {
+    const int words = d * b / 32;
+    for (int w = lane; w < words; w += 32) {
+        const int bit0 = w * 32;
+        uint32_t word = 0;
+        for (int i = bit0 / b; i * b < bit0 + 32; ++i) {
+            const int sh = i * b - bit0;
+            const uint32_t c = codes[i];
+            word |= sh >= 0 ? (c << sh) : (c >> -sh);
+        }
+        reinterpret_cast<uint32_t*>(dst)[w] = word;
+    }
+}
+
+// TurboQuant-MSE code of one vector ([Explainer] steps 1-2): returns the fp32
+// norm; idx[k] is the code of coordinate lane + 32k.
+template <int D>
+__device__ __forceinline__ float mse_codes(const float (&v)[D / 32], const float* signs, const float* bound, int nb,
+                                           int lane, int (&idx)[D / 32]) {
+    constexpr int PER = D / 32;
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) ss = fmaf(v[k], v[k], ss);
+    const float n = sqrtf(warp_sum(ss));
+    float y[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) y[k] = v[k] * signs[lane + 32 * k];
+    fwht_warp<PER>(y, lane);
+    // y = H D v / (n sqrt(d)); a zero vector maps to y = 0
+    const float inv = n > 0.f ? rsqrtf((float)D) / n : 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const float yk = y[k] * inv;
+        int c = 0;
+        for (int j = 0; j < nb; ++j) c += yk > bound[j];
+        idx[k] = c;
+    }
+    return n;
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
+    constexpr int PER = D / 32;
+    constexpr int kWarps = 8;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t* st = reinterpret_cast<uint16_t*>(smem);                    // S^T, bf16 [D][D]
+    float* rbuf = reinterpret_cast<float*>(smem + D * D * 2);            // [warps][D]
+    uint8_t* codes = smem + D * D * 2 + kWarps * D * 4;                  // [warps][D]
+    float* tables = reinterpret_cast<float*>(codes + kWarps * D);        // signs, k/v cent, k/v bound
+    float* s_signs = tables;
+    float* s_kc = tables + D;
+    float* s_kb = s_kc + kMaxLevels;
+    float* s_vc = s_kb + kMaxLevels;
+    float* s_vb = s_vc + kMaxLevels;
+
+    const Layout& L = a.lay;
+    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+        const int j = e / D, i = e % D;
+        st[i * D + j] = a.dp.s_bf16[e];
+    }
+    for (int e = threadIdx.x; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
+    for (int e = threadIdx.x; e < kMaxLevels; e += blockDim.x) {
+        s_kc[e] = a.dp.k_cent[e];
+        s_kb[e] = a.dp.k_bound[e];
+        s_vc[e] = a.dp.v_cent[e];
+        s_vb[e] = a.dp.v_bound[e];
+    }
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* r = rbuf + warp * D;
+    uint8_t* cw = codes + warp * D;
+    const float rsd = rsqrtf((float)D);
+    const int64_t nvec = a.num_tokens * a.heads;
+    for (int64_t w = (int64_t)blockIdx.x * kWarps + warp; w < nvec; w += (int64_t)gridDim.x * kWarps) {
+        const int64_t t = w / a.heads;
+        const int h = (int)(w - t * a.heads);
+        const int64_t slot = a.slots[t];
+        if (slot < 0 || slot >= a.num_slots) {
+            if (slot != -1 && lane == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
+            continue;
+        }
+        const int row = (int)(slot & 15);
+        uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
+        const Tin* kin = static_cast<const Tin*>(a.k) + w * D;
+        const Tin* vin = static_cast<const Tin*>(a.v) + w * D;
+
+        // ------------------------------------------------------------ key
+        float x[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) x[k] = load_as_float(kin + lane + 32 * k);
+        int idx[PER];
+        const float n = mse_codes<D>(x, s_signs, s_kb, (1 << L.k_bits) - 1, lane, idx);
+        const __half n16 = __float2half_rn(n);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) cw[lane + 32 * k] = (uint8_t)idx[k];
+        __syncwarp();
+        pack_row(cw, D, L.k_bits, page + L.k_codes + row * L.k_code_row, lane);
+        if (lane == 0) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
+        if (L.k_qjl) {
+            // residual r = k - n16 R^T c[idx], with R^T c = D H c / sqrt(d)
+            float c[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) c[k] = s_kc[idx[k]];
+            fwht_warp<PER>(c, lane);
+            const float n16f = __half2float(n16);
+            float rr = 0.f;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = lane + 32 * k;
+                const float res = x[k] - n16f * (c[k] * s_signs[i] * rsd);
+                r[i] = res;
+                rr = fmaf(res, res, rr);
+            }
+            const float rho = sqrtf(warp_sum(rr));
+            __syncwarp();
+            // z_j = sum_i S[j][i] r_i for j = lane + 32k; bit j = [z_j >= 0]
+            float z[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) z[k] = 0.f;
+            for (int i = 0; i < D; ++i) {
+                const float ri = r[i];
+#pragma unroll
+                for (int k = 0; k < PER; ++k) z[k] = fmaf(bf16_bits_to_float(st[i * D + lane + 32 * k]), ri, z[k]);
+            }
+            uint32_t* srow = reinterpret_cast<uint32_t*>(page + L.k_signs + row * L.k_sign_row);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const uint32_t word = __ballot_sync(0xffffffffu, z[k] >= 0.f);
+                if (lane == k) srow[k] = word;
+            }
+            if (lane == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho);
+        }
+        __syncwarp();
+
+        // ---------------------------------------------------------- value
+#pragma unroll
+        for (int k = 0; k < PER; ++k) x[k] = load_as_float(vin + lane + 32 * k);
+        if (L.v_mode == TQ_V_MSE) {
+            const float vn = mse_codes<D>(x, s_signs, s_vb, (1 << L.v_bits) - 1, lane, idx);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) cw[lane + 32 * k] = (uint8_t)idx[k];
+            if (lane == 0) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(vn);
+        } else {
+            // group g = coordinates [32g, 32g+32) = slot k of every lane
+            const int top = (1 << L.v_bits) - 1;
+            uint32_t* meta = reinterpret_cast<uint32_t*>(page + L.v_meta + row * L.v_meta_row);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const float lo = warp_min(x[k]), hi = warp_max(x[k]);
+                const __half z16 = __float2half_rn(lo);
+                const __half s16 = __float2half_rn((hi - lo) / (float)top);
+                const float zf = __half2float(z16), sf = __half2float(s16);
+                int q = 0;
+                if (sf > 0.f) {
+                    const float tq = (x[k] - zf) / sf;
+                    const float fl = floorf(tq);
+                    q = (int)fl + ((tq - fl) >= 0.5f ? 1 : 0);
+                    q = min(max(q, 0), top);
+                }
+                cw[lane + 32 * k] = (uint8_t)q;
+                if (lane == k)
+                    meta[k] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+            }
+        }
+        __syncwarp();
+        pack_row(cw, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
+        __syncwarp();
+    }
+}
+
+template <int D, typename Tin>
+static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1) {
+    const size_t smem = (size_t)D * D * 2 + 8 * D * 4 + 8 * D + (D + 4 * kMaxLevels) * 4;
+    auto kern = store_kernel<D, Tin>;
+    // one-time setup per kernel instance (before any stream capture)
+    static int sms = 0;
+    if (sms == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return TQ_ERR_CUDA;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int64_t want = (a.num_tokens * a.heads + 7) / 8;
+    const int grid = (int)std::min<int64_t>(want, (int64_t)sms * (D == 128 ? 4 : 1));
+    if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
+    kern<<<grid, 256, smem, s>>>(a);
+    if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" tq_status tq_store(const tq_cache* c, const void* k, const void* v, int in_dtype, int64_t num_tokens,
+                              const int64_t* slot_mapping, void* cache_buf, void* stream) {
+    if (!c || num_tokens < 0) return TQ_ERR_INVALID_ARG;
+    if (num_tokens == 0) return TQ_OK;
+    if (!k || !v || !slot_mapping || !cache_buf) return TQ_ERR_INVALID_ARG;
+    if (in_dtype != TQ_DTYPE_F32 && in_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+    if (((uintptr_t)cache_buf & 15) || ((uintptr_t)k & 3) || ((uintptr_t)v & 3)) return TQ_ERR_MISALIGNED;
+    StoreArgs a;
+    a.k = k;
+    a.v = v;
+    a.slots = slot_mapping;
+    a.cache = static_cast<uint8_t*>(cache_buf);
+    a.num_tokens = num_tokens;
+    a.num_slots = c->cfg.num_blocks * kBlock;
+    a.heads = c->cfg.num_kv_heads;
+    a.lay = c->lay;
+    a.dp = c->dp;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int d = c->cfg.head_dim;
+    void *e0 = c->prof_start[TQ_PROF_STORE], *e1 = c->prof_stop[TQ_PROF_STORE];
+    if (in_dtype == TQ_DTYPE_F32)
+        return d == 128 ? launch<128, float>(a, s, e0, e1) : launch<256, float>(a, s, e0, e1);
+    return d == 128 ? launch<128, __nv_bfloat16>(a, s, e0, e1) : launch<256, __nv_bfloat16>(a, s, e0, e1);
+}
