@@ -396,3 +396,12 @@ def test_decode_extreme_logits_reach_the_one_hot_limit():
     s = quant.key_scores(Q[0, 0], f["k_n16"], f["k_idx"], f["k_rho16"], f["k_bits"], P.R, P.k_centroids, P.S)
     v_hat = quant.group32_reconstruct(f["v_s16"], f["v_z16"], f["v_codes"])
     assert np.max(np.abs(out[0, 0] - v_hat[np.argmax(s)])) < 1e-9
+
+
+def test_store_with_no_tokens_is_a_noop():
+    P = paged.CacheParams(128, 3, True, "g32", 4, 2, 1)
+    cache = np.zeros((2, 8, P.layout.page_bytes), np.uint8)
+    empty = np.zeros((0, 8, 128))
+    paged.store(cache, P, empty, empty, np.zeros(0, np.int64))
+    paged.store(cache, P, np.ones((3, 8, 128)), np.ones((3, 8, 128)), np.full(3, -1))
+    assert not cache.any()
