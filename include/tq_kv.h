@@ -33,21 +33,27 @@
  *     set a bit in a device error word read by tq_get_device_error; kernels
  *     never trap.
  *
- * Page layout (a reading: the pages fix only "2-bit codes pack four per byte,
- * 4-bit codes two per byte", [Hub] step 5).  cache = uint8
+ * Page layout (a reading: the pages fix only the packing density, 2-bit codes
+ * a quarter byte and 4-bit codes half a byte, [Hub] step 5).  cache = uint8
  * [num_blocks][num_kv_heads][page_bytes]; a page holds the 16 token rows of one
- * block for one KV head, as consecutive planes of 16 rows each:
- *   K codes   16 x (d*k_bits/8) bytes  LSB-first bitstream per row: coordinate i
- *                                      at stream bits [i*b, (i+1)*b); stream
- *                                      bit m = bit (m%8) of byte m/8
- *   K signs   16 x (d/8)               (k_qjl) QJL sign j = bit j of the row
- *   K norm    16 x fp16                ||k|| rounded to fp16
- *   K rnorm   16 x fp16                (k_qjl) ||residual|| rounded to fp16
- *   V codes   16 x (d*v_bits/8)        same bitstream rule
- *   V meta    16 x fp16 norm           (TQ_V_MSE)
- *          or 16 x (d/32) x {fp16 scale, fp16 zero}   (TQ_V_G32)
+ * block for one KV head.  Bit c of a d-bit row is bit c%8 of byte c/8.  Planes,
+ * each of 16 rows, in this order:
+ *   K code planes  k_bits x 16 x (d/8)  bit-sliced: plane p, bit c of row r =
+ *                                       bit p of the code of coordinate c
+ *   K signs        16 x (d/8)           (k_qjl) bit c = [(S r)_c >= 0]
+ *   K norm         16 x fp16            ||k|| rounded to fp16
+ *   K rnorm        16 x fp16            (k_qjl) ||residual|| rounded to fp16
+ *   V codes   MSE: v_bits x 16 x (d/8)  bit-sliced like the keys
+ *             G32: 16 x (d*v_bits/8)    v_bits-bit fields, LSB-first; field
+ *                                       slot k = (d/8)*g + 2*m + e (g < 8,
+ *                                       m < d/16, e < 2) holds coordinate
+ *                                       32*(m/2) + 4*g + 2*(m%2) + e
+ *   V meta    MSE: 16 x fp16 norm
+ *             G32: 16 x (d/32) x {fp16 scale, fp16 zero}  (natural group order)
  * Every plane size is a multiple of 16 bytes.  Token t of sequence b is
  * stored in block block_table[b][t/16] at row t%16 (slot = block*16 + row).
+ * The bit order lets the decode build tensor-core operands from stored words
+ * with one logic operation per register.
  */
 #ifndef TQ_KV_H
 #define TQ_KV_H
@@ -63,7 +69,8 @@ typedef int tq_status;
 enum {
     TQ_OK = 0,
     TQ_ERR_INVALID_ARG = -1,      /* null pointer, size out of range, inconsistent config */
-    TQ_ERR_UNSUPPORTED = -2,      /* d not in {128,256}, bits not in {2,3,4}, block size != 16 */
+    TQ_ERR_UNSUPPORTED = -2,      /* d not in {128,256}, bits not in {2,3,4} (group-32: {2,4}),
+                                     block != 16, H_q/H_kv > 4 and not a multiple of 4 (or > 16) */
     TQ_ERR_BUFFER_TOO_SMALL = -3, /* a caller buffer is smaller than tq_cache_sizes says */
     TQ_ERR_CUDA = -4,             /* a CUDA runtime call failed (launch, copy) */
     TQ_ERR_MISALIGNED = -5        /* a device pointer is not 16-byte aligned */
@@ -77,19 +84,21 @@ enum {
     TQ_DEVERR_SLOT = 1u << 0,      /* store: slot >= num_blocks*16 or < -1; token skipped */
     TQ_DEVERR_BLOCK = 1u << 1,     /* decode: block id outside [0, num_blocks); block skipped */
     TQ_DEVERR_SEQLEN = 1u << 2,    /* decode: seq_len < 0 or > 16*max_blocks_per_seq; clamped */
-    TQ_DEVERR_TAIL = 1u << 3       /* decode: tail_len < 0 or > tail_cap; clamped */
+    TQ_DEVERR_TAIL = 1u << 3,      /* decode: tail_len < 0 or > tail_cap; clamped */
+    TQ_DEVERR_TIMEOUT = 1u << 4    /* decode: a bounded wait for a staged page gave up; split abandoned */
 };
 
 typedef struct tq_cache_config {
     int32_t head_dim;           /* d, 128 or 256 ([Hub] step 2: codebooks for 128 and 256) */
     int32_t num_kv_heads;       /* H_kv >= 1 */
-    int32_t num_q_heads;        /* H_q, a multiple of H_kv; q head h reads KV head h / (H_q/H_kv) */
+    int32_t num_q_heads;        /* H_q = G * H_kv with G <= 4 or G in {8, 12, 16}; q head h reads
+                                   KV head h / G */
     int32_t block_size;         /* tokens per cache block; must be 16 */
     int64_t num_blocks;         /* blocks in the cache pool */
     int32_t k_bits;             /* key code bits, 2..4 */
     int32_t k_qjl;              /* 1: keys also keep ||r|| and sign(S r) ([Roadmap] §1); 0: MSE only */
     int32_t v_mode;             /* TQ_V_MSE (rotate + codebook) or TQ_V_G32 (uniform group-32) */
-    int32_t v_bits;             /* value code bits, 2..4 */
+    int32_t v_bits;             /* value code bits: 2..4 (MSE), 2 or 4 (group-32) */
     uint64_t seed_rot;          /* seed of the rotation's +-1 diagonal */
     uint64_t seed_qjl;          /* seed of the d x d Gaussian QJL matrix S */
     int32_t max_batch;          /* sequences per decode call (grid size) */

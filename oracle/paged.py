@@ -3,23 +3,31 @@
 [Paged] "Which path vLLM takes": new K/V vectors are quantised, packed and
 written into a paged KV cache (fixed-size blocks found through a block table);
 decode reads the compressed blocks through the block table, decodes them and
-runs attention.  [Hub] step 5 fixes only that 2-bit codes pack 4 per byte and
-4-bit codes 2 per byte.
+runs attention.  [Hub] step 5 fixes only the packing density: 2-bit codes take
+a quarter byte each and 4-bit codes half a byte.
 
-Layout reading (parity unpinned -- the pages fix none of it):
+Layout reading (parity unpinned -- the pages fix none of it; chosen so that a
+tensor-core decode can turn stored bits into matrix operands with one logic
+operation per register):
   * cache = uint8 [num_blocks, num_kv_heads, page_bytes]; a page holds the 16
     tokens of one block for one KV head; token t of a sequence lives in block
     block_table[b][t // 16] at row t % 16 (slot = block * 16 + row).
-  * a page is a run of planes, each plane 16 token rows:
-      K codes   16 x (d*kb/8)     LSB-first bitstream per row: coordinate i
-                                   occupies stream bits [i*kb, (i+1)*kb), stream
-                                   bit m is bit (m % 8) of byte m // 8
-      K signs   16 x (d/8)        (keys with QJL) bit j of the row = sign bit j
-      K norm    16 x fp16         n16, little-endian
-      K rnorm   16 x fp16         rho16 (keys with QJL)
-      V codes   16 x (d*vb/8)     same bitstream rule
-      V norm    16 x fp16         (TurboQuant-MSE values)
-   or V scale/zero 16 x (d/32) x (fp16 scale, fp16 zero)  (group-32 values)
+  * bit c of a d-bit row is bit (c % 8) of byte c // 8 (LSB first).
+  * a page is a run of planes, each of 16 token rows:
+      K code planes  kb x 16 x (d/8)  bit-sliced: plane p, bit c of row r is
+                                      bit p of the key code of coordinate c
+      K signs        16 x (d/8)       (keys with QJL) bit c = [(S r)_c >= 0]
+      K norm         16 x fp16        n16, little-endian
+      K rnorm        16 x fp16        rho16 (keys with QJL)
+      V codes  MSE:  vb x 16 x (d/8)  bit-sliced like the keys
+              G32:   16 x (d*vb/8)    vb-bit fields, LSB-first: field slot k
+                                      holds the code of coordinate tau(k)
+      V meta   MSE:  16 x fp16        value norm
+              G32:   16 x (d/32) x (fp16 scale, fp16 zero)   (natural groups)
+  * tau (group-32 slots): with w = d/8, slot k = w*g + 2*m + e
+    (0 <= g < 8, 0 <= m < d/16, e in {0, 1}) holds coordinate
+    32*(m // 2) + 4*g + 2*(m % 2) + e.  The 16 slots (w*g + 2m + e) for fixed
+    m all lie in group m // 2, and the two slots of a pair are neighbours.
 """
 
 import numpy as np
@@ -29,30 +37,55 @@ from . import quant
 BLOCK = 16
 
 
+def group32_slot_coordinates(d):
+    """tau: coordinate held by each group-32 field slot (array of length d)."""
+    w = d // 8
+    k = np.arange(d)
+    g, rest = k // w, k % w
+    m, e = rest // 2, rest % 2
+    return 32 * (m // 2) + 4 * g + 2 * (m % 2) + e
+
+
 class PageLayout:
     """Byte offsets of the planes of one (block, KV head) page."""
 
     def __init__(self, d, k_bits, k_qjl, v_mode, v_bits):
         assert v_mode in ("mse", "g32")
+        assert v_mode == "mse" or v_bits in (2, 4)
         self.d, self.k_bits, self.k_qjl, self.v_mode, self.v_bits = d, k_bits, bool(k_qjl), v_mode, v_bits
-        self.k_code_row = d * k_bits // 8
-        self.k_sign_row = d // 8
-        self.v_code_row = d * v_bits // 8
+        self.bit_row = d // 8                      # one bit per coordinate
+        self.v_code_row = d * v_bits // 8          # group-32 bitstream row
         self.v_meta_row = 2 if v_mode == "mse" else 4 * (d // 32)
         off = 0
         self.k_codes = off
-        off += BLOCK * self.k_code_row
+        off += k_bits * BLOCK * self.bit_row
         self.k_signs = off
-        off += BLOCK * self.k_sign_row if self.k_qjl else 0
+        off += BLOCK * self.bit_row if self.k_qjl else 0
         self.k_norm = off
         off += BLOCK * 2
         self.k_rnorm = off
         off += BLOCK * 2 if self.k_qjl else 0
         self.v_codes = off
-        off += BLOCK * self.v_code_row
+        off += (v_bits * BLOCK * self.bit_row) if v_mode == "mse" else BLOCK * self.v_code_row
         self.v_meta = off
         off += BLOCK * self.v_meta_row
         self.page_bytes = off
+
+    def planes(self):
+        """(name, byte offset of row 0, row width) of every plane."""
+        out = [(f"k_code{p}", self.k_codes + p * BLOCK * self.bit_row, self.bit_row) for p in range(self.k_bits)]
+        if self.k_qjl:
+            out.append(("k_signs", self.k_signs, self.bit_row))
+        out.append(("k_norm", self.k_norm, 2))
+        if self.k_qjl:
+            out.append(("k_rnorm", self.k_rnorm, 2))
+        if self.v_mode == "mse":
+            out += [(f"v_code{p}", self.v_codes + p * BLOCK * self.bit_row, self.bit_row)
+                    for p in range(self.v_bits)]
+        else:
+            out.append(("v_codes", self.v_codes, self.v_code_row))
+        out.append(("v_meta", self.v_meta, self.v_meta_row))
+        return out
 
 
 def pack_codes(idx, bits):
@@ -69,12 +102,22 @@ def unpack_codes(rows, d, bits):
 
 
 def pack_bits(flags):
-    """[N, d] booleans -> [N, d/8] bytes, flag j -> bit (j % 8) of byte j // 8."""
+    """[N, d] booleans -> [N, d/8] bytes, flag c -> bit (c % 8) of byte c // 8."""
     return np.packbits(np.asarray(flags, np.uint8), axis=1, bitorder="little")
 
 
 def unpack_bits(rows, d):
     return np.unpackbits(np.asarray(rows, np.uint8), axis=1, bitorder="little")[:, :d].astype(bool)
+
+
+def pack_bit_planes(idx, bits):
+    """[N, d] codes -> list of `bits` planes, plane p = pack_bits(bit p of each code)."""
+    idx = np.asarray(idx, np.int64)
+    return [pack_bits((idx >> p) & 1) for p in range(bits)]
+
+
+def unpack_bit_planes(planes, d):
+    return sum(unpack_bits(pl, d).astype(np.int64) << p for p, pl in enumerate(planes))
 
 
 def f16_bytes(x):
@@ -108,12 +151,14 @@ class CacheParams:
 def encode(P, K, V):
     """Quantise rows of K and V ([N, d] each) into the page-row byte images.
 
-    Returns (fields, pre) where fields maps a plane name to its [N, row_bytes]
-    uint8 rows and pre holds the fp64 pre-images of every decision."""
+    Returns (fields, pre) where fields maps a plane name (PageLayout.planes)
+    to its [N, row_bytes] uint8 rows and pre holds the fp64 pre-images of every
+    decision."""
     L = P.layout
     fields, pre = {}, {}
     n16, idx, pk = quant.mse_quantise(K, P.R, P.k_boundaries)
-    fields["k_codes"] = pack_codes(idx, L.k_bits)
+    for p, plane in enumerate(pack_bit_planes(idx, L.k_bits)):
+        fields[f"k_code{p}"] = plane
     fields["k_norm"] = f16_bytes(n16[:, None])
     pre.update(k_n=pk["n"], k_y=pk["y"], k_idx=idx)
     if L.k_qjl:
@@ -123,26 +168,24 @@ def encode(P, K, V):
         pre.update(k_rho=pz["rho"], k_z=pz["z"], k_bits=bits)
     if L.v_mode == "mse":
         vn16, vidx, pv = quant.mse_quantise(V, P.R, P.v_boundaries)
-        fields["v_codes"] = pack_codes(vidx, L.v_bits)
+        for p, plane in enumerate(pack_bit_planes(vidx, L.v_bits)):
+            fields[f"v_code{p}"] = plane
         fields["v_meta"] = f16_bytes(vn16[:, None])
         pre.update(v_n=pv["n"], v_y=pv["y"], v_idx=vidx)
     else:
         s16, z16, q, pg = quant.group32_quantise(V, L.v_bits)
-        fields["v_codes"] = pack_codes(q, L.v_bits)
+        tau = group32_slot_coordinates(P.d)
+        fields["v_codes"] = pack_codes(q[:, tau], L.v_bits)
         fields["v_meta"] = f16_bytes(np.stack([s16, z16], axis=2).reshape(len(V), 2 * s16.shape[1]))
         pre.update(v_scale=pg["scale"], v_zero=pg["zero"], v_t=pg["t"], v_q=q)
     return fields, pre
 
 
 def _plane(L, name):
-    return {
-        "k_codes": (L.k_codes, L.k_code_row),
-        "k_signs": (L.k_signs, L.k_sign_row),
-        "k_norm": (L.k_norm, 2),
-        "k_rnorm": (L.k_rnorm, 2),
-        "v_codes": (L.v_codes, L.v_code_row),
-        "v_meta": (L.v_meta, L.v_meta_row),
-    }[name]
+    for n, base, width in L.planes():
+        if n == name:
+            return base, width
+    raise KeyError(name)
 
 
 def store(cache, P, K, V, slot_mapping):
@@ -182,10 +225,16 @@ def read_tokens(cache, P, block_table_row, length, head):
     rows = t % BLOCK
     g = lambda name: gather_rows(cache, P, blocks, rows, head, name)  # noqa: E731
     out = {
-        "k_idx": unpack_codes(g("k_codes"), P.d, L.k_bits),
+        "k_idx": unpack_bit_planes([g(f"k_code{p}") for p in range(L.k_bits)], P.d),
         "k_n16": bytes_f16(g("k_norm"))[:, 0],
-        "v_codes": unpack_codes(g("v_codes"), P.d, L.v_bits),
     }
+    if L.v_mode == "mse":
+        out["v_codes"] = unpack_bit_planes([g(f"v_code{p}") for p in range(L.v_bits)], P.d)
+    else:
+        slots = unpack_codes(g("v_codes"), P.d, L.v_bits)
+        codes = np.zeros_like(slots)
+        codes[:, group32_slot_coordinates(P.d)] = slots
+        out["v_codes"] = codes
     if L.k_qjl:
         out["k_bits"] = unpack_bits(g("k_signs"), P.d)
         out["k_rho16"] = bytes_f16(g("k_rnorm"))[:, 0]

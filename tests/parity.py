@@ -54,25 +54,27 @@ def boundary_masks(P, pre):
     return m
 
 
+def _mask_key(name):
+    if name.startswith("k_code"):
+        return "k_codes"
+    if name.startswith("v_code"):
+        return "v_codes"
+    return name
+
+
 def _excused(mask, name, L, byte_in_row):
     """Whether a mismatching byte of a plane row touches an uncertain field."""
-    if name in ("k_codes", "v_codes"):
-        bits = L.k_bits if name == "k_codes" else L.v_bits
-        lo, hi = byte_in_row * 8 // bits, (byte_in_row * 8 + 7) // bits
-        return bool(mask[lo:hi + 1].any())
-    if name == "k_signs":
+    if name == "v_codes" and L.v_mode == "g32":
+        lo, hi = byte_in_row * 8 // L.v_bits, (byte_in_row * 8 + 7) // L.v_bits
+        coords = paged.group32_slot_coordinates(L.d)[lo:hi + 1]
+        return bool(mask[coords].any())
+    if name.startswith(("k_code", "v_code", "k_signs")):
         return bool(mask[byte_in_row * 8: byte_in_row * 8 + 8].any())
-    if name == "v_meta" and mask.ndim == 0:
-        return bool(mask)
     return bool(np.any(mask))
 
 
 def _plane_list(L):
-    planes = [("k_codes", L.k_codes, L.k_code_row), ("k_norm", L.k_norm, 2), ("v_codes", L.v_codes, L.v_code_row),
-              ("v_meta", L.v_meta, L.v_meta_row)]
-    if L.k_qjl:
-        planes += [("k_signs", L.k_signs, L.k_sign_row), ("k_rnorm", L.k_rnorm, 2)]
-    return planes
+    return L.planes()
 
 
 def gpu_rows(cache_pages, L, slots, heads, name, base, width):
@@ -105,7 +107,7 @@ def compare_store(cache_pages, P, K, V, slots, heads):
         checked += exp.size
         mismatched += len(bad_vec)
         for vec, byte in zip(bad_vec, bad_byte):
-            if not _excused(masks[name][vec], name, L, int(byte)):
+            if not _excused(masks[_mask_key(name)][vec], name, L, int(byte)):
                 unexplained.append((name, int(vec), int(byte), int(got[vec, byte]), int(exp[vec, byte])))
     counted = {k: int(np.sum(v)) for k, v in masks.items()}
     return dict(checked_bytes=checked, mismatched_bytes=mismatched, unexplained=unexplained,

@@ -66,7 +66,7 @@ def test_qjl_matrix_matches_oracle(d, seed):
 
 
 @pytest.mark.parametrize("d,kb,vm,vb", [(128, 2, 0, 2), (128, 3, 1, 4), (256, 2, 0, 2), (128, 4, 1, 2),
-                                        (256, 3, 1, 3)])
+                                        (256, 3, 0, 3), (256, 4, 1, 4)])
 def test_page_bytes_match_oracle_layout(d, kb, vm, vb):
     cfg = tq.tq_cache_config(head_dim=d, num_kv_heads=8, num_q_heads=32, num_blocks=10, k_bits=kb, v_mode=vm,
                              v_bits=vb, max_blocks_per_seq=4)
@@ -83,7 +83,8 @@ def test_bad_configs_are_rejected_on_the_host():
     tq.tq_cache_sizes(tq.tq_cache_config(**ok))
     for bad, status in [(dict(head_dim=64), -2), (dict(k_bits=5), -2), (dict(v_bits=1), -2), (dict(block_size=32), -2),
                         (dict(num_q_heads=30), -1), (dict(num_blocks=0), -1), (dict(v_mode=7), -2),
-                        (dict(split_blocks=0), -1), (dict(tail_cap=-1), -1)]:
+                        (dict(split_blocks=0), -1), (dict(tail_cap=-1), -1), (dict(v_mode=1, v_bits=3), -2),
+                        (dict(num_q_heads=48), -2)]:
         with pytest.raises(tq.TQError) as e:
             tq.tq_cache_sizes(tq.tq_cache_config(**{**ok, **bad}))
         assert e.value.status == status, bad

@@ -201,6 +201,46 @@ def test_pack_unpack_round_trip(bits):
     assert np.array_equal(paged.unpack_bits(paged.pack_bits(flags), 256), flags)
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_bit_planes_round_trip_and_hand_example(bits):
+    rng = np.random.default_rng(10 + bits)
+    codes = rng.integers(0, 2**bits, size=(16, 128))
+    planes = paged.pack_bit_planes(codes, bits)
+    assert len(planes) == bits and all(p.shape == (16, 16) for p in planes)
+    assert np.array_equal(paged.unpack_bit_planes(planes, 128), codes)
+    # codes 5, 3, 6, 0, ...: bit-0 plane byte 0 = 1,1,0 -> 0x03; bit 1: 0,1,1 -> 0x06; bit 2: 1,0,1 -> 0x05
+    ex = np.zeros((1, 8), np.int64)
+    ex[0, :3] = [5, 3, 6]
+    pl = paged.pack_bit_planes(ex, 3)
+    assert [pl[0][0, 0], pl[1][0, 0], pl[2][0, 0]] == [0x03, 0x06, 0x05]
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_group32_slot_permutation(d):
+    tau = paged.group32_slot_coordinates(d)
+    assert np.array_equal(np.sort(tau), np.arange(d))          # a bijection
+    if d == 128:
+        # hand-computed from slot k = 16 g + 2 m + e -> 32 (m//2) + 4 g + 2 (m%2) + e
+        assert list(tau[:8]) == [0, 1, 2, 3, 32, 33, 34, 35] and list(tau[16:20]) == [4, 5, 6, 7]
+    w = d // 8
+    for k in range(0, d, 2):  # the two slots of a pair are adjacent coordinates of one group
+        assert tau[k + 1] == tau[k] + 1 and tau[k] // 32 == tau[k + 1] // 32
+    for m in range(d // 16):  # slot pair m of every g lies in group m // 2
+        assert {tau[w * g + 2 * m] // 32 for g in range(8)} == {m // 2}
+
+
+def test_group32_slot_round_trip_through_a_page():
+    P = paged.CacheParams(128, 2, True, "g32", 4, 2, 1)
+    rng = np.random.default_rng(4)
+    V = rng.standard_normal((16, 1, 128))
+    K = rng.standard_normal((16, 1, 128))
+    cache = np.zeros((1, 1, P.layout.page_bytes), np.uint8)
+    pre = paged.store(cache, P, K, V, np.arange(16))
+    f = paged.read_tokens(cache, P, np.array([0]), 16, 0)
+    assert np.array_equal(f["v_codes"], pre["v_q"])
+    assert np.array_equal(f["k_idx"], pre["k_idx"])
+
+
 def test_page_layout_sizes():
     # bytes per token-head: codes + signs + 2 fp16 norms, plus value codes and
     # metadata (these totals follow from the layout reading, e.g. 68 + 80 for
@@ -372,7 +412,7 @@ def test_store_skips_negative_slots_and_block_table_is_respected():
     skip[3] = -1
     paged.store(a, P, K, V, slots)
     paged.store(b, P, K, V, skip)
-    row3 = paged.gather_rows(b, P, np.array([0]), np.array([3]), 0, "k_codes")
+    row3 = paged.gather_rows(b, P, np.array([0]), np.array([3]), 0, "k_code0")
     assert np.all(row3 == 0)
     # the same tokens placed in other physical blocks decode identically
     c = np.zeros_like(a)

@@ -58,7 +58,7 @@ CASES = [
     ("c2_like", 128, 8, 3, "g32", 4, "bf16", True, 3, 10.0),
     ("c3_like_d256", 256, 4, 2, "mse", 2, "bf16", True, 5, 15.0),
     ("k4_v2g32", 128, 2, 4, "g32", 2, "bf16", True, 3, 10.0),
-    ("d256_f32_k3_g32v3", 256, 2, 3, "g32", 3, "f32", True, 5, 15.0),
+    ("d256_f32_k3_g32v2", 256, 2, 3, "g32", 2, "f32", True, 5, 15.0),
     ("no_qjl_v4mse", 128, 2, 3, "mse", 4, "bf16", False, 3, 10.0),
     ("k4_v3mse_d256", 256, 1, 4, "mse", 3, "bf16", True, 5, 15.0),
 ]

@@ -15,7 +15,7 @@ import numpy as np
 
 __all__ = [
     "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_V_MSE", "TQ_V_G32",
-    "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "EXPORTED",
+    "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
     "library_path", "load_library", "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_set_profile_events", "tq_get_device_error", "TQCache",
@@ -24,7 +24,7 @@ __all__ = [
 
 TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
 TQ_V_MSE, TQ_V_G32 = 0, 1
-TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL = 1, 2, 4, 8
+TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 
 # every function include/tq_kv.h declares
 EXPORTED = [

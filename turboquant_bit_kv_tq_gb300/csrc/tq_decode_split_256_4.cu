@@ -1,0 +1,11 @@
+// Split-KV decode kernels for head dim 256, 4-bit keys.
+#include "tq_decode_kernels.cuh"
+
+namespace tq {
+
+template <>
+tq_status dispatch_split<256, 4>(const DecodeArgs& a, cudaStream_t s, size_t smem) {
+    return dispatch_nt<256, 4>(a, s, smem);
+}
+
+}  // namespace tq

@@ -19,9 +19,14 @@ tq_status compute_layout(const tq_cache_config& c, Layout* lay) {
     if (c.block_size != kBlock) return TQ_ERR_UNSUPPORTED;
     if (c.k_bits < 2 || c.k_bits > 4 || c.v_bits < 2 || c.v_bits > 4) return TQ_ERR_UNSUPPORTED;
     if (c.v_mode != TQ_V_MSE && c.v_mode != TQ_V_G32) return TQ_ERR_UNSUPPORTED;
+    // group-32 values pack 2 or 4 bits per coordinate ([Hub] step 4)
+    if (c.v_mode == TQ_V_G32 && c.v_bits != 2 && c.v_bits != 4) return TQ_ERR_UNSUPPORTED;
     if (c.k_qjl != 0 && c.k_qjl != 1) return TQ_ERR_INVALID_ARG;
     if (c.num_kv_heads < 1 || c.num_q_heads < c.num_kv_heads || c.num_q_heads % c.num_kv_heads) return TQ_ERR_INVALID_ARG;
-    if (c.num_q_heads / c.num_kv_heads > 16) return TQ_ERR_UNSUPPORTED;
+    {
+        const int G = c.num_q_heads / c.num_kv_heads;  // grouped query heads per KV head
+        if (G > 16 || (G > 4 && G % 4)) return TQ_ERR_UNSUPPORTED;
+    }
     if (c.num_blocks < 1 || c.max_batch < 1 || c.max_blocks_per_seq < 1 || c.split_blocks < 1 || c.tail_cap < 0)
         return TQ_ERR_INVALID_ARG;
     Layout L;
@@ -82,19 +87,40 @@ ParamsLayout params_layout(const tq_cache_config& c) {
     off = up256(off + kMaxLevels * 4);
     p.v_bound = off;
     off = up256(off + kMaxLevels * 4);
+    p.k_walsh = off;
+    off = up256(off + 9 * 4);
+    p.v_walsh = off;
+    off = up256(off + 9 * 4);
     p.err = off;
     off = up256(off + 4);
     p.total = off;
     return p;
 }
 
+DecodeGeom decode_geom(const tq_cache_config& c) {
+    DecodeGeom g;
+    const int G = c.num_q_heads / c.num_kv_heads;
+    g.hg = G < 4 ? G : 4;
+    g.nhg = G <= 4 ? 1 : G / 4;
+    g.nt = (4 * g.hg + 7) / 8;
+    g.npk = 1 << (c.k_bits - 1);
+    g.npl = g.npk + (c.k_qjl ? 1 : 0);
+    g.frag_words = g.nhg * g.npl * (c.head_dim / 32) * g.nt * 2 * 32;
+    return g;
+}
+
 WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     const Splits s = compute_splits(c);
+    const DecodeGeom gm = decode_geom(c);
     const size_t bh = size_t(c.max_batch) * c.num_q_heads, d = c.head_dim;
     WorkspaceLayout w;
     size_t off = 0;
     w.q = off;
     off = up256(off + bh * 3 * d * 4);
+    w.frag = off;
+    off = up256(off + size_t(c.max_batch) * c.num_kv_heads * gm.frag_words * 4);
+    w.cst = off;
+    off = up256(off + bh * 4 * 4);
     w.acc = off;
     off = up256(off + bh * s.n_splits * d * 4);
     w.ml = off;
@@ -215,6 +241,26 @@ struct SphereDensity {
         return C / (d - 1) * (exp(e * log1p(-a * a)) - exp(e * log1p(-b * b)));
     }
 };
+
+// Expansion of a symmetric codebook over XOR bit-planes: with chi_S(i) =
+// (-1)^popcount(i & S), c[i] = sum_S chat_S chi_S(i), chat_S = mean_i c[i] chi_S(i);
+// symmetry (c[L-1-i] = -c[i]) leaves only odd |S|.  Writing chi_S = 1 - 2 u_S,
+// u_S = XOR of the bits of i in S:  c[i] = alpha + sum_S beta_S u_S(i) with
+// alpha = sum_S chat_S, beta_S = -2 chat_S.  out = {alpha, beta_S...} in the
+// order of plane_subset().
+static void walsh_planes(const std::vector<double>& c, int bits, float* out) {
+    const int L = 1 << bits, planes = 1 << (bits - 1);
+    double alpha = 0.0;
+    for (int pi = 0; pi < planes; ++pi) {
+        const int S = plane_subset(bits, pi);
+        double chat = 0.0;
+        for (int i = 0; i < L; ++i) chat += (__builtin_popcount(i & S) & 1) ? -c[i] : c[i];
+        chat /= L;
+        alpha += chat;
+        out[1 + pi] = (float)(-2.0 * chat);
+    }
+    out[0] = (float)alpha;
+}
 
 static void lloyd_max_sphere(int d, int bits, std::vector<double>& c, std::vector<double>& b, double* mse) {
     const int L = 1 << bits;
@@ -346,6 +392,8 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     put(pl.k_bound, h->k_bound);
     put(pl.v_cent, h->v_cent);
     put(pl.v_bound, h->v_bound);
+    walsh_planes(h->k_cent, cfg->k_bits, (float*)(img.data() + pl.k_walsh));
+    if (cfg->v_mode == TQ_V_MSE) walsh_planes(h->v_cent, cfg->v_bits, (float*)(img.data() + pl.v_walsh));
     cudaStream_t s = (cudaStream_t)stream;
     if (cudaMemcpyAsync(params_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
@@ -361,10 +409,15 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     h->dp.k_bound = (const float*)(base + pl.k_bound);
     h->dp.v_cent = (const float*)(base + pl.v_cent);
     h->dp.v_bound = (const float*)(base + pl.v_bound);
+    h->dp.k_walsh = (const float*)(base + pl.k_walsh);
+    h->dp.v_walsh = (const float*)(base + pl.v_walsh);
     h->dp.err = (uint32_t*)(base + pl.err);
     const WorkspaceLayout wl = workspace_layout(*cfg);
     uint8_t* ws = (uint8_t*)workspace_dev;
+    h->geom = decode_geom(*cfg);
     h->ws_q = (float*)(ws + wl.q);
+    h->ws_frag = (uint32_t*)(ws + wl.frag);
+    h->ws_cst = (float*)(ws + wl.cst);
     h->ws_acc = (float*)(ws + wl.acc);
     h->ws_ml = (float*)(ws + wl.ml);
     *out = h;

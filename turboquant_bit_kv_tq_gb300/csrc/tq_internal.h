@@ -32,8 +32,20 @@ struct DeviceParams {
     const float* k_bound;    // [16] key boundaries
     const float* v_cent;     // [16] value centroids (MSE)
     const float* v_bound;    // [16]
+    // code value = alpha + sum_P beta[P] * u_P(code bits), u_P = XOR of the
+    // code bits in the P-th odd subset (plane_subset); [0] = alpha
+    const float* k_walsh;    // [1 + 8]
+    const float* v_walsh;    // [1 + 8] (MSE values)
     uint32_t* err;           // device error word
 };
+
+// Odd-size subsets of the code bits, in increasing mask order: the planes of a
+// b-bit symmetric codebook (2^(b-1) of them).
+__host__ __device__ constexpr int plane_subset(int bits, int i) {
+    return bits == 2 ? (i == 0 ? 1 : 2)
+         : bits == 3 ? (i == 0 ? 1 : i == 1 ? 2 : i == 2 ? 4 : 7)
+                     : (i == 0 ? 1 : i == 1 ? 2 : i == 2 ? 4 : i == 3 ? 7 : i == 4 ? 8 : i == 5 ? 11 : i == 6 ? 13 : 14);
+}
 
 // Split-KV geometry of a configuration.
 struct Splits {
@@ -42,11 +54,21 @@ struct Splits {
 };
 
 struct ParamsLayout {
-    size_t signs, s_f32, st_f32, s_bf16, k_cent, k_bound, v_cent, v_bound, err, total;
+    size_t signs, s_f32, st_f32, s_bf16, k_cent, k_bound, v_cent, v_bound, k_walsh, v_walsh, err, total;
 };
 
+// Decode geometry: query heads per head group (<= 4, one CTA each), head
+// groups per KV head, score n-tiles, key code planes, score planes (+ QJL) and
+// score-operand words per (batch, KV head).
+struct DecodeGeom {
+    int hg, nhg, nt, npk, npl, frag_words;
+};
+DecodeGeom decode_geom(const tq_cache_config& c);
+
 struct WorkspaceLayout {
-    size_t q, acc, ml, total;  // q: [B][Hq][3][d]; acc: [B][Hq][S][d]; ml: [B][Hq][S][2]
+    // q: [B][Hq][3][d] fp32; frag: [B][Hkv][frag_words] u32 (score operands);
+    // cst: [B][Hq][4] fp32; acc: [B][Hq][S][d]; ml: [B][Hq][S][2]
+    size_t q, frag, cst, acc, ml, total;
 };
 
 tq_status compute_layout(const tq_cache_config& c, Layout* lay);
@@ -61,7 +83,10 @@ struct tq_cache {
     tq::Layout lay;
     tq::Splits splits;
     tq::DeviceParams dp;
+    tq::DecodeGeom geom;
     float* ws_q;
+    uint32_t* ws_frag;
+    float* ws_cst;
     float* ws_acc;
     float* ws_ml;
     // profiling events (cudaEvent_t) around the store / decode-split kernels

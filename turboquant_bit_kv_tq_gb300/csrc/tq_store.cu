@@ -42,6 +42,31 @@ __device__ __forceinline__ void pack_row(const uint8_t* codes, int d, int b, uin
     }
 }
 
+// Bit-sliced code planes: plane p, bit c of the row = bit p of the code of
+// coordinate c.  Lane l holds coordinates l + 32k, so word k of a plane row is
+// one warp ballot.
+template <int D>
+__device__ __forceinline__ void write_bit_planes(const int (&idx)[D / 32], int bits, uint8_t* planes, int row,
+                                                 int lane) {
+    for (int p = 0; p < bits; ++p) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(planes + (p * kBlock + row) * (D / 8));
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+            const uint32_t word = __ballot_sync(0xffffffffu, (idx[k] >> p) & 1);
+            if (lane == k) dst[k] = word;
+        }
+    }
+}
+
+// Group-32 value field slot of coordinate c: group gr = c/32, offset o = c%32
+// -> slot (D/8)*(o/4) + 2*(2*gr + (o%4)/2) + o%2 (inverse of the slot map in
+// the page layout).
+template <int D>
+__device__ __forceinline__ int g32_slot(int c) {
+    const int gr = c >> 5, o = c & 31;
+    return (D / 8) * (o >> 2) + 2 * (2 * gr + ((o & 3) >> 1)) + (o & 1);
+}
+
 // TurboQuant-MSE code of one vector ([Explainer] steps 1-2): returns the fp32
 // norm; idx[k] is the code of coordinate lane + 32k.
 template <int D>
@@ -122,10 +147,7 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         int idx[PER];
         const float n = mse_codes<D>(x, s_signs, s_kb, (1 << L.k_bits) - 1, lane, idx);
         const __half n16 = __float2half_rn(n);
-#pragma unroll
-        for (int k = 0; k < PER; ++k) cw[lane + 32 * k] = (uint8_t)idx[k];
-        __syncwarp();
-        pack_row(cw, D, L.k_bits, page + L.k_codes + row * L.k_code_row, lane);
+        write_bit_planes<D>(idx, L.k_bits, page + L.k_codes, row, lane);
         if (lane == 0) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
         if (L.k_qjl) {
             // residual r = k - n16 R^T c[idx], with R^T c = D H c / sqrt(d)
@@ -153,7 +175,7 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
 #pragma unroll
                 for (int k = 0; k < PER; ++k) z[k] = fmaf(bf16_bits_to_float(st[i * D + lane + 32 * k]), ri, z[k]);
             }
-            uint32_t* srow = reinterpret_cast<uint32_t*>(page + L.k_signs + row * L.k_sign_row);
+            uint32_t* srow = reinterpret_cast<uint32_t*>(page + L.k_signs + row * (D / 8));
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
                 const uint32_t word = __ballot_sync(0xffffffffu, z[k] >= 0.f);
@@ -168,8 +190,7 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         for (int k = 0; k < PER; ++k) x[k] = load_as_float(vin + lane + 32 * k);
         if (L.v_mode == TQ_V_MSE) {
             const float vn = mse_codes<D>(x, s_signs, s_vb, (1 << L.v_bits) - 1, lane, idx);
-#pragma unroll
-            for (int k = 0; k < PER; ++k) cw[lane + 32 * k] = (uint8_t)idx[k];
+            write_bit_planes<D>(idx, L.v_bits, page + L.v_codes, row, lane);
             if (lane == 0) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(vn);
         } else {
             // group g = coordinates [32g, 32g+32) = slot k of every lane
@@ -188,13 +209,13 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
                     q = (int)fl + ((tq - fl) >= 0.5f ? 1 : 0);
                     q = min(max(q, 0), top);
                 }
-                cw[lane + 32 * k] = (uint8_t)q;
+                cw[g32_slot<D>(lane + 32 * k)] = (uint8_t)q;
                 if (lane == k)
                     meta[k] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
             }
+            __syncwarp();
+            pack_row(cw, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
         }
-        __syncwarp();
-        pack_row(cw, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
         __syncwarp();
     }
 }
