@@ -84,7 +84,7 @@ def _ncu_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks/throttle reasons sampled every 50 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -98,7 +98,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -393,7 +393,12 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        t_clk = time.perf_counter()
         step_ms, split_ms = _time_steps(torch, tq, c, st, stream, args.steps, flush)
+        # keep the same load running (untimed) until the sampler has seen
+        # enough of it: a short timed region may fall between two samples
+        while time.perf_counter() - t_clk < 0.6:
+            _time_steps(torch, tq, c, st, stream, 20, flush, split_events=False)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -449,6 +454,8 @@ def run_ours(args):
                        "k_bits": w.k_bits, "k_qjl": w.k_qjl, "v_mode": w.v_mode, "v_bits": w.v_bits,
                        "split_blocks": split_blocks, "out_dtype": "bf16",
                        "l2": "flushed: 256 MiB buffer written between timed steps (outside the events)",
+                       "clocks": "sampled every 50 ms over the timed steps plus untimed steps of the same "
+                                 "load up to 0.6 s",
                        "step": "tq_store of each sequence's new token + tq_decode_attention"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": _ncu_traffic("split_kernel", w.name),
