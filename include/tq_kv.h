@@ -233,6 +233,36 @@ tq_status tq_set_profile_events(tq_cache* cache, int kernel, void* start_event, 
  */
 tq_status tq_get_device_error(const tq_cache* cache, uint32_t* flags, void* stream);
 
+/*
+ * Decode attention that allocates nothing and takes no workspace buffer.
+ * The paper has no counterpart: this is an interface for callers that cannot
+ * allocate device memory themselves -- an engine whose block manager
+ * pre-budgets every byte of the GPU (a library cudaMalloc would bypass its
+ * accounting or fail once the pool has taken the memory), or code that must
+ * not risk the device-wide synchronisation a cudaMalloc can cause.
+ *
+ * Same arguments, results and errors as tq_decode_attention, except that the
+ * split-KV scratch lives in one file-scope device array of
+ * TQ_NOALLOC_SCRATCH_BYTES per GPU (reserved on every GPU that loads the
+ * library's module, held until the process exits) instead of the handle's
+ * workspace, which this call never touches.
+ *   - Returns TQ_ERR_BUFFER_TOO_SMALL, launching nothing, when the
+ *     configuration's workspace (tq_cache_sizes) exceeds the array.
+ *   - The first call on a device looks the array up (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream
+ *     capture.
+ *   - All calls share the array and it keeps the last call's contents; every
+ *     byte a call reads was written earlier by the same call.  Calls whose
+ *     kernels overlap on the GPU (other streams, other threads) race on it:
+ *     order them on one stream.
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define TQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+tq_status tq_decode_attention_noalloc(const tq_cache* cache, const void* q, int q_dtype, const void* cache_buf,
+                                      const int32_t* block_table, const int32_t* seq_lens, const void* tail_k,
+                                      const void* tail_v, const int32_t* tail_lens, float scale, int batch,
+                                      void* out, int out_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

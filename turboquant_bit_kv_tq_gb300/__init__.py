@@ -18,7 +18,8 @@ __all__ = [
     "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
     "library_path", "load_library", "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
-    "tq_store", "tq_decode_attention", "tq_set_profile_events", "tq_get_device_error", "TQCache",
+    "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
+    "tq_get_device_error", "TQCache",
     "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT",
 ]
 
@@ -30,7 +31,7 @@ TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIM
 EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
-    "tq_set_profile_events", "tq_get_device_error",
+    "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -98,6 +99,8 @@ def load_library():
             "tq_store": (i32, [_P, _P, _P, i32, i64, _P, _P, _P]),
             "tq_decode_attention": (i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_set_profile_events": (i32, [_P, i32, _P, _P]),
+            "tq_decode_attention_noalloc": (
+                i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_get_device_error": (i32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
         }
         for name, (res, args) in sig.items():
@@ -226,6 +229,22 @@ def tq_decode_attention(handle, q, cache, block_table, seq_lens, out, tail_k=Non
         _dev(seq_lens, "seq_lens", torch.int32), _dev(tail_k, "tail_k"), _dev(tail_v, "tail_v"),
         _dev(tail_lens, "tail_lens", torch.int32), float(scale), q.shape[0], _dev(out, "out"), _dtype_code(out),
         _stream_ptr(stream)), "tq_decode_attention")
+
+
+def tq_decode_attention_noalloc(handle, q, cache, block_table, seq_lens, out, tail_k=None, tail_v=None,
+                                tail_lens=None, scale=0.0, stream=None):
+    """tq_decode_attention with its scratch in the library's static device
+    array instead of the handle's workspace (allocates nothing)."""
+    import torch
+
+    if tail_k is not None:
+        _dev(tail_k, "tail_k", torch.bfloat16)
+        _dev(tail_v, "tail_v", torch.bfloat16)
+    _check(load_library().tq_decode_attention_noalloc(
+        handle, _dev(q, "q"), _dtype_code(q), _dev(cache, "cache"), _dev(block_table, "block_table", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(tail_k, "tail_k"), _dev(tail_v, "tail_v"),
+        _dev(tail_lens, "tail_lens", torch.int32), float(scale), q.shape[0], _dev(out, "out"), _dtype_code(out),
+        _stream_ptr(stream)), "tq_decode_attention_noalloc")
 
 
 def tq_set_profile_events(handle, kernel, start=None, stop=None):
