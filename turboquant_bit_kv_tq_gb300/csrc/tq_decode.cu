@@ -8,8 +8,8 @@
 namespace tq {
 
 template <int D>
-static tq_status launch(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1) {
-    const size_t prep_smem = (size_t)3 * a.group * D * 4 + (size_t)a.group * 2 * 4;
+static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) {
+    const size_t prep_smem = prep_smem_bytes<D>(a.group);
     static bool prep_attr = false;  // once per head dim, before any capture
     if (!prep_attr) {
         if (cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
@@ -17,10 +17,10 @@ static tq_status launch(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev
             return TQ_ERR_CUDA;
         prep_attr = true;
     }
-    const size_t main_smem = SplitSmem<D>::total(a.lay.page_bytes);
-    const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
-    const size_t smem = std::max(main_smem, a.tail_cap > 0 ? tail_smem : (size_t)0);
-    if (smem > 227 * 1024 || prep_smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
+    size_t smem = 0;
+    const tq_status cfg = split_config<D>(a, &a.stages, &smem);
+    if (cfg != TQ_OK) return cfg;
+    if (prep_smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
     prep_kernel<D><<<dim3(a.heads, a.batch), 256, prep_smem, s>>>(a);
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
     tq_status st;
@@ -33,6 +33,10 @@ static tq_status launch(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
     combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1) {
+    return a.lay.d == 128 ? launch_dim<128>(a, s, ev0, ev1) : launch_dim<256>(a, s, ev0, ev1);
 }
 
 }  // namespace tq
@@ -77,11 +81,11 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     a.dp = c->dp;
     a.gm = c->geom;
     a.ws_q = c->ws_q;
-    a.ws_frag = c->ws_frag;
+    a.ws_bimg = c->ws_bimg;
     a.ws_cst = c->ws_cst;
     a.ws_acc = c->ws_acc;
     a.ws_ml = c->ws_ml;
     cudaStream_t s = (cudaStream_t)stream;
     void *e0 = c->prof_start[TQ_PROF_DECODE_SPLIT], *e1 = c->prof_stop[TQ_PROF_DECODE_SPLIT];
-    return d == 128 ? launch<128>(a, s, e0, e1) : launch<256>(a, s, e0, e1);
+    return launch_decode(a, s, e0, e1);
 }

@@ -8,16 +8,14 @@
 //
 // Three launches on the caller's stream:
 //   prep     per (KV head, b): R q, S q and q for the grouped query heads,
-//            pre-scaled by scale*log2(e); the score operands of the tensor-core
-//            contraction (fp8 pieces, register-fragment order) and per-head
-//            constants
-//   split    per (split, KV head x head group, b): four warps stream 16-token
-//            pages through per-warp shared-memory rings filled by bulk async
-//            copies; scores are fp8 tensor-core contractions (key code
-//            bit-planes x R q, QJL sign plane x S q), then online exp2
-//            softmax, then the value contraction on fp16 tensor cores; the
-//            newest exact tokens (hybrid tail) are one extra split on CUDA
-//            cores -> (m, l, acc) partials
+//            pre-scaled by scale*log2(e); per-head constants and the score
+//            operand image (fp8 pieces in the tensor-core shared-memory layout)
+//   split    per (split, KV head x head group, b): 128-token tiles of pages
+//            staged by bulk async copies; scores are fp8 tcgen05 contractions
+//            (key code bit-planes x R q, QJL sign plane x S q) accumulated in
+//            tensor memory, then online exp2 softmax, then the value
+//            contraction on fp16 tensor cores; the newest exact tokens (hybrid
+//            tail) are one extra split on CUDA cores -> (m, l, acc) partials
 //   combine  per (b, q head): merge the partials, undo the rotation for
 //            TurboQuant-MSE values, write out.
 //
@@ -28,12 +26,14 @@
 // position m of a byte becomes an exact fp8 (e4m3) operand with one AND (m < 7:
 // value 2^k_m, k = -9,-8,-7,-6,-5,-3,1) or one AND+OR (m = 7: +-1); the
 // per-position factor is folded into the query-side operand, which carries 4
-// fp8 pieces (~16 significant bits) as extra matrix columns.
+// fp8 pieces (~20 significant bits) as extra matrix rows (N = 5 per head).
 //
 // Value contraction.  Group-32 codes become exact fp16 subnormals (q * 2^-24,
 // q * 2^-20 by nibble position); the per-(token, group) scale multiplies the
 // probabilities (hi + lo fp16 pieces), the zero points add on CUDA cores.
-// MSE values use XOR bit-planes of their codes the same way.
+// MSE values use the XOR bit-planes of their codes as +-1 operands, so that the
+// codebook's constant term (which the inverse rotation would put entirely into
+// output coordinate 0) vanishes for a symmetric codebook instead of cancelling.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -46,7 +46,6 @@ namespace tq {
 
 constexpr int kTile = 128;  // tail split: tokens per smem tile
 constexpr int kMaxG = 16;
-constexpr int kStages = 3;  // per-warp page ring depth
 constexpr int kWarpsPerGroup = 4;
 
 struct DecodeArgs {
@@ -65,12 +64,13 @@ struct DecodeArgs {
     int64_t num_blocks;
     int heads, q_heads, group;
     int max_blocks, split_blocks, tail_cap;
+    int stages;  // split ring depth (tiles)
     Splits sp;
     Layout lay;
     DeviceParams dp;
     DecodeGeom gm;
     float* ws_q;
-    uint32_t* ws_frag;
+    uint8_t* ws_bimg;
     float* ws_cst;
     float* ws_acc;
     float* ws_ml;
@@ -79,7 +79,7 @@ struct DecodeArgs {
 // ------------------------------------------------------------ helpers
 __device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -88,7 +88,7 @@ __device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -125,8 +125,8 @@ __device__ __forceinline__ uint8_t float_to_e4m3(float x) {
     return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
-// piece k (0..3) of x * scale: successive e4m3 roundings of the residual, each
-// piece scaled by 16 over the previous one
+// piece k of x * scale: successive e4m3 roundings of the residual, each piece
+// scaled by 16 over the previous one
 __device__ __forceinline__ uint8_t e4m3_piece(float x, float scale, int k) {
     float y = x * scale;
     uint8_t p = 0;
@@ -135,6 +135,25 @@ __device__ __forceinline__ uint8_t e4m3_piece(float x, float scale, int k) {
         y = (y - e4m3_to_float(p)) * 16.f;
     }
     return p;
+}
+
+// 2^x for x <= 0 (softmax weights; approximate to ~2 ulp)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// lazy softmax rescaling: the running reference maximum only moves when a new
+// score exceeds it by more than this many log2 units (weights stay <= 2^8)
+constexpr float kRescaleSlack = 8.f;
+
+// sum of the kPieces piece accumulators of one head (fp32 bit patterns)
+__device__ __forceinline__ float piece_sum(const uint32_t* c) {
+    float x = __uint_as_float(c[kPieces - 1]);
+#pragma unroll
+    for (int k = kPieces - 2; k >= 0; --k) x = fmaf(x, 0.0625f, __uint_as_float(c[k]));
+    return x;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -155,22 +174,104 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
+// ------------------------------------------------- tensor memory (tcgen05)
+// A tensor-memory address holds the lane in bits 31..16 and the column in
+// bits 15..0; warp w may access lanes 32*(w%4) .. 32*(w%4)+31 only.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive 32-bit columns of the calling thread's lane
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]) : "r"(taddr) : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major without swizzle: 8-row x 16-byte
+// core matrices; lbo = byte step between core matrices along K, sbo = byte
+// step between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of a dense fp8 (e4m3 x e4m3) MMA with fp32
+// accumulation, both operands K-major, M = 128.
+__host__ __device__ constexpr uint32_t fp8_idesc(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | (8u << 24); }
+
+// D[128 x N] (+)= A[128 x 32] * B[N x 32]^T with A in tensor memory, B in
+// shared memory; issued by one thread
+__device__ __forceinline__ void mma_fp8_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// arrive on a shared-memory mbarrier once all prior MMAs of this thread are done
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------ prep
 // ws_q[b][h] = { R q * f, S q * f * sqrt(pi/2)/d, q * f },  f = scale*log2(e);
-// ws_cst[b][h] = { C_h, Q_h, 2^-sigmaK, 2^-sigmaQ } and the fp8 score operands:
+// ws_cst[b][h] = { C_h, Q_h, 2^-sigmaK, 2^-sigmaQ } with
 //   C_h = alpha sum_i (Rq)_i + 1/2 sum_P beta_P sum_{i%8=7} (Rq)_i
 //   Q_h = -sum_j (Sq)_j + sum_{j%8=7} (Sq)_j
-// (the i%8=7 terms undo the +-1 form of byte-bit 7, see bit_operand).
+// (the i%8=7 terms undo the +-1 form of byte-bit 7, see bit_operand), and the
+// score operand image of every head group: row n = kPieces*head + piece, K index
+// kk = P*d + 4*col + e holds piece `piece` of
+//   beta_P * (R q)_c * bit_weight(c%8) * 2^sigmaK   (key plane P < npk)
+//   2 * (S q)_c * bit_weight(c%8) * 2^sigmaQ        (sign plane P = npk)
+// for coordinate c = 32*(col/8) + 8*e + col%8: the coordinate that byte e of
+// tensor-memory column col of plane P holds in the split kernel.
+template <int D>
+__host__ __device__ constexpr size_t prep_smem_bytes(int G) {
+    return (size_t)D * D * 2 + (size_t)3 * G * D * 4 + 2 * kMaxG * 4 + 16;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     const int g = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
     const int G = a.group, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     extern __shared__ __align__(16) uint8_t smem[];
-    float* qv = reinterpret_cast<float*>(smem);  // [G][D]
-    float* rq = qv + G * D;                      // [G][D]
-    float* sq = rq + G * D;                      // [G][D]
-    float* sig = sq + G * D;                     // [G][2] = 2^sigmaK, 2^sigmaQ
+    uint16_t* st = reinterpret_cast<uint16_t*>(smem);           // S^T bf16 [D][D]
+    float* qv = reinterpret_cast<float*>(smem + (size_t)D * D * 2);  // [G][D]
+    float* rq = qv + G * D;                                     // [G][D]
+    float* sq = rq + G * D;                                     // [G][D]
+    float* sig = sq + G * D;                                    // [kMaxG][2] = 2^sigmaK, 2^sigmaQ
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sig + 2 * kMaxG);
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(smem_u32(bar), D * D * 2);
+        bulk_copy(smem_u32(st), a.dp.st_bf16, D * D * 2, smem_u32(bar));
+    }
     const int64_t hbase = (int64_t)b * a.q_heads + (int64_t)g * G;
     for (int e = tid; e < G * D; e += blockDim.x)
         qv[e] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[hbase * D + e]
@@ -186,14 +287,29 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) rq[h * D + lane + 32 * k] = x[k] * rsqrtf((float)D) * f;
     }
-    // S q (thread per output coordinate)
+    // S q from the shared copy of S^T: thread (j, head parity)
+    bool s_ok = mbar_wait(smem_u32(bar), 0, a.dp.err);
     const float kq = f * sqrtf(1.5707963267948966f) / (float)D;
-    for (int e = tid; e < G * D; e += blockDim.x) {
-        const int h = e / D, j = e % D;
-        float s = 0.f;
-        for (int i = 0; i < D; ++i) s = fmaf(a.dp.st_f32[i * D + j], qv[h * D + i], s);
-        sq[e] = s * kq;
+    {
+        constexpr int HS = 256 / D;  // head strides covered by the block (2 at d=128, 1 at d=256)
+        const int j = tid % D, h0 = tid / D;
+        for (int hb = h0; hb < G; hb += 2 * HS) {
+            const int h1 = hb + HS;
+            float s0 = 0.f, s1 = 0.f;
+            if (s_ok) {
+#pragma unroll 8
+                for (int i = 0; i < D; ++i) {
+                    const float sv = bf16_bits_to_float(st[i * D + j]);
+                    s0 = fmaf(sv, qv[hb * D + i], s0);
+                    if (h1 < G) s1 = fmaf(sv, qv[h1 * D + i], s1);
+                }
+            }
+            sq[hb * D + j] = s0 * kq;
+            if (h1 < G) sq[h1 * D + j] = s1 * kq;
+        }
     }
+    // a copy that never completed must land before the block exits
+    if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
     float* dst = a.ws_q + hbase * 3 * D;
     for (int e = tid; e < G * D; e += blockDim.x) {
@@ -213,15 +329,15 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     for (int h = warp; h < G; h += nwarps) {
         float s_rq = 0.f, s_rq7 = 0.f, s_sq = 0.f, s_sq7 = 0.f, m_rq = 0.f, m_sq = 0.f;
         for (int i = lane; i < D; i += 32) {
-            const float r = rq[h * D + i], s = sq[h * D + i];
+            const float r = rq[h * D + i], sv = sq[h * D + i];
             s_rq += r;
-            s_sq += s;
+            s_sq += sv;
             if ((i & 7) == 7) {
                 s_rq7 += r;
-                s_sq7 += s;
+                s_sq7 += sv;
             }
             m_rq = fmaxf(m_rq, fabsf(r) * fabsf(bit_weight(i & 7)));
-            m_sq = fmaxf(m_sq, fabsf(s) * fabsf(bit_weight(i & 7)));
+            m_sq = fmaxf(m_sq, fabsf(sv) * fabsf(bit_weight(i & 7)));
         }
         s_rq = warp_sum(s_rq);
         s_rq7 = warp_sum(s_rq7);
@@ -242,47 +358,33 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
         }
     }
     __syncthreads();
-    // score operand fragments: word (head group, plane, chunk, tile, reg, lane);
-    // byte j of a word is K-row 4*(lane%4) + j (+16 for reg 1) of column lane/4
-    constexpr int NCH = D / 32;
-    const int words = gm.frag_words;
-    uint32_t* fr = a.ws_frag + ((int64_t)b * a.heads + g) * words;
-    for (int wi = tid; wi < words; wi += blockDim.x) {
-        int x = wi;
-        const int ln = x % 32;
-        x /= 32;
-        const int r = x % 2;
-        x /= 2;
-        const int T = x % gm.nt;
-        x /= gm.nt;
-        const int ch = x % NCH;
-        x /= NCH;
-        const int P = x % gm.npl;
-        const int hgi = x / gm.npl;
-        const int gq = ln >> 2, tq = ln & 3;
-        int head, piece;
-        if (gm.nt == 2) {
-            head = gq >> 1;
-            piece = 2 * T + (gq & 1);
-        } else {
-            head = gq >> 2;
-            piece = gq & 3;
-        }
+    // score operand images, one 32-bit word (4 K indices) per step
+    const int kt = gm.npl * D;           // K extent (bytes per row)
+    const int row_words = kt / 4;
+    const int img_words = gm.n_cols * row_words;
+    const uint32_t sbo = 8u * kt;        // byte step between 8-row groups
+    uint8_t* img0 = a.ws_bimg + ((int64_t)b * a.heads + g) * gm.nhg * gm.bimg_bytes;
+    for (int wi = tid; wi < gm.nhg * img_words; wi += blockDim.x) {
+        const int hgi = wi / img_words, rem = wi % img_words;
+        const int n = rem / row_words, kk0 = (rem % row_words) * 4;
+        const int P = kk0 / D, col = (kk0 % D) / 4;
+        const int hl = n / kPieces, piece = n % kPieces;
         uint32_t word = 0;
-        if (head < gm.hg) {
-            const int h = hgi * 4 + head;
-            const bool qjl_plane = P == gm.npk;
-            const float beta = qjl_plane ? 2.f : kw[1 + P];
-            const float* src = qjl_plane ? sq + h * D : rq + h * D;
-            const float sc = sig[2 * h + (qjl_plane ? 1 : 0)];
+        if (hl < gm.hc) {
+            const int h = hgi * gm.hc + hl;
+            const bool sign_plane = P == gm.npk;
+            const float beta = sign_plane ? 2.f : kw[1 + P];
+            const float* src = sign_plane ? sq + h * D : rq + h * D;
+            const float sc = sig[2 * h + (sign_plane ? 1 : 0)];
+            const float bw = bit_weight(col & 7);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int coord = 128 * (ch >> 2) + 32 * tq + 8 * j + 2 * (ch & 3) + r;
-                const float v = beta * src[coord] * bit_weight(coord & 7);
-                word |= (uint32_t)e4m3_piece(v, sc, piece) << (8 * j);
+            for (int e = 0; e < 4; ++e) {
+                const int c = 32 * (col >> 3) + 8 * e + (col & 7);
+                word |= (uint32_t)e4m3_piece(beta * src[c] * bw, sc, piece) << (8 * e);
             }
         }
-        fr[wi] = word;
+        const uint32_t off = (n & 7) * 16 + (n >> 3) * sbo + (kk0 >> 4) * 128 + (kk0 & 15);
+        *reinterpret_cast<uint32_t*>(img0 + (size_t)hgi * gm.bimg_bytes + off) = word;
     }
 }
 
@@ -395,323 +497,425 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
 }
 
 // -------------------------------------------------------------- split
-// shared memory of a compressed-split CTA: per warp a page ring and the
-// probability operands, then the rings' mbarriers, then the merge buffer
-template <int D>
-struct SplitSmem {
-    static constexpr int kPbufHalves = 8 * 4 * 2 * 16;  // [<=8 groups/planes][4 heads][2 pieces][16 tokens]
-    static __host__ __device__ size_t stride(int page_bytes) { return (size_t)((page_bytes + 127) & ~127); }
-    static __host__ __device__ size_t per_warp(int page_bytes) { return kStages * stride(page_bytes) + kPbufHalves * 2; }
-    static __host__ __device__ size_t total(int page_bytes) {
-        return (size_t)kWarpsPerGroup * per_warp(page_bytes) + (size_t)kWarpsPerGroup * kStages * 8 +
-               (size_t)kWarpsPerGroup * 4 * (D + 2) * 4;
-    }
+// One CTA = one split (split_blocks pages) of one KV head for a head group of
+// hc query heads; four warps walk the split in 128-token tiles (8 pages):
+//   * the tile's pages arrive by bulk async copies into a ring of tiles
+//   * thread t owns token t: it expands the token's key planes into fp8 score
+//     operands in tensor-memory lane t (one AND per 4 coordinates)
+//   * one thread issues the fp8 MMAs D[token][head, piece] += A * B^T against
+//     the query operand image in shared memory (tcgen05, fp32 accumulators in
+//     tensor memory); each thread reads its token's scores back
+//   * online exp2 softmax per warp; the probabilities, times the group-32 scale
+//     or the MSE norm and plane weight, go to a per-warp buffer as fp16 hi + lo
+//   * each warp contracts the values of its two pages on fp16 tensor cores
+//     (mma.sync); the token order inside the contraction is permuted so that a
+//     B register is one buffer word holding tokens (t, t+8).
+constexpr int kTilePages = 8;
+constexpr int kTileTokens = kTilePages * kBlock;  // 128 = MMA M
+constexpr int kTmemCols = 256;  // per CTA; two CTAs per SM share the 512 columns
+
+// score accumulator columns (kPieces per head, whole multiples of 16) and the
+// first A operand column (after both accumulators) for nth n-tiles of heads
+__host__ __device__ constexpr int score_cols(int nth) { return (kPieces * 4 * nth + 15) / 16 * 16; }
+__host__ __device__ constexpr int tmem_a_col(int nth) { return (2 * score_cols(nth) + 31) / 32 * 32; }
+
+struct SplitLayout {
+    size_t tile, ring, bimg, pbuf, cst, zsm, bars, tslot, total;
+    int pls, pbuf_words;  // probability buffer: words per page, per warp
 };
 
-template <int D, int KB, int NT, bool G32, int VB>
+// nsets: probability operand sets (group-32: d/32 groups; MSE: value planes)
+template <int D>
+__host__ __device__ inline SplitLayout split_layout(int page_bytes, const DecodeGeom& gm, int nsets, int stages) {
+    auto up = [](size_t x) { return (x + 127) & ~(size_t)127; };
+    const int h4 = 4 * gm.nth;
+    SplitLayout l;
+    l.tile = up((size_t)kTilePages * page_bytes);
+    l.pls = nsets * h4 * 24 + 16;
+    l.pbuf_words = 2 * l.pls;
+    size_t off = 0;
+    l.ring = off;
+    off = up(off + (size_t)stages * l.tile);
+    l.bimg = off;
+    off = up(off + (size_t)gm.bimg_bytes);
+    l.pbuf = off;
+    off = up(off + (size_t)kWarpsPerGroup * l.pbuf_words * 4);
+    l.cst = off;
+    off = up(off + (size_t)h4 * 4 * 4);
+    l.zsm = off;
+    off = up(off + (size_t)kWarpsPerGroup * h4 * (D / 32) * 4);
+    l.bars = off;
+    off = up(off + (size_t)(stages + 2) * 8);
+    l.tslot = off;
+    off = up(off + 4);
+    l.total = off;
+    return l;
+}
+// per-warp partials merged at the end, placed over the ring
+template <int D>
+__host__ __device__ constexpr size_t split_red_bytes(int h4) {
+    return (size_t)kWarpsPerGroup * h4 * (D + 2) * 4;
+}
+
+template <int D, int KB, bool G32, int VB, int NTH>
 __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
     constexpr int NPK = 1 << (KB - 1);  // key code planes
-    constexpr int NCH = D / 32;         // score k-chunks (32 coordinates)
+    constexpr int NW = D / 32;          // 32-bit words of a plane row
+    constexpr int NCOL = D / 4;         // tensor-memory columns of one plane
     constexpr int NMT = D / 16;         // value m-tiles (16 coordinates)
-    constexpr int NW = D / 128;         // 32-bit words of a bit-plane row per thread role
     constexpr int NPV = G32 ? 1 : (1 << (VB - 1));
+    constexpr int NSET = G32 ? D / 32 : NPV;
     constexpr int NZ = G32 ? D / 32 : 1;
-    // one CTA = one head group (4 warps) of one KV head for one split
+    constexpr int H4 = 4 * NTH;         // heads of the CTA, padded to whole n-tiles
+    constexpr int NCOLS = score_cols(NTH);  // score accumulator columns (head, piece)
+    constexpr int TA = tmem_a_col(NTH);     // first A operand column
+    constexpr int PCH = (kTmemCols - TA) / NCOL;  // planes per tensor-memory chunk
     const DecodeGeom gm = a.gm;
-    const int chunk = blockIdx.x, g = blockIdx.y / gm.nhg, hg = blockIdx.y % gm.nhg, b = blockIdx.z;
+    const int chunk = blockIdx.x, g = blockIdx.y / gm.nhg, hgi = blockIdx.y % gm.nhg, b = blockIdx.z;
     if (b >= a.batch) return;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem[];
     if (a.tail_cap > 0 && chunk == a.sp.n_chunks) {
-        if (hg == 0) tail_split<D>(a, g, b, smem);  // all G heads of the tail in one CTA
+        if (hgi == 0) tail_split<D>(a, g, b, smem);  // all G heads of the tail in one CTA
         return;
     }
     const Layout& L = a.lay;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pw = warp;  // page worker: pages pw, pw + 4, ...
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
-    const int HG = gm.hg;
+    const int hc = gm.hc, npl = gm.npl, S = a.stages;
     const bool qjl = L.k_qjl;
+    const SplitLayout sl = split_layout<D>(L.page_bytes, gm, NSET, S);
+    uint8_t* ring = smem + sl.ring;
+    const uint8_t* bimg = smem + sl.bimg;
+    uint32_t* pbw = reinterpret_cast<uint32_t*>(smem + sl.pbuf) + warp * sl.pbuf_words;
+    float* cst = reinterpret_cast<float*>(smem + sl.cst);
+    float* zsm = reinterpret_cast<float*>(smem + sl.zsm) + warp * H4 * (D / 32);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);  // [S] ring, [S] image, [S+1] MMA
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + sl.tslot);
+    float* red = reinterpret_cast<float*>(smem + sl.ring);
 
     // this split's token range
     int len = a.seq_lens[b];
     if (len < 0 || len > a.max_blocks * kBlock) {
-        if (threadIdx.x == 0 && g == 0 && chunk == 0 && hg == 0) set_error(a.dp.err, TQ_DEVERR_SEQLEN);
+        if (tid == 0 && g == 0 && chunk == 0 && hgi == 0) set_error(a.dp.err, TQ_DEVERR_SEQLEN);
         len = max(0, min(len, a.max_blocks * kBlock));
     }
     const int t0 = chunk * a.split_blocks * kBlock;
     const int t1 = min(len, t0 + a.split_blocks * kBlock);
     const int n_pages = t1 > t0 ? (t1 - t0 + kBlock - 1) / kBlock : 0;
+    const int n_tiles = (n_pages + kTilePages - 1) / kTilePages;
 
-    const int pb = L.page_bytes;
-    const size_t pstride = SplitSmem<D>::stride(pb);
-    const size_t rings = (size_t)kWarpsPerGroup * SplitSmem<D>::per_warp(pb);
-    uint8_t* ring = smem + (size_t)warp * SplitSmem<D>::per_warp(pb);
-    __half* pbuf = reinterpret_cast<__half*>(ring + kStages * pstride);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + rings) + warp * kStages;
-    float* red = reinterpret_cast<float*>(smem + rings + (size_t)kWarpsPerGroup * kStages * 8);
-
-    // score operands of this head group (registers for the whole split)
-    uint32_t bf[NPK + 1][NCH][NT][2];
-    {
-        const uint32_t* fr = a.ws_frag + ((int64_t)b * a.heads + g) * gm.frag_words;
-#pragma unroll
-        for (int P = 0; P < NPK + 1; ++P)
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                for (int T = 0; T < NT; ++T)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        bf[P][ch][T][r] = (P == NPK && !qjl)
-                                              ? 0u
-                                              : fr[((((hg * gm.npl + P) * NCH + ch) * NT + T) * 2 + r) * 32 + lane];
+    for (int e = tid; e < H4 * 4; e += blockDim.x) {
+        const int h = e >> 2;
+        cst[e] = h < hc ? a.ws_cst[((int64_t)b * a.q_heads + g * a.group + hgi * hc + h) * 4 + (e & 3)] : 0.f;
     }
-    const int my_head = hg * 4 + tq;  // softmax / value head of this thread (valid if tq < HG)
-    const bool head_ok = tq < HG;
-    float C = 0.f, Qc = 0.f, scK = 0.f, scQ = 0.f;
-    if (head_ok) {
-        const float* c = a.ws_cst + ((int64_t)b * a.q_heads + g * a.group + my_head) * 4;
-        C = c[0];
-        Qc = c[1];
-        scK = c[2];
-        scQ = c[3];
+    for (int e = lane; e < sl.pbuf_words; e += 32) pbw[e] = 0u;
+    // MSE values: with sigma_P = 1 - 2 u_P (+-1 operands, no constant offset to
+    // cancel later), c = (alpha + sum_P beta_P / 2) - sum_P (beta_P / 2) sigma_P
+    float v_dc = 0.f, v_beta[NPV];
+    if constexpr (!G32) {
+        v_dc = a.dp.v_walsh[0];
+#pragma unroll
+        for (int P = 0; P < NPV; ++P) {
+            v_beta[P] = -0.5f * a.dp.v_walsh[1 + P];
+            v_dc += 0.5f * a.dp.v_walsh[1 + P];
+        }
     }
-    float v_alpha = 0.f, v_beta[NPV];
-#pragma unroll
-    for (int P = 0; P < NPV; ++P) v_beta[P] = G32 ? 0.f : a.dp.v_walsh[1 + P];
-    if (!G32) v_alpha = a.dp.v_walsh[0];
 
-    float m_run = -INFINITY, l_part = 0.f;
-    float pv[NMT][4];
-#pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) pv[mt][0] = pv[mt][1] = pv[mt][2] = pv[mt][3] = 0.f;
-    float zacc[NZ];
-#pragma unroll
-    for (int i = 0; i < NZ; ++i) zacc[i] = 0.f;
-    for (int e = lane; e < SplitSmem<D>::kPbufHalves; e += 32) pbuf[e] = __float2half(0.f);
-
-    // page ring: lane 0 issues bulk copies completing on the stage's mbarrier
     const int32_t* btab = a.block_table + (int64_t)b * a.max_blocks + t0 / kBlock;
-    uint32_t invalid = 0;  // bit s: stage s holds a page with a bad block id (not copied)
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[s])) : "memory");
+    if (tid == 0) {
+        for (int i = 0; i < S + 2; ++i) mbar_init(smem_u32(&bars[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncwarp();
-    auto issue = [&](int i, int s) {
-        const int blk = btab[i];
-        const bool ok = blk >= 0 && blk < a.num_blocks;
-        if (ok) {
-            if (lane == 0) {
-                const uint32_t bar = smem_u32(&bars[s]);
-                const uint8_t* src = a.cache + ((int64_t)blk * a.heads + g) * pb;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(pb) : "memory");
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        smem_u32(ring + s * pstride)),
-                    "l"(src), "r"(pb), "r"(bar)
-                    : "memory");
-            }
-            invalid &= ~(1u << s);
-        } else {
-            if (lane == 0) set_error(a.dp.err, TQ_DEVERR_BLOCK);
-            invalid |= 1u << s;
+    __syncthreads();
+    // (thread 0) bulk copies of tile i's pages into stage s; bad block ids are
+    // flagged and not copied, their tokens are masked
+    auto issue_tile = [&](int i, int s) {
+        const int p0 = i * kTilePages, np = min(kTilePages, n_pages - p0);
+        uint32_t bytes = 0;
+        for (int j = 0; j < np; ++j) {
+            const int blk = btab[p0 + j];
+            if (blk >= 0 && blk < a.num_blocks)
+                bytes += L.page_bytes;
+            else
+                set_error(a.dp.err, TQ_DEVERR_BLOCK);
+        }
+        const uint32_t bar = smem_u32(&bars[s]);
+        mbar_expect_tx(bar, bytes);
+        for (int j = 0; j < np; ++j) {
+            const int blk = btab[p0 + j];
+            if (blk >= 0 && blk < a.num_blocks)
+                bulk_copy(smem_u32(ring + s * sl.tile + (size_t)j * L.page_bytes),
+                          a.cache + ((int64_t)blk * a.heads + g) * L.page_bytes, L.page_bytes, bar);
         }
     };
-    const int my_pages = n_pages > pw ? (n_pages - pw + kWarpsPerGroup - 1) / kWarpsPerGroup : 0;
-    for (int j = 0; j < kStages && j < my_pages; ++j) issue(pw + kWarpsPerGroup * j, j);
-    uint32_t phase = 0;  // bit s = parity to wait for on stage s
-    int consumed = 0;
-
-    for (int j = 0; j < my_pages; ++j) {
-        const int s = j % kStages;
-        const int pi = pw + kWarpsPerGroup * j;
-        const bool page_ok = !((invalid >> s) & 1);
-        if (page_ok) {
-            if (!mbar_wait(smem_u32(&bars[s]), (phase >> s) & 1, a.dp.err)) break;
-            phase ^= 1u << s;
+    int issued = 0;  // tiles issued so far (thread 0)
+    uint32_t tmem = 0;
+    if (n_tiles > 0) {
+        if (warp == 0) tmem_alloc(tslot, kTmemCols);
+        if (tid == 0) {
+            const uint32_t bb = smem_u32(&bars[S]);
+            mbar_expect_tx(bb, gm.bimg_bytes);
+            bulk_copy(smem_u32(bimg), a.ws_bimg + (((int64_t)b * a.heads + g) * gm.nhg + hgi) * gm.bimg_bytes,
+                      gm.bimg_bytes, bb);
+            for (; issued < S && issued < n_tiles; ++issued) issue_tile(issued, issued);
         }
-        consumed = j + 1;
-        const uint8_t* pg = ring + s * pstride;
-        const int n_valid = min(kBlock, t1 - (t0 + kBlock * pi));
-        const bool v0 = page_ok && gq < n_valid, v1 = page_ok && gq + 8 < n_valid;
-
-        // ---------------- scores: key code planes x R q, sign plane x S q
-        float ck[NT][4], cq[NT][4];
-#pragma unroll
-        for (int T = 0; T < NT; ++T)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ck[T][i] = cq[T][i] = 0.f;
-        {
-            uint32_t up[NPK][NW][2];
-            {
-                uint32_t kw[KB][NW][2];
-#pragma unroll
-                for (int p = 0; p < KB; ++p)
-#pragma unroll
-                    for (int w = 0; w < NW; ++w)
-#pragma unroll
-                        for (int h8 = 0; h8 < 2; ++h8)
-                            kw[p][w][h8] = *reinterpret_cast<const uint32_t*>(
-                                pg + L.k_codes + (p * kBlock + gq + 8 * h8) * (D / 8) + 4 * (tq + 4 * w));
-#pragma unroll
-                for (int P = 0; P < NPK; ++P)
-#pragma unroll
-                    for (int w = 0; w < NW; ++w)
-#pragma unroll
-                        for (int h8 = 0; h8 < 2; ++h8) {
-                            uint32_t x = 0;
-#pragma unroll
-                            for (int p = 0; p < KB; ++p)
-                                if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w][h8];
-                            up[P][w][h8] = x;
-                        }
-            }
-            uint32_t sw[NW][2] = {};
-            if (qjl)
-#pragma unroll
-                for (int w = 0; w < NW; ++w)
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8)
-                        sw[w][h8] = *reinterpret_cast<const uint32_t*>(pg + L.k_signs + (gq + 8 * h8) * (D / 8) +
-                                                                       4 * (tq + 4 * w));
-#define TQ_SCORE_CHUNK(CH, M0)                                                                                  \
-    {                                                                                                           \
-        constexpr int w_ = (CH) / 4;                                                                            \
-        _Pragma("unroll") for (int P = 0; P < NPK; ++P) {                                                       \
-            const uint32_t a0 = bit_operand<M0>(up[P][w_][0]), a1 = bit_operand<M0>(up[P][w_][1]);             \
-            const uint32_t a2 = bit_operand<M0 + 1>(up[P][w_][0]), a3 = bit_operand<M0 + 1>(up[P][w_][1]);     \
-            _Pragma("unroll") for (int T = 0; T < NT; ++T)                                                      \
-                mma_e4m3(ck[T], a0, a1, a2, a3, bf[P][CH][T][0], bf[P][CH][T][1]);                             \
-        }                                                                                                       \
-        if (qjl) {                                                                                              \
-            const uint32_t a0 = bit_operand<M0>(sw[w_][0]), a1 = bit_operand<M0>(sw[w_][1]);                   \
-            const uint32_t a2 = bit_operand<M0 + 1>(sw[w_][0]), a3 = bit_operand<M0 + 1>(sw[w_][1]);           \
-            _Pragma("unroll") for (int T = 0; T < NT; ++T)                                                      \
-                mma_e4m3(cq[T], a0, a1, a2, a3, bf[NPK][CH][T][0], bf[NPK][CH][T][1]);                         \
-        }                                                                                                       \
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tmem = *tslot;
     }
-            TQ_SCORE_CHUNK(0, 0)
-            TQ_SCORE_CHUNK(1, 2)
-            TQ_SCORE_CHUNK(2, 4)
-            TQ_SCORE_CHUNK(3, 6)
-            if constexpr (NCH == 8) {
-                TQ_SCORE_CHUNK(4, 0)
-                TQ_SCORE_CHUNK(5, 2)
-                TQ_SCORE_CHUNK(6, 4)
-                TQ_SCORE_CHUNK(7, 6)
-            }
-#undef TQ_SCORE_CHUNK
-        }
-        // piece sums -> scores (log2 units) of tokens gq, gq+8 for head tq
-        float pk0, pk1, pq0, pq1;
-        if constexpr (NT == 2) {
-            pk0 = ck[0][0] + ck[0][1] * 0.0625f + ck[1][0] * 0.00390625f + ck[1][1] * 0.000244140625f;
-            pk1 = ck[0][2] + ck[0][3] * 0.0625f + ck[1][2] * 0.00390625f + ck[1][3] * 0.000244140625f;
-            pq0 = cq[0][0] + cq[0][1] * 0.0625f + cq[1][0] * 0.00390625f + cq[1][1] * 0.000244140625f;
-            pq1 = cq[0][2] + cq[0][3] * 0.0625f + cq[1][2] * 0.00390625f + cq[1][3] * 0.000244140625f;
-        } else {
-            const float w0 = (tq & 1) ? 0.00390625f : 1.f, w1 = (tq & 1) ? 0.000244140625f : 0.0625f;
-            pk0 = ck[0][0] * w0 + ck[0][1] * w1;
-            pk1 = ck[0][2] * w0 + ck[0][3] * w1;
-            pq0 = cq[0][0] * w0 + cq[0][1] * w1;
-            pq1 = cq[0][2] * w0 + cq[0][3] * w1;
-            pk0 += __shfl_xor_sync(0xffffffffu, pk0, 1);
-            pk1 += __shfl_xor_sync(0xffffffffu, pk1, 1);
-            pq0 += __shfl_xor_sync(0xffffffffu, pq0, 1);
-            pq1 += __shfl_xor_sync(0xffffffffu, pq1, 1);
-            // lanes 2h, 2h+1 of a quad hold head h; lane h takes it
-            const int src = (lane & ~3) | ((2 * tq) & 3);
-            pk0 = __shfl_sync(0xffffffffu, pk0, src);
-            pk1 = __shfl_sync(0xffffffffu, pk1, src);
-            pq0 = __shfl_sync(0xffffffffu, pq0, src);
-            pq1 = __shfl_sync(0xffffffffu, pq1, src);
-        }
-        const __half* kn = reinterpret_cast<const __half*>(pg + L.k_norm);
-        const float n0 = __half2float(kn[gq]), n1 = __half2float(kn[gq + 8]);
-        float r0 = 0.f, r1 = 0.f;
-        if (qjl) {
-            const __half* rn = reinterpret_cast<const __half*>(pg + L.k_rnorm);
-            r0 = __half2float(rn[gq]);
-            r1 = __half2float(rn[gq + 8]);
-        }
-        const float s0 = (v0 && head_ok) ? n0 * (C + pk0 * scK) + r0 * (Qc + pq0 * scQ) : -INFINITY;
-        const float s1 = (v1 && head_ok) ? n1 * (C + pk1 * scK) + r1 * (Qc + pq1 * scQ) : -INFINITY;
 
-        // ---------------- online softmax (the 8 lanes sharing tq hold one head)
-        float mx = fmaxf(s0, s1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
-        const float p0 = s0 == -INFINITY ? 0.f : exp2f(s0 - m_new);
-        const float p1 = s1 == -INFINITY ? 0.f : exp2f(s1 - m_new);
-        l_part = l_part * alpha + p0 + p1;
-        m_run = m_new;
+    float m_ref[H4], l_part[H4], zacc[H4][NZ];
+    float pv[NTH][NMT][4];
 #pragma unroll
-        for (int mt = 0; mt < NMT; ++mt)
+    for (int h = 0; h < H4; ++h) {
+        m_ref[h] = -INFINITY;
+        l_part[h] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pv[mt][i] *= alpha;
+        for (int z = 0; z < NZ; ++z) zacc[h][z] = 0.f;
+    }
 #pragma unroll
-        for (int i = 0; i < NZ; ++i) zacc[i] *= alpha;
+    for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) pv[nt][mt][0] = pv[nt][mt][1] = pv[nt][mt][2] = pv[nt][mt][3] = 0.f;
 
-        // ---------------- probability operands: pbuf[set][head][piece][token]
-        // (set = value group for group-32, value plane for MSE; hi + lo fp16)
-        auto put = [&](int set, int tok, float x) {
-            const __half hi = __float2half_rn(x);
-            const __half lo = __float2half_rn(x - __half2float(hi));
-            pbuf[((set * 4 + tq) * 2 + 0) * 16 + tok] = hi;
-            pbuf[((set * 4 + tq) * 2 + 1) * 16 + tok] = lo;
-        };
-        if constexpr (G32) {
-            const __half* meta0 = reinterpret_cast<const __half*>(pg + L.v_meta + gq * L.v_meta_row);
-            const __half* meta1 = reinterpret_cast<const __half*>(pg + L.v_meta + (gq + 8) * L.v_meta_row);
+    bool ok = n_tiles > 0 ? mbar_wait(smem_u32(&bars[S]), 0, a.dp.err) : true;
+    bool mma_ok = true;
+    uint32_t ring_phase = 0, mma_phase = 0;
+    int consumed = 0;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t idesc = fp8_idesc(NCOLS);
+    const uint32_t sbo = 8u * (uint32_t)(npl * D);
+    const int pj = tid >> 4, r = tid & 15;  // this thread's page and row in the tile
+    const int pl = pj & 1, pair = r & 7, hf = r >> 3;
+
+    for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % S;
+        ok = mbar_wait(smem_u32(&bars[s]), (ring_phase >> s) & 1, a.dp.err) && ok;
+        ring_phase ^= 1u << s;
+        consumed = i + 1;
+        const int p0 = i * kTilePages, np = min(kTilePages, n_pages - p0);
+        const uint8_t* tile = ring + s * sl.tile;
+        const int pos = t0 + (p0 + pj) * kBlock + r;
+        bool valid = pj < np && pos < t1;
+        if (valid) {
+            const int blk = btab[p0 + pj];
+            valid = blk >= 0 && blk < a.num_blocks;
+        }
+        const uint8_t* pg = tile + pj * L.page_bytes;
+
+        // ---------------- score operands of this token, chunks of planes
+        uint32_t kw[KB][NW], sw[NW];
 #pragma unroll
-            for (int gr = 0; gr < D / 32; ++gr) {
-                const float sc0 = __half2float(meta0[2 * gr]), z0 = __half2float(meta0[2 * gr + 1]);
-                const float sc1 = __half2float(meta1[2 * gr]), z1 = __half2float(meta1[2 * gr + 1]);
-                if (head_ok) {
-                    put(gr, gq, p0 * sc0);
-                    put(gr, gq + 8, p1 * sc1);
-                }
-                zacc[gr] = fmaf(p0, z0, fmaf(p1, z1, zacc[gr]));
+        for (int p = 0; p < KB; ++p)
+#pragma unroll
+            for (int w4 = 0; w4 < NW; w4 += 4) {
+                const uint4 u = *reinterpret_cast<const uint4*>(pg + L.k_codes + (p * kBlock + r) * (D / 8) + 4 * w4);
+                kw[p][w4] = u.x;
+                kw[p][w4 + 1] = u.y;
+                kw[p][w4 + 2] = u.z;
+                kw[p][w4 + 3] = u.w;
             }
-        } else {
-            const __half* vn = reinterpret_cast<const __half*>(pg + L.v_meta);
-            const float nv0 = __half2float(vn[gq]), nv1 = __half2float(vn[gq + 8]);
-            if (head_ok)
 #pragma unroll
-                for (int P = 0; P < NPV; ++P) {
-                    put(P, gq, p0 * nv0 * v_beta[P]);
-                    put(P, gq + 8, p1 * nv1 * v_beta[P]);
+        for (int w4 = 0; w4 < NW; w4 += 4) {
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (qjl) u = *reinterpret_cast<const uint4*>(pg + L.k_signs + r * (D / 8) + 4 * w4);
+            sw[w4] = u.x;
+            sw[w4 + 1] = u.y;
+            sw[w4 + 2] = u.z;
+            sw[w4 + 3] = u.w;
+        }
+        bool stop = false;
+        for (int c0 = 0; c0 < npl; c0 += PCH) {
+            const int c1 = min(npl, c0 + PCH);
+#pragma unroll
+            for (int P = 0; P <= NPK; ++P) {
+                if (P < c0 || P >= c1) continue;
+                uint32_t wv[NW];
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    uint32_t x = 0;
+                    if (P < NPK) {
+#pragma unroll
+                        for (int p = 0; p < KB; ++p)
+                            if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w];
+                    } else {
+                        x = sw[w];
+                    }
+                    wv[w] = x;
                 }
-            zacc[0] = fmaf(v_alpha, fmaf(p0, nv0, p1 * nv1), zacc[0]);
+#pragma unroll
+                for (int q = 0; q < NW / 4; ++q) {
+                    // the empty volatile asm orders this chunk after the previous
+                    // store, so that only 32 operand registers are live at a time
+                    asm volatile("" : "+r"(wv[4 * q]), "+r"(wv[4 * q + 1]), "+r"(wv[4 * q + 2]), "+r"(wv[4 * q + 3]));
+                    uint32_t a32[32];
+#pragma unroll
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const uint32_t x = wv[4 * q + w4];
+                        a32[8 * w4 + 0] = bit_operand<0>(x);
+                        a32[8 * w4 + 1] = bit_operand<1>(x);
+                        a32[8 * w4 + 2] = bit_operand<2>(x);
+                        a32[8 * w4 + 3] = bit_operand<3>(x);
+                        a32[8 * w4 + 4] = bit_operand<4>(x);
+                        a32[8 * w4 + 5] = bit_operand<5>(x);
+                        a32[8 * w4 + 6] = bit_operand<6>(x);
+                        a32[8 * w4 + 7] = bit_operand<7>(x);
+                    }
+                    tmem_st32(tmem + lane_base + TA + (P - c0) * NCOL + 32 * q, a32);
+                }
+            }
+            tc_wait_st();
+            tc_fence_before();
+            const bool all_ok = __syncthreads_and(ok && mma_ok);
+            tc_fence_after();
+            if (!all_ok) {
+                stop = true;
+                break;
+            }
+            if (tid == 0) {
+                // every warp is past tile i-1: its stage takes the next tile
+                if (c0 == 0 && i >= 1 && issued < n_tiles) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_tile(issued, (i - 1) % S);
+                    ++issued;
+                }
+                for (int P = c0; P < c1; ++P)
+                    for (int kb = 0; kb < NW; ++kb) {
+                        const uint32_t d_addr = tmem + (P < NPK ? 0u : (uint32_t)NCOLS);
+                        const uint32_t a_addr = tmem + TA + (P - c0) * NCOL + 8 * kb;
+                        const uint64_t bd = smem_desc(smem_u32(bimg) + (P * (D / 16) + 2 * kb) * 128, 128, sbo);
+                        const uint32_t acc = P < NPK ? (P > 0 || kb > 0) : (kb > 0);
+                        mma_fp8_ts(d_addr, a_addr, bd, idesc, acc);
+                    }
+                tc_commit(smem_u32(&bars[S + 1]));
+            }
+            mma_ok = mbar_wait(smem_u32(&bars[S + 1]), mma_phase, a.dp.err);
+            mma_phase ^= 1;
+            tc_fence_after();
+        }
+        if (stop) break;
+
+        // ---------------- scores of this token (log2 units)
+        const float n16 = __half2float(*reinterpret_cast<const __half*>(pg + L.k_norm + 2 * r));
+        const float rho = qjl ? __half2float(*reinterpret_cast<const __half*>(pg + L.k_rnorm + 2 * r)) : 0.f;
+        float sc[H4];
+        {
+            uint32_t acc[NCOLS];
+            float sk[H4];
+#pragma unroll
+            for (int q = 0; q < NCOLS / 16; ++q) tmem_ld16(tmem + lane_base + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&acc[16 * q]));
+            tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < H4; ++h) sk[h] = piece_sum(&acc[kPieces * h]);
+            if (qjl) {
+#pragma unroll
+                for (int q = 0; q < NCOLS / 16; ++q)
+                    tmem_ld16(tmem + lane_base + NCOLS + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&acc[16 * q]));
+                tc_wait_ld();
+            }
+#pragma unroll
+            for (int h = 0; h < H4; ++h) {
+                float v = n16 * (cst[4 * h] + sk[h] * cst[4 * h + 2]);
+                if (qjl) v += rho * (cst[4 * h + 1] + piece_sum(&acc[kPieces * h]) * cst[4 * h + 3]);
+                sc[h] = (valid && h < hc) ? v : -INFINITY;
+            }
+        }
+
+        // ---------------- online softmax per warp: m_ref is a reference
+        // maximum that moves (with a rescale) only when a score passes it by
+        // more than kRescaleSlack
+        float p[H4];
+#pragma unroll
+        for (int h = 0; h < H4; ++h) {
+            const bool mv = sc[h] > m_ref[h] + kRescaleSlack;
+            if (__any_sync(0xffffffffu, mv)) {
+                const float mx = warp_max(sc[h]);
+                const float alpha = m_ref[h] == -INFINITY ? 0.f : fast_exp2(m_ref[h] - mx);
+                l_part[h] *= alpha;
+#pragma unroll
+                for (int z = 0; z < NZ; ++z) zacc[h][z] *= alpha;
+                // value accumulators: thread (gq, tq) of n-tile nt holds head 4 nt + tq
+                if (tq == (h & 3)) {
+#pragma unroll
+                    for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pv[h >> 2][mt][e] *= alpha;
+                }
+                m_ref[h] = mx;
+            }
+            p[h] = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_ref[h]);
+            l_part[h] += p[h];
+        }
+
+        // ---------------- probability operands: word (set, head, pair, piece)
+        // of page pl holds tokens (pair, pair + 8) as fp16 halves
+        {
+            __half* pb = reinterpret_cast<__half*>(pbw + pl * sl.pls) + hf;
+            auto put = [&](int set, int h, float x) {
+                const __half hi = __float2half_rn(x);
+                const __half lo = __float2half_rn(x - __half2float(hi));
+                const int wd = (set * H4 + h) * 24 + pair * 2;
+                pb[2 * wd] = hi;
+                pb[2 * wd + 2] = lo;
+            };
+            if constexpr (G32) {
+                constexpr int MW = D / 32;  // {fp16 scale, fp16 zero} per group
+                uint32_t mw[MW];
+#pragma unroll
+                for (int w4 = 0; w4 < MW; w4 += 4) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(pg + L.v_meta + r * L.v_meta_row + 4 * w4);
+                    mw[w4] = u.x;
+                    mw[w4 + 1] = u.y;
+                    mw[w4 + 2] = u.z;
+                    mw[w4 + 3] = u.w;
+                }
+#pragma unroll
+                for (int gr = 0; gr < MW; ++gr) {
+                    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&mw[gr]));
+                    const float sv = valid ? sz.x : 0.f, zv = valid ? sz.y : 0.f;
+#pragma unroll
+                    for (int h = 0; h < H4; ++h) {
+                        if (h < hc) put(gr, h, p[h] * sv);
+                        zacc[h][gr] = fmaf(p[h], zv, zacc[h][gr]);
+                    }
+                }
+            } else {
+                const float nv = valid ? __half2float(*reinterpret_cast<const __half*>(pg + L.v_meta + 2 * r)) : 0.f;
+#pragma unroll
+                for (int h = 0; h < H4; ++h) {
+                    const float pn = p[h] * nv;
+                    if (h < hc)
+#pragma unroll
+                        for (int P = 0; P < NPV; ++P) put(P, h, pn * v_beta[P]);
+                    zacc[h][0] = fmaf(v_dc, pn, zacc[h][0]);
+                }
+            }
         }
         __syncwarp();
 
-        // ---------------- values: code operands x probability operands
-        {
-            const int bh = gq >> 1, bpc = gq & 1;  // B column gq -> (head, piece)
+        // ---------------- values of this warp's two pages
+#pragma unroll
+        for (int pl2 = 0; pl2 < 2; ++pl2) {
+            const int pjw = 2 * warp + pl2;
+            if (pjw >= np) break;
+            const uint8_t* pgw = tile + pjw * L.page_bytes;
+            const uint32_t* pbr = pbw + pl2 * sl.pls + (gq >> 1) * 24 + (gq & 1) + 2 * tq;  // + (set*H4 + 4 nt)*24
             if constexpr (G32) {
                 constexpr int TB = D * VB / 64;  // bytes of a token row per thread role
                 constexpr int TW = TB / 4;
                 uint32_t va[TW], vb2[TW], vc[TW], vd[TW];
-                const uint8_t* vrow = pg + L.v_codes + TB * gq;
+                const uint8_t* vrow = pgw + L.v_codes + TB * gq;
 #pragma unroll
                 for (int w = 0; w < TW; ++w) {
-                    va[w] = *reinterpret_cast<const uint32_t*>(vrow + (2 * tq) * L.v_code_row + 4 * w);
-                    vb2[w] = *reinterpret_cast<const uint32_t*>(vrow + (2 * tq + 1) * L.v_code_row + 4 * w);
-                    vc[w] = *reinterpret_cast<const uint32_t*>(vrow + (2 * tq + 8) * L.v_code_row + 4 * w);
-                    vd[w] = *reinterpret_cast<const uint32_t*>(vrow + (2 * tq + 9) * L.v_code_row + 4 * w);
+                    va[w] = *reinterpret_cast<const uint32_t*>(vrow + tq * L.v_code_row + 4 * w);
+                    vb2[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 8) * L.v_code_row + 4 * w);
+                    vc[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 4) * L.v_code_row + 4 * w);
+                    vd[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 12) * L.v_code_row + 4 * w);
                 }
 #pragma unroll
                 for (int mt = 0; mt < NMT; ++mt) {
                     const int gr = mt >> 1;
-                    const __half* bp = &pbuf[((gr * 4 + bh) * 2 + bpc) * 16 + 2 * tq];
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
                     const int byte = VB == 4 ? mt : (mt >> 1);
                     const uint32_t sb = byte & 3;
                     const uint32_t sel = sb | (sb << 4) | ((4 + sb) << 8) | ((4 + sb) << 12);
@@ -730,131 +934,139 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
                         a2 = r89 & (0x00030003u << sh);
                         a3 = r89 & (0x000C000Cu << sh);
                     }
-                    mma_f16(pv[mt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+                    for (int nt = 0; nt < NTH; ++nt) {
+                        const uint32_t* bp = pbr + (gr * H4 + 4 * nt) * 24;
+                        mma_f16(pv[nt][mt], a0, a1, a2, a3, bp[0], bp[8]);
+                    }
                 }
             } else {
                 // value bit-planes: thread role gq owns coordinates (D/8)*gq ... + D/8 - 1
                 constexpr int CB = D / 64;  // bytes of a plane row per thread role (2 or 4)
-                uint32_t wlo[VB][2], whi[VB][2];  // token pairs (2tq, 2tq+1) and (2tq+8, 2tq+9)
+                uint32_t wlo[VB][2], whi[VB][2];  // token pairs (tq, tq+8) and (tq+4, tq+12)
 #pragma unroll
-                for (int p = 0; p < VB; ++p) {
-                    const uint8_t* base = pg + L.v_codes + p * kBlock * (D / 8) + CB * gq;
+                for (int pp = 0; pp < VB; ++pp) {
+                    const uint8_t* base = pgw + L.v_codes + pp * kBlock * (D / 8) + CB * gq;
                     if constexpr (CB == 2) {
-                        const uint32_t ra = *reinterpret_cast<const uint16_t*>(base + (2 * tq) * (D / 8));
-                        const uint32_t rb = *reinterpret_cast<const uint16_t*>(base + (2 * tq + 1) * (D / 8));
-                        const uint32_t rc = *reinterpret_cast<const uint16_t*>(base + (2 * tq + 8) * (D / 8));
-                        const uint32_t rd = *reinterpret_cast<const uint16_t*>(base + (2 * tq + 9) * (D / 8));
-                        wlo[p][0] = ra | (rb << 16);
-                        whi[p][0] = rc | (rd << 16);
-                        wlo[p][1] = whi[p][1] = 0;
+                        const uint32_t ra = *reinterpret_cast<const uint16_t*>(base + tq * (D / 8));
+                        const uint32_t rb = *reinterpret_cast<const uint16_t*>(base + (tq + 8) * (D / 8));
+                        const uint32_t rc = *reinterpret_cast<const uint16_t*>(base + (tq + 4) * (D / 8));
+                        const uint32_t rd = *reinterpret_cast<const uint16_t*>(base + (tq + 12) * (D / 8));
+                        wlo[pp][0] = ra | (rb << 16);
+                        whi[pp][0] = rc | (rd << 16);
+                        wlo[pp][1] = whi[pp][1] = 0;
                     } else {
-                        const uint32_t ra = *reinterpret_cast<const uint32_t*>(base + (2 * tq) * (D / 8));
-                        const uint32_t rb = *reinterpret_cast<const uint32_t*>(base + (2 * tq + 1) * (D / 8));
-                        const uint32_t rc = *reinterpret_cast<const uint32_t*>(base + (2 * tq + 8) * (D / 8));
-                        const uint32_t rd = *reinterpret_cast<const uint32_t*>(base + (2 * tq + 9) * (D / 8));
-                        wlo[p][0] = (ra & 0xFFFFu) | (rb << 16);
-                        wlo[p][1] = (ra >> 16) | (rb & 0xFFFF0000u);
-                        whi[p][0] = (rc & 0xFFFFu) | (rd << 16);
-                        whi[p][1] = (rc >> 16) | (rd & 0xFFFF0000u);
+                        const uint32_t ra = *reinterpret_cast<const uint32_t*>(base + tq * (D / 8));
+                        const uint32_t rb = *reinterpret_cast<const uint32_t*>(base + (tq + 8) * (D / 8));
+                        const uint32_t rc = *reinterpret_cast<const uint32_t*>(base + (tq + 4) * (D / 8));
+                        const uint32_t rd = *reinterpret_cast<const uint32_t*>(base + (tq + 12) * (D / 8));
+                        wlo[pp][0] = (ra & 0xFFFFu) | (rb << 16);
+                        wlo[pp][1] = (ra >> 16) | (rb & 0xFFFF0000u);
+                        whi[pp][0] = (rc & 0xFFFFu) | (rd << 16);
+                        whi[pp][1] = (rc >> 16) | (rd & 0xFFFF0000u);
                     }
                 }
 #pragma unroll
                 for (int P = 0; P < NPV; ++P) {
                     uint32_t ul[2] = {0, 0}, uh[2] = {0, 0};
 #pragma unroll
-                    for (int p = 0; p < VB; ++p)
-                        if ((plane_subset(VB, P) >> p) & 1) {
-                            ul[0] ^= wlo[p][0];
-                            ul[1] ^= wlo[p][1];
-                            uh[0] ^= whi[p][0];
-                            uh[1] ^= whi[p][1];
+                    for (int pp = 0; pp < VB; ++pp)
+                        if ((plane_subset(VB, P) >> pp) & 1) {
+                            ul[0] ^= wlo[pp][0];
+                            ul[1] ^= wlo[pp][1];
+                            uh[0] ^= whi[pp][0];
+                            uh[1] ^= whi[pp][1];
                         }
-                    const __half* bp = &pbuf[((P * 4 + bh) * 2 + bpc) * 16 + 2 * tq];
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 8);
 #pragma unroll
                     for (int mt = 0; mt < NMT; ++mt) {
+                        // bit k of each half moved to the fp16 sign: 1.0 or -1.0
                         const int wsel = mt >> 3, sh = 2 * (mt & 7);
-                        const uint32_t a0 = (ul[wsel] >> sh) & 0x00010001u;
-                        const uint32_t a1 = (ul[wsel] >> (sh + 1)) & 0x00010001u;
-                        const uint32_t a2 = (uh[wsel] >> sh) & 0x00010001u;
-                        const uint32_t a3 = (uh[wsel] >> (sh + 1)) & 0x00010001u;
-                        mma_f16(pv[mt], a0, a1, a2, a3, b0, b1);
+                        const uint32_t a0 = ((ul[wsel] << (15 - sh)) & 0x80008000u) | 0x3C003C00u;
+                        const uint32_t a1 = ((ul[wsel] << (14 - sh)) & 0x80008000u) | 0x3C003C00u;
+                        const uint32_t a2 = ((uh[wsel] << (15 - sh)) & 0x80008000u) | 0x3C003C00u;
+                        const uint32_t a3 = ((uh[wsel] << (14 - sh)) & 0x80008000u) | 0x3C003C00u;
+#pragma unroll
+                        for (int nt = 0; nt < NTH; ++nt) {
+                            const uint32_t* bp = pbr + (P * H4 + 4 * nt) * 24;
+                            mma_f16(pv[nt][mt], a0, a1, a2, a3, bp[0], bp[8]);
+                        }
                     }
                 }
             }
         }
         __syncwarp();
-        // refill this stage with page j + kStages
-        if (j + kStages < my_pages) {
-            if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            issue(pw + kWarpsPerGroup * (j + kStages), s);
-        }
     }
-    // a wait that gave up leaves copies in flight: drain them (bounded) before
-    // the shared memory is released
-    for (int j = consumed; j < my_pages && j < consumed + kStages; ++j) {
-        const int s = j % kStages;
-        if (!((invalid >> s) & 1)) {
-            mbar_wait(smem_u32(&bars[s]), (phase >> s) & 1, a.dp.err);
-            phase ^= 1u << s;
+    // copies issued but not consumed (a wait gave up) must land before the
+    // shared memory is released
+    if (tid == 0)
+        for (int t = consumed; t < issued; ++t) {
+            const int s = t % S;
+            mbar_wait(smem_u32(&bars[s]), (ring_phase >> s) & 1, a.dp.err);
+            ring_phase ^= 1u << s;
         }
-    }
+    if (!mma_ok) mbar_wait(smem_u32(&bars[S + 1]), mma_phase ^ 1, a.dp.err);
+    tc_fence_before();
+    __syncthreads();
+    if (n_tiles > 0 && warp == 0) tmem_dealloc(tmem, kTmemCols);
 
-    // ---------------- per-warp partial -> smem -> merged split partial
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, 4);
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, 8);
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, 16);
+    // ---------------- per-warp partials -> shared memory -> merged split partial
 #pragma unroll
-    for (int i = 0; i < NZ; ++i) {
-        zacc[i] += __shfl_xor_sync(0xffffffffu, zacc[i], 4);
-        zacc[i] += __shfl_xor_sync(0xffffffffu, zacc[i], 8);
-        zacc[i] += __shfl_xor_sync(0xffffffffu, zacc[i], 16);
+    for (int h = 0; h < H4; ++h) {
+        l_part[h] = warp_sum(l_part[h]);
+#pragma unroll
+        for (int z = 0; z < NZ; ++z) zacc[h][z] = warp_sum(zacc[h][z]);
     }
-    // red[pw][head][0..D-1: acc | D: m | D+1: l]
-    float* my = red + (pw * 4 + tq) * (D + 2);
-    if (head_ok) {
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < H4; ++h) {
+#pragma unroll
+            for (int z = 0; z < NZ; ++z) zsm[h * NZ + z] = zacc[h][z];
+            red[(warp * H4 + h) * (D + 2) + D] = m_ref[h];
+            red[(warp * H4 + h) * (D + 2) + D + 1] = l_part[h];
+        }
+    __syncwarp();
+#pragma unroll
+    for (int nt = 0; nt < NTH; ++nt) {
+        const int head = 4 * nt + tq;
+        float* my = red + (warp * H4 + head) * (D + 2);
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
-            float v0v = pv[mt][0] + pv[mt][1], v1v = pv[mt][2] + pv[mt][3];
+            float v0v = pv[nt][mt][0] + pv[nt][mt][1], v1v = pv[nt][mt][2] + pv[nt][mt][3];
             int c0;
             if constexpr (G32) {
                 // operand scales: 4-bit q*2^-24 (even slot), q*2^-20 (odd slot);
                 // 2-bit q*2^(4(mt%2)-24), q*2^(4(mt%2)-22)
                 const float s0 = VB == 4 ? 16777216.f : ((mt & 1) ? 1048576.f : 16777216.f);
                 const float s1 = VB == 4 ? 1048576.f : ((mt & 1) ? 262144.f : 4194304.f);
+                const float zv = zsm[head * NZ + (mt >> 1)];
                 c0 = 32 * (mt >> 1) + 4 * gq + 2 * (mt & 1);
-                v0v = fmaf(v0v, s0, zacc[mt >> 1]);
-                v1v = fmaf(v1v, s1, zacc[mt >> 1]);
+                v0v = fmaf(v0v, s0, zv);
+                v1v = fmaf(v1v, s1, zv);
             } else {
+                const float zv = zsm[head * NZ];
                 c0 = (D / 8) * gq + 2 * mt;
-                v0v = fmaf(v0v, 16777216.f, zacc[0]);
-                v1v = fmaf(v1v, 16777216.f, zacc[0]);
+                v0v += zv;
+                v1v += zv;
             }
             my[c0] = v0v;
             my[c0 + 1] = v1v;
         }
-        if (gq == 0) {
-            my[D] = m_run;
-            my[D + 1] = l_part;
-        }
     }
     __syncthreads();
-    // merge the page workers of the head group; write (m, l, acc)
-    for (int e = threadIdx.x; e < HG * D; e += blockDim.x) {
+    // merge the four warps; write (m, l, acc) of this split
+    for (int e = threadIdx.x; e < hc * D; e += blockDim.x) {
         const int h = e / D, i = e % D;
         float M = -INFINITY;
-        for (int w = 0; w < kWarpsPerGroup; ++w) M = fmaxf(M, red[(w * 4 + h) * (D + 2) + D]);
+        for (int w = 0; w < kWarpsPerGroup; ++w) M = fmaxf(M, red[(w * H4 + h) * (D + 2) + D]);
         float acc = 0.f, l = 0.f;
         for (int w = 0; w < kWarpsPerGroup; ++w) {
-            const float* r = red + (w * 4 + h) * (D + 2);
-            if (r[D] == -INFINITY) continue;
-            const float wt = exp2f(r[D] - M);
-            acc = fmaf(wt, r[i], acc);
-            l = fmaf(wt, r[D + 1], l);
+            const float* rr = red + (w * H4 + h) * (D + 2);
+            if (rr[D] == -INFINITY) continue;
+            const float wt = exp2f(rr[D] - M);
+            acc = fmaf(wt, rr[i], acc);
+            l = fmaf(wt, rr[D + 1], l);
         }
-        const int64_t idx = ((int64_t)b * a.q_heads + g * a.group + hg * 4 + h) * a.sp.n_splits + chunk;
+        const int64_t idx = ((int64_t)b * a.q_heads + g * a.group + hgi * hc + h) * a.sp.n_splits + chunk;
         a.ws_acc[idx * D + i] = acc;
         if (i == 0) {
             a.ws_ml[idx * 2] = M;
@@ -924,9 +1136,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------------- split dispatch
-template <int D, int KB, int NT, bool G32, int VB>
+template <int D, int KB, bool G32, int VB, int NTH>
 inline tq_status launch_split(const DecodeArgs& a, cudaStream_t s, size_t smem) {
-    auto kern = split_kernel<D, KB, NT, G32, VB>;
+    auto kern = split_kernel<D, KB, G32, VB, NTH>;
     static bool attr_set = false;  // once per kernel instance, before any capture
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
@@ -937,26 +1149,53 @@ inline tq_status launch_split(const DecodeArgs& a, cudaStream_t s, size_t smem) 
     return TQ_OK;
 }
 
-template <int D, int KB, int NT>
+template <int D, int KB, int NTH>
 inline tq_status dispatch_v(const DecodeArgs& a, cudaStream_t s, size_t smem) {
     if (a.lay.v_mode == TQ_V_G32)
-        return a.lay.v_bits == 4 ? launch_split<D, KB, NT, true, 4>(a, s, smem)
-                                 : launch_split<D, KB, NT, true, 2>(a, s, smem);
+        return a.lay.v_bits == 4 ? launch_split<D, KB, true, 4, NTH>(a, s, smem)
+                                 : launch_split<D, KB, true, 2, NTH>(a, s, smem);
     switch (a.lay.v_bits) {
-        case 2: return launch_split<D, KB, NT, false, 2>(a, s, smem);
-        case 3: return launch_split<D, KB, NT, false, 3>(a, s, smem);
-        default: return launch_split<D, KB, NT, false, 4>(a, s, smem);
+        case 2: return launch_split<D, KB, false, 2, NTH>(a, s, smem);
+        case 3: return launch_split<D, KB, false, 3, NTH>(a, s, smem);
+        default: return launch_split<D, KB, false, 4, NTH>(a, s, smem);
     }
 }
 
 template <int D, int KB>
-inline tq_status dispatch_nt(const DecodeArgs& a, cudaStream_t s, size_t smem) {
-    return a.gm.nt == 2 ? dispatch_v<D, KB, 2>(a, s, smem) : dispatch_v<D, KB, 1>(a, s, smem);
+inline tq_status dispatch_nth(const DecodeArgs& a, cudaStream_t s, size_t smem) {
+    if constexpr (D == 128)
+        if (a.gm.nth == 2) return dispatch_v<D, KB, 2>(a, s, smem);
+    return dispatch_v<D, KB, 1>(a, s, smem);
 }
 
 // split-kernel launch for one (head dim, key bits); each pair is compiled in
 // its own translation unit
 template <int D, int KB>
 tq_status dispatch_split(const DecodeArgs& a, cudaStream_t s, size_t smem);
+
+// Ring depth and dynamic shared memory of the split launch: the deepest ring
+// (4..2 tiles) that keeps two CTAs per SM, else the deepest that fits one.
+// At least 80 KB is requested so that no third CTA competes for tensor memory.
+template <int D>
+inline tq_status split_config(const DecodeArgs& a, int* stages, size_t* smem) {
+    const int nsets = a.lay.v_mode == TQ_V_G32 ? D / 32 : (1 << (a.lay.v_bits - 1));
+    const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
+    const size_t limits[2] = {112 * 1024, 226 * 1024};
+    for (size_t lim : limits)
+        for (int st = 4; st >= 2; --st) {
+            const SplitLayout sl = split_layout<D>(a.lay.page_bytes, a.gm, nsets, st);
+            size_t need = std::max(sl.total, a.tail_cap > 0 ? tail_smem : (size_t)0);
+            if (need > lim || (size_t)st * sl.tile < split_red_bytes<D>(4 * a.gm.nth)) continue;
+            *stages = st;
+            *smem = std::max(need, (size_t)80 * 1024);
+            return TQ_OK;
+        }
+    return TQ_ERR_UNSUPPORTED;
+}
+
+// prep -> split (optionally bracketed by profiling events) -> combine on the
+// caller's stream.  Defined in tq_decode.cu, the one translation unit that
+// instantiates the prep and combine kernels.
+tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1);
 
 }  // namespace tq

@@ -35,32 +35,6 @@ static tq_status scratch_address(uint8_t** out) {
     return TQ_OK;
 }
 
-template <int D>
-static tq_status launch_noalloc(const DecodeArgs& a, cudaStream_t s) {
-    const size_t prep_smem = (size_t)3 * a.group * D * 4 + (size_t)a.group * 2 * 4;
-    static bool prep_attr = false;
-    if (!prep_attr) {
-        if (cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return TQ_ERR_CUDA;
-        prep_attr = true;
-    }
-    const size_t main_smem = SplitSmem<D>::total(a.lay.page_bytes);
-    const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
-    const size_t smem = std::max(main_smem, a.tail_cap > 0 ? tail_smem : (size_t)0);
-    if (smem > 227 * 1024 || prep_smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
-    prep_kernel<D><<<dim3(a.heads, a.batch), 256, prep_smem, s>>>(a);
-    tq_status st;
-    switch (a.lay.k_bits) {
-        case 2: st = dispatch_split<D, 2>(a, s, smem); break;
-        case 3: st = dispatch_split<D, 3>(a, s, smem); break;
-        default: st = dispatch_split<D, 4>(a, s, smem); break;
-    }
-    if (st != TQ_OK) return st;
-    combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, 0, s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-}
-
 }  // namespace tq
 
 using namespace tq;
@@ -110,10 +84,10 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache* c, const void* 
     a.gm = c->geom;
     // every scratch byte read below is written earlier by the same call
     a.ws_q = reinterpret_cast<float*>(ws + wl.q);
-    a.ws_frag = reinterpret_cast<uint32_t*>(ws + wl.frag);
+    a.ws_bimg = ws + wl.bimg;
     a.ws_cst = reinterpret_cast<float*>(ws + wl.cst);
     a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
     a.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
     cudaStream_t s = (cudaStream_t)stream;
-    return d == 128 ? launch_noalloc<128>(a, s) : launch_noalloc<256>(a, s);
+    return launch_decode(a, s, nullptr, nullptr);
 }

@@ -5,7 +5,7 @@ namespace tq {
 
 template <>
 tq_status dispatch_split<128, 4>(const DecodeArgs& a, cudaStream_t s, size_t smem) {
-    return dispatch_nt<128, 4>(a, s, smem);
+    return dispatch_nth<128, 4>(a, s, smem);
 }
 
 }  // namespace tq

@@ -5,7 +5,7 @@ namespace tq {
 
 template <>
 tq_status dispatch_split<256, 3>(const DecodeArgs& a, cudaStream_t s, size_t smem) {
-    return dispatch_nt<256, 3>(a, s, smem);
+    return dispatch_nth<256, 3>(a, s, smem);
 }
 
 }  // namespace tq

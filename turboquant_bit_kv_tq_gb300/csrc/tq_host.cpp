@@ -79,6 +79,8 @@ ParamsLayout params_layout(const tq_cache_config& c) {
     off = up256(off + d * d * 4);
     p.s_bf16 = off;
     off = up256(off + d * d * 2);
+    p.st_bf16 = off;
+    off = up256(off + d * d * 2);
     p.k_cent = off;
     off = up256(off + kMaxLevels * 4);
     p.k_bound = off;
@@ -100,12 +102,14 @@ ParamsLayout params_layout(const tq_cache_config& c) {
 DecodeGeom decode_geom(const tq_cache_config& c) {
     DecodeGeom g;
     const int G = c.num_q_heads / c.num_kv_heads;
-    g.hg = G < 4 ? G : 4;
-    g.nhg = G <= 4 ? 1 : G / 4;
-    g.nt = (4 * g.hg + 7) / 8;
+    // value accumulators stay in registers: at most 8 heads at d=128, 4 at d=256
+    g.hc = G <= 4 ? G : (c.head_dim == 128 && G % 8 == 0 ? 8 : 4);
+    g.nhg = G / g.hc;
+    g.nth = (g.hc + 3) / 4;
     g.npk = 1 << (c.k_bits - 1);
     g.npl = g.npk + (c.k_qjl ? 1 : 0);
-    g.frag_words = g.nhg * g.npl * (c.head_dim / 32) * g.nt * 2 * 32;
+    g.n_cols = (kPieces * 4 * g.nth + 15) / 16 * 16;
+    g.bimg_bytes = g.n_cols * g.npl * c.head_dim;
     return g;
 }
 
@@ -117,8 +121,8 @@ WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     size_t off = 0;
     w.q = off;
     off = up256(off + bh * 3 * d * 4);
-    w.frag = off;
-    off = up256(off + size_t(c.max_batch) * c.num_kv_heads * gm.frag_words * 4);
+    w.bimg = off;
+    off = up256(off + size_t(c.max_batch) * c.num_kv_heads * gm.nhg * gm.bimg_bytes);
     w.cst = off;
     off = up256(off + bh * 4 * 4);
     w.acc = off;
@@ -375,11 +379,13 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     float* s32 = (float*)(img.data() + pl.s_f32);
     float* st32 = (float*)(img.data() + pl.st_f32);
     uint16_t* s16 = (uint16_t*)(img.data() + pl.s_bf16);
+    uint16_t* st16 = (uint16_t*)(img.data() + pl.st_bf16);
     for (int i = 0; i < d; ++i) signs[i] = h->signs[i];
     for (int j = 0; j < d; ++j)
         for (int i = 0; i < d; ++i) {
             const uint16_t bits = h->s_bf16[(size_t)j * d + i];
             s16[(size_t)j * d + i] = bits;
+            st16[(size_t)i * d + j] = bits;
             s32[(size_t)j * d + i] = bf16_to_float(bits);
             st32[(size_t)i * d + j] = bf16_to_float(bits);
         }
@@ -405,6 +411,7 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     h->dp.s_f32 = (const float*)(base + pl.s_f32);
     h->dp.st_f32 = (const float*)(base + pl.st_f32);
     h->dp.s_bf16 = (const uint16_t*)(base + pl.s_bf16);
+    h->dp.st_bf16 = (const uint16_t*)(base + pl.st_bf16);
     h->dp.k_cent = (const float*)(base + pl.k_cent);
     h->dp.k_bound = (const float*)(base + pl.k_bound);
     h->dp.v_cent = (const float*)(base + pl.v_cent);
@@ -416,7 +423,7 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     uint8_t* ws = (uint8_t*)workspace_dev;
     h->geom = decode_geom(*cfg);
     h->ws_q = (float*)(ws + wl.q);
-    h->ws_frag = (uint32_t*)(ws + wl.frag);
+    h->ws_bimg = (uint8_t*)(ws + wl.bimg);
     h->ws_cst = (float*)(ws + wl.cst);
     h->ws_acc = (float*)(ws + wl.acc);
     h->ws_ml = (float*)(ws + wl.ml);

@@ -28,6 +28,7 @@ struct DeviceParams {
     const float* s_f32;      // S row-major [d][d]
     const float* st_f32;     // S^T [d][d] (st[i*d + j] = S[j][i])
     const uint16_t* s_bf16;  // S row-major, bf16 bits
+    const uint16_t* st_bf16; // S^T, bf16 bits
     const float* k_cent;     // [16] key centroids (padded)
     const float* k_bound;    // [16] key boundaries
     const float* v_cent;     // [16] value centroids (MSE)
@@ -54,21 +55,28 @@ struct Splits {
 };
 
 struct ParamsLayout {
-    size_t signs, s_f32, st_f32, s_bf16, k_cent, k_bound, v_cent, v_bound, k_walsh, v_walsh, err, total;
+    size_t signs, s_f32, st_f32, s_bf16, st_bf16, k_cent, k_bound, v_cent, v_bound, k_walsh, v_walsh, err, total;
 };
 
-// Decode geometry: query heads per head group (<= 4, one CTA each), head
-// groups per KV head, score n-tiles, key code planes, score planes (+ QJL) and
-// score-operand words per (batch, KV head).
+// Query-side fp8 pieces of the score contraction: piece k carries the
+// residual of pieces 0..k-1 times 16^k, ~4 significant bits each (~20 in all).
+constexpr int kPieces = 5;
+
+// Decode geometry.  One split CTA serves a head group of hc query heads
+// (nhg groups per KV head); its value contraction runs in nth n-tiles of 4
+// heads; the score contraction has npl planes (npk key code planes + the QJL
+// sign plane) and n_cols columns, kPieces per head (4 nth heads, rounded up to
+// a multiple of 16).  bimg_bytes is the score operand image of one head group:
+// n_cols rows of npl*d fp8 bytes in the tensor-core shared-memory layout.
 struct DecodeGeom {
-    int hg, nhg, nt, npk, npl, frag_words;
+    int hc, nhg, nth, npk, npl, n_cols, bimg_bytes;
 };
 DecodeGeom decode_geom(const tq_cache_config& c);
 
 struct WorkspaceLayout {
-    // q: [B][Hq][3][d] fp32; frag: [B][Hkv][frag_words] u32 (score operands);
+    // q: [B][Hq][3][d] fp32; bimg: [B][Hkv][nhg][bimg_bytes] (score operands);
     // cst: [B][Hq][4] fp32; acc: [B][Hq][S][d]; ml: [B][Hq][S][2]
-    size_t q, frag, cst, acc, ml, total;
+    size_t q, bimg, cst, acc, ml, total;
 };
 
 tq_status compute_layout(const tq_cache_config& c, Layout* lay);
@@ -85,7 +93,7 @@ struct tq_cache {
     tq::DeviceParams dp;
     tq::DecodeGeom geom;
     float* ws_q;
-    uint32_t* ws_frag;
+    uint8_t* ws_bimg;
     float* ws_cst;
     float* ws_acc;
     float* ws_ml;
