@@ -113,6 +113,15 @@ typedef struct tq_cache tq_cache;
 const char* tq_status_string(tq_status s);
 
 /*
+ * The CUDA runtime's name and message for the most recent failing CUDA call
+ * made by this library on the calling host thread (the cause behind a
+ * TQ_ERR_CUDA status); "" if there was none.  The pointer stays valid until
+ * the next library call on the same thread.  Diagnostic only: the pages have
+ * no counterpart.
+ */
+const char* tq_last_cuda_error(void);
+
+/*
  * Lloyd-Max codebook for one coordinate of a randomly rotated unit vector in
  * R^d ([Hub] step 2: the rotated coordinate is Beta distributed; density
  * f(t) ~ (1-t^2)^((d-3)/2) on [-1,1]).  Host only, deterministic.

@@ -16,7 +16,7 @@ import numpy as np
 __all__ = [
     "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_V_MSE", "TQ_V_G32",
     "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
-    "library_path", "load_library", "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs",
+    "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
     "tq_get_device_error", "TQCache",
@@ -31,7 +31,7 @@ TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIM
 EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
-    "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc",
+    "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -39,7 +39,10 @@ TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 class TQError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__(f"{what}: {tq_status_string(status)} ({status})")
+        msg = f"{what}: {tq_status_string(status)} ({status})"
+        if status == -4:
+            msg += f" [{tq_last_cuda_error()}]"
+        super().__init__(msg)
 
 
 class tq_cache_config(ctypes.Structure):
@@ -89,6 +92,7 @@ def load_library():
         sz = ctypes.POINTER(ctypes.c_size_t)
         sig = {
             "tq_status_string": (ctypes.c_char_p, [i32]),
+            "tq_last_cuda_error": (ctypes.c_char_p, []),
             "tq_make_codebook": (i32, [i32, i32, dp, dp, dp]),
             "tq_make_rotation_signs": (i32, [i32, u64, ctypes.POINTER(ctypes.c_float)]),
             "tq_make_qjl_matrix": (i32, [i32, u64, ctypes.POINTER(ctypes.c_uint16)]),
@@ -117,6 +121,11 @@ def _check(status, what):
 
 def tq_status_string(status):
     return load_library().tq_status_string(status).decode()
+
+
+def tq_last_cuda_error():
+    """The CUDA runtime message behind the last TQ_ERR_CUDA on this thread."""
+    return load_library().tq_last_cuda_error().decode()
 
 
 def _dptr(a):

@@ -3,7 +3,7 @@
 
 #include <algorithm>
 
-#include "tq_decode_kernels.cuh"
+#include "tq_decode_ws.cuh"
 
 namespace tq {
 
@@ -17,22 +17,53 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
             return TQ_ERR_CUDA;
         prep_attr = true;
     }
-    size_t smem = 0;
-    const tq_status cfg = split_config<D>(a, &a.stages, &smem);
-    if (cfg != TQ_OK) return cfg;
     if (prep_smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
+    size_t smem = 0;
+    int grid = 0;
+    if (ws_fits(a.gm, D)) {
+        // persistent warp-specialized split kernel: two CTAs per SM, the
+        // deepest ring that fits; the exact tail runs as its own kernel
+        static int sms = 0;
+        if (sms == 0) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+                return TQ_ERR_CUDA;
+        }
+        const int n_items = a.batch * a.heads * a.gm.nhg * a.sp.n_chunks;
+        const int kitems = ws_items_per_cta(n_items, std::min(n_items, kWsCtasPerSm * sms));
+        grid = (n_items + kitems - 1) / kitems;  // contiguous runs of kitems items
+        const int nsets = a.lay.v_mode == TQ_V_G32 ? D / 32 : (1 << (a.lay.v_bits - 1));
+        a.stages = 0;
+        for (int st = kWsMaxStages; st >= 2 && a.stages == 0; --st) {
+            const WsLayout wl = ws_layout<D>(a.lay.page_bytes, a.gm, nsets, st, kitems, a.split_blocks);
+            if (wl.total <= 112 * 1024) {
+                a.stages = st;
+                smem = std::max(wl.total, (size_t)77 * 1024);  // never a third CTA per SM (tensor memory)
+            }
+        }
+        if (a.stages == 0) grid = 0;  // too many items per CTA for the staged schedule
+    }
+    if (grid == 0) {
+        const tq_status cfg = split_config<D>(a, &a.stages, &smem);
+        if (cfg != TQ_OK) return cfg;
+    }
     prep_kernel<D><<<dim3(a.heads, a.batch), 256, prep_smem, s>>>(a);
+    if (grid > 0 && a.tail_cap > 0) {
+        const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
+        tail_kernel<D><<<dim3(a.heads, a.batch), 128, tail_smem, s>>>(a);
+    }
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
     tq_status st;
     switch (a.lay.k_bits) {
-        case 2: st = dispatch_split<D, 2>(a, s, smem); break;
-        case 3: st = dispatch_split<D, 3>(a, s, smem); break;
-        default: st = dispatch_split<D, 4>(a, s, smem); break;
+        case 2: st = dispatch_split<D, 2>(a, s, smem, grid); break;
+        case 3: st = dispatch_split<D, 3>(a, s, smem, grid); break;
+        default: st = dispatch_split<D, 4>(a, s, smem, grid); break;
     }
     if (st != TQ_OK) return st;
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
     combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, 0, s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1) {

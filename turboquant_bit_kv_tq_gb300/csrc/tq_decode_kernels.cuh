@@ -161,6 +161,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)_
 // bounded mbarrier wait; records TQ_DEVERR_TIMEOUT and returns false if the
 // phase never completes
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+#pragma unroll 1
     for (int it = 0; it < (1 << 24); ++it) {
         uint32_t done;
         asm volatile(
@@ -1141,12 +1142,14 @@ inline tq_status launch_split(const DecodeArgs& a, cudaStream_t s, size_t smem) 
     auto kern = split_kernel<D, KB, G32, VB, NTH>;
     static bool attr_set = false;  // once per kernel instance, before any capture
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return TQ_ERR_CUDA;
+        {
+            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+            if (fs != TQ_OK) return fs;
+        }
         attr_set = true;
     }
     kern<<<dim3(a.sp.n_splits, a.heads * a.gm.nhg, a.batch), 32 * kWarpsPerGroup, smem, s>>>(a);
-    return TQ_OK;
+    return cuda_status(cudaGetLastError());
 }
 
 template <int D, int KB, int NTH>
@@ -1169,9 +1172,10 @@ inline tq_status dispatch_nth(const DecodeArgs& a, cudaStream_t s, size_t smem) 
 }
 
 // split-kernel launch for one (head dim, key bits); each pair is compiled in
-// its own translation unit
+// its own translation unit.  grid > 0: the warp-specialized persistent kernel
+// (tq_decode_ws.cuh) on `grid` CTAs; grid == 0: split_kernel.
 template <int D, int KB>
-tq_status dispatch_split(const DecodeArgs& a, cudaStream_t s, size_t smem);
+tq_status dispatch_split(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid);
 
 // Ring depth and dynamic shared memory of the split launch: the deepest ring
 // (4..2 tiles) that keeps two CTAs per SM, else the deepest that fits one.

@@ -1,0 +1,850 @@
+// Warp-specialized, persistent split kernel of the decode path (included by
+// the split translation units after tq_decode_kernels.cuh).
+//
+// Two CTAs per SM (bulk-copy throughput is per CTA) each walk a list of work
+// items (one split of one KV head's head group of one sequence) as a stream of
+// 128-token tiles, with two warpgroups running concurrently and handing tiles
+// over through mbarriers:
+//   scores     (warps 0-3, thread t = token t of the tile): expand the key
+//              bit-planes into fp8 operands in tensor memory; thread 0 issues
+//              the tcgen05 MMAs into the accumulator columns, and the bulk
+//              async copies of the tiles' pages (a ring of `stages` tiles) and
+//              of each item's query operand image (two buffers) ahead of use
+//   consumers  (warps 4-7, same token mapping): read the scores, online exp2
+//              softmax, probability operands, value contraction of the warp's
+//              two pages on fp16 tensor cores, per-item merge of the partials
+// so that the expansion and MMAs of tile i+1 overlap the value contraction of
+// tile i.  The score and value arithmetic is the
+// same as in split_kernel (tq_decode_kernels.cuh).
+#pragma once
+
+#include "tq_decode_kernels.cuh"
+
+namespace tq {
+
+constexpr int kWsWarps = 8;  // 4 score + 4 consumer
+constexpr int kWsThreads = 32 * kWsWarps;
+constexpr int kWsMaxStages = 8;
+constexpr int kWsCtasPerSm = 2;   // bulk-copy throughput is per CTA: two CTAs per SM stream ~1.7x one
+constexpr int kWsTmemCols = 256;  // 512 / kWsCtasPerSm
+// setmaxnreg split of the 256 x 128 registers a CTA launches with (score
+// warpgroup + consumer warpgroup = 2 x 128): configurations with larger value
+// accumulators move more registers to the consumers
+__host__ __device__ constexpr int ws_regs_cons(int d, int nth, bool g32) { return (nth == 2 || (d == 256 && g32)) ? 184 : 152; }
+__host__ __device__ constexpr int ws_regs_score(int d, int nth, bool g32) { return 256 - ws_regs_cons(d, nth, g32); }
+
+// tensor-memory plan: one accumulator buffer of 2*score_cols (key | sign),
+// then one A operand buffer
+__host__ __device__ constexpr int ws_dcols(int nth) { return 2 * score_cols(nth); }
+__host__ __device__ constexpr int ws_acap(int nth) { return kWsTmemCols - ws_dcols(nth); }
+
+struct WsLayout {
+    size_t tile, ring, bimg, pbuf, zsm, red, items, icst, ids, smask, bars, tslot, total;
+    int pls, pbuf_words;
+};
+
+struct WsItem {
+    int b, g, hgi, chunk, t0, t1, n_pages, n_tiles;
+    // query operand image: buffer slot, whether this item loads it (and the
+    // load's index among the slot's loads) and whether the slot is released
+    // after the item's last MMA
+    int slot, load, lidx, release;
+};
+
+// items per CTA (the largest share of the round-robin distribution)
+__host__ __device__ inline int ws_items_per_cta(int n_items, int grid) { return (n_items + grid - 1) / grid; }
+
+// kitems: items per CTA; split_blocks: pages per item at most
+// image buffers: one per head group of a KV head (at most two)
+__host__ __device__ inline int ws_nimg(const DecodeGeom& gm) { return gm.nhg < 2 ? 1 : 2; }
+
+template <int D>
+__host__ __device__ inline WsLayout ws_layout(int page_bytes, const DecodeGeom& gm, int nsets, int stages,
+                                              int kitems, int split_blocks) {
+    auto up = [](size_t x) { return (x + 127) & ~(size_t)127; };
+    const int h4 = 4 * gm.nth;
+    WsLayout l;
+    l.tile = up((size_t)kTilePages * page_bytes);
+    l.pls = nsets * h4 * 24 + 16;
+    l.pbuf_words = 2 * l.pls;
+    size_t off = 0;
+    l.ring = off;
+    off = up(off + (size_t)stages * l.tile);
+    l.bimg = off;
+    off = up(off + (size_t)ws_nimg(gm) * gm.bimg_bytes);
+    // the per-item merge buffer reuses the probability buffers
+    l.pbuf = l.red = off;
+    const size_t pb = (size_t)4 * l.pbuf_words * 4, rb = (size_t)4 * h4 * (D + 2) * 4;
+    off = up(off + (pb > rb ? pb : rb));
+    l.zsm = off;
+    off = up(off + (size_t)4 * h4 * (D / 32) * 4);
+    l.items = off;
+    off = up(off + (size_t)kitems * sizeof(WsItem));
+    l.icst = off;
+    off = up(off + (size_t)kitems * h4 * 4 * 4);
+    l.ids = off;
+    off = up(off + (size_t)kitems * split_blocks * 4);
+    l.smask = off;
+    off = up(off + (size_t)stages * 4);
+    l.bars = off;
+    off = up(off + (size_t)(2 * stages + 8) * 8);
+    l.tslot = off;
+    off = up(off + 4);
+    l.total = off;
+    return l;
+}
+
+// a configuration runs here when all its score planes fit one A buffer
+__host__ __device__ inline bool ws_fits(const DecodeGeom& gm, int d) { return gm.npl * (d / 4) <= ws_acap(gm.nth); }
+
+// work item idx: head group fastest, then split, KV head, sequence; every CTA
+// takes a contiguous run of items, so consecutive items of a CTA mostly share
+// their query operand images and re-read the pages of the other head group
+// from L2
+__device__ inline WsItem ws_item(const DecodeArgs& a, int idx, bool* len_bad) {
+    WsItem it;
+    const int nhg = a.gm.nhg, nch = a.sp.n_chunks;
+    it.hgi = idx % nhg;
+    idx /= nhg;
+    it.chunk = idx % nch;
+    idx /= nch;
+    it.g = idx % a.heads;
+    it.b = idx / a.heads;
+    int len = a.seq_lens[it.b];
+    *len_bad = len < 0 || len > a.max_blocks * kBlock;
+    len = max(0, min(len, a.max_blocks * kBlock));
+    it.t0 = it.chunk * a.split_blocks * kBlock;
+    it.t1 = min(len, it.t0 + a.split_blocks * kBlock);
+    it.n_pages = it.t1 > it.t0 ? (it.t1 - it.t0 + kBlock - 1) / kBlock : 0;
+    it.n_tiles = (it.n_pages + kTilePages - 1) / kTilePages;
+    return it;
+}
+
+// non-blocking: has the phase of the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// bounded wait that is skipped once the caller has given up (dead)
+__device__ __forceinline__ void ws_wait(uint32_t bar, uint32_t parity, bool& dead, uint32_t* err) {
+    if (!dead) dead = !mbar_wait(bar, parity, err);
+}
+
+// Copy issue cursor of a split CTA (one thread): walks the tiles of the CTA's
+// non-empty items in order, loading an item's query operand image before its
+// first tile when it needs one.  issue_upto runs up to limit_seq, blocking only
+// for tiles up to need_seq (whose stage releases depend on MMAs already
+// issued) and otherwise stopping at the first stage or image not yet free.
+// Out of line so that the kernel holds one copy of it.
+struct WsIssuer {
+    const WsItem* items;
+    const int32_t* ids;
+    uint32_t* smask;
+    uint8_t* ring;
+    uint8_t* bimg;
+    uint64_t *full, *empty, *bfull, *bempty;
+    const uint8_t* cache;
+    const uint8_t* ws_bimg;
+    uint32_t* err;
+    size_t tile;
+    int nk, SB, S, page_bytes, bimg_bytes, heads, nhg;
+    int64_t num_blocks;
+    int c_k = 0, c_t = 0, c_seq = 0;
+    bool c_img = false, dead = false;
+
+    __device__ void next_item() {
+        while (c_k < nk && items[c_k].n_tiles == 0) ++c_k;
+    }
+
+    __device__ __noinline__ void issue_upto(int limit_seq, int need_seq, int max_tiles) {
+#pragma unroll 1
+        for (int n = 0; c_k < nk && c_seq <= limit_seq && !dead && (n < max_tiles || c_seq <= need_seq); ++n) {
+            const WsItem& it = items[c_k];
+            if (!c_img) {
+                if (it.load) {
+                    if (it.lidx >= 1) {
+                        const uint32_t par = (it.lidx - 1) & 1;
+                        const uint32_t bar = smem_u32(&bempty[it.slot]);
+                        if (c_seq <= need_seq)
+                            dead = !mbar_wait(bar, par, err);
+                        else if (!mbar_test(bar, par))
+                            break;
+                        if (dead) break;
+                    }
+                    mbar_expect_tx(smem_u32(&bfull[it.slot]), bimg_bytes);
+                    bulk_copy(smem_u32(bimg + (size_t)it.slot * bimg_bytes),
+                              ws_bimg + (((int64_t)it.b * heads + it.g) * nhg + it.hgi) * bimg_bytes, bimg_bytes,
+                              smem_u32(&bfull[it.slot]));
+                }
+                c_img = true;
+            }
+            const int s = c_seq % S;
+            if (c_seq >= S) {
+                const uint32_t par = ((c_seq / S) - 1) & 1;
+                if (c_seq <= need_seq)
+                    dead = !mbar_wait(smem_u32(&empty[s]), par, err);
+                else if (!mbar_test(smem_u32(&empty[s]), par))
+                    break;
+                if (dead) break;
+            }
+            // the consumers' reads of this stage happen-before the copies
+            // through the empty barrier (release/acquire)
+            const int32_t* cid = ids + c_k * SB;
+            const int p0 = c_t * kTilePages, np = min(kTilePages, it.n_pages - p0);
+            uint32_t bytes = 0, mask = 0;
+#pragma unroll 1
+            for (int j = 0; j < np; ++j) {
+                const int blk = cid[p0 + j];
+                if (blk >= 0 && blk < num_blocks) {
+                    bytes += page_bytes;
+                    mask |= 1u << j;
+                } else {
+                    set_error(err, TQ_DEVERR_BLOCK);
+                }
+            }
+            smask[s] = mask;  // published by the arrive below
+            mbar_expect_tx(smem_u32(&full[s]), bytes);
+#pragma unroll 1
+            for (int j = 0; j < np; ++j)
+                if ((mask >> j) & 1)
+                    bulk_copy(smem_u32(ring + s * tile + (size_t)j * page_bytes),
+                              cache + ((int64_t)cid[p0 + j] * heads + it.g) * page_bytes, page_bytes,
+                              smem_u32(&full[s]));
+            ++c_seq;
+            if (++c_t == it.n_tiles) {
+                c_t = 0;
+                c_img = false;
+                ++c_k;
+                next_item();
+            }
+        }
+    }
+};
+
+template <int D, int KB, bool G32, int VB, int NTH>
+__global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(DecodeArgs a) {
+    constexpr int NPK = 1 << (KB - 1);
+    constexpr int NW = D / 32;
+    constexpr int NCOL = D / 4;
+    constexpr int NMT = D / 16;
+    constexpr int NPV = G32 ? 1 : (1 << (VB - 1));
+    constexpr int NSET = G32 ? D / 32 : NPV;
+    constexpr int NZ = G32 ? D / 32 : 1;
+    constexpr int H4 = 4 * NTH;
+    constexpr int NCOLS = score_cols(NTH);
+    constexpr int DC = ws_dcols(NTH);  // accumulator columns (key | sign)
+    constexpr int TA = DC;             // first A operand column
+    extern __shared__ __align__(16) uint8_t smem[];
+    const DecodeGeom gm = a.gm;
+    const Layout& L = a.lay;
+    const int S = a.stages;
+    const int n_items = a.batch * a.heads * gm.nhg * a.sp.n_chunks;
+    const int KI = ws_items_per_cta(n_items, gridDim.x);
+    const int k0 = blockIdx.x * KI;                 // this CTA's first item
+    const int nk = max(0, min(KI, n_items - k0));  // and its item count
+    const WsLayout sl = ws_layout<D>(L.page_bytes, gm, NSET, S, KI, a.split_blocks);
+    uint8_t* ring = smem + sl.ring;
+    uint8_t* bimg = smem + sl.bimg;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
+    uint64_t* full = bars;               // [S]  tile landed (tx)
+    uint64_t* empty = bars + S;          // [S]  tile released (4 consumer warps + score group)
+    uint64_t* bfull = bars + 2 * S;      // [slot] operand image landed (tx)
+    uint64_t* bempty = bfull + 2;        // [slot] operand image released (MMA commit)
+    uint64_t* mdone = bempty + 2;        // MMAs of a tile done (commit): scores ready, A operand free
+    uint64_t* dfree = mdone + 1;         // scores read (4 consumer warps)
+    uint64_t* aready = dfree + 1;        // A operand of a tile stored (4 score warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + sl.tslot);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t* err = a.dp.err;
+    WsItem* items = reinterpret_cast<WsItem*>(smem + sl.items);
+    float* icst = reinterpret_cast<float*>(smem + sl.icst);      // [item][head][4]
+    int32_t* ids = reinterpret_cast<int32_t*>(smem + sl.ids);     // [item][split_blocks] block ids
+    uint32_t* smask = reinterpret_cast<uint32_t*>(smem + sl.smask);  // [stage] pages copied
+    auto B = [&](const uint64_t* p) { return smem_u32(p); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(B(&full[s]), 1);
+            mbar_init(B(&empty[s]), 5);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B(&bfull[i]), 1);
+            mbar_init(B(&bempty[i]), 1);
+        }
+        mbar_init(B(mdone), 1);
+        mbar_init(B(dfree), 4);
+        mbar_init(B(aready), 4);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(tslot, kWsTmemCols);
+
+    // prologue: this CTA's items, their per-head constants and block ids into
+    // shared memory (batches of independent loads), so that the tile loop
+    // below makes no global loads
+    const int hc = gm.hc, SB = a.split_blocks;
+    for (int k = tid; k < nk; k += blockDim.x) {
+        bool bad = false;
+        const WsItem it = ws_item(a, k0 + k, &bad);
+        items[k] = it;
+        if (bad && it.g == 0 && it.chunk == 0 && it.hgi == 0) set_error(err, TQ_DEVERR_SEQLEN);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int nimg = ws_nimg(gm);
+        int key[2] = {-1, -1}, nload[2] = {0, 0}, last[2] = {-1, -1};
+        for (int k = 0; k < nk; ++k) {
+            WsItem& it = items[k];
+            it.slot = it.load = it.lidx = it.release = 0;
+            if (it.n_tiles == 0) continue;
+            const int sl_ = it.hgi % nimg, kk = (it.b * a.heads + it.g) * gm.nhg + it.hgi;
+            it.slot = sl_;
+            if (key[sl_] != kk) {
+                if (last[sl_] >= 0) items[last[sl_]].release = 1;
+                it.load = 1;
+                it.lidx = nload[sl_]++;
+                key[sl_] = kk;
+            }
+            last[sl_] = k;
+        }
+    }
+    for (int base = tid; base < nk * H4 * 4; base += blockDim.x * 4) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * blockDim.x;
+            v[u] = 0.f;
+            if (e < nk * H4 * 4) {
+                const WsItem& it = items[e / (H4 * 4)];
+                const int h = (e >> 2) % H4;
+                if (h < hc) v[u] = a.ws_cst[((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc + h) * 4 + (e & 3)];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < nk * H4 * 4) icst[e] = v[u];
+        }
+    }
+    for (int base = tid; base < nk * SB; base += blockDim.x * 8) {
+        int32_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = base + u * blockDim.x;
+            v[u] = -1;
+            if (e < nk * SB) {
+                const WsItem& it = items[e / SB];
+                const int pg = e % SB;
+                if (pg < it.n_pages) v[u] = a.block_table[(int64_t)it.b * a.max_blocks + it.t0 / kBlock + pg];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < nk * SB) ids[e] = v[u];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool dead = false;
+
+    if (warp < 4) {
+        // ------------------------------------------------- score operands
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(ws_regs_score(D, NTH, G32)));
+        const int pj = tid >> 4, r = tid & 15;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const uint32_t idesc = fp8_idesc(NCOLS);
+        const uint32_t sbo = 8u * (uint32_t)(gm.npl * D);
+        const bool qjl = L.k_qjl;
+        // copy issue cursor (thread 32), see WsIssuer
+        constexpr int kIssuer = 32;
+        WsIssuer iss{items, ids, smask, ring, bimg, full, empty, bfull, bempty, a.cache, a.ws_bimg, err,
+                     sl.tile, nk, SB, S, L.page_bytes, gm.bimg_bytes, a.heads, gm.nhg, a.num_blocks};
+        if (tid == kIssuer) iss.next_item();
+        if (tid == kIssuer) iss.issue_upto(S - 1, 0, S);
+        int tseq = 0;
+        for (int k = 0; k < nk; ++k) {
+            const WsItem it = items[k];
+            if (it.n_tiles == 0) continue;
+            const uint8_t* img = bimg + (size_t)it.slot * gm.bimg_bytes;
+            for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
+                const int s = tseq % S;
+                ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
+                if (tseq >= 1) ws_wait(B(mdone), (tseq - 1) & 1, dead, err);  // A operand free
+                tc_fence_after();
+                const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
+                uint32_t kw[KB][NW], sw[NW];
+#pragma unroll
+                for (int p = 0; p < KB; ++p)
+#pragma unroll
+                    for (int w4 = 0; w4 < NW; w4 += 4) {
+                        const uint4 u =
+                            *reinterpret_cast<const uint4*>(pg + L.k_codes + (p * kBlock + r) * (D / 8) + 4 * w4);
+                        kw[p][w4] = u.x;
+                        kw[p][w4 + 1] = u.y;
+                        kw[p][w4 + 2] = u.z;
+                        kw[p][w4 + 3] = u.w;
+                    }
+#pragma unroll
+                for (int w4 = 0; w4 < NW; w4 += 4) {
+                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                    if (qjl) u = *reinterpret_cast<const uint4*>(pg + L.k_signs + r * (D / 8) + 4 * w4);
+                    sw[w4] = u.x;
+                    sw[w4 + 1] = u.y;
+                    sw[w4 + 2] = u.z;
+                    sw[w4 + 3] = u.w;
+                }
+                const uint32_t abase = tmem + lane_base + TA;
+#pragma unroll
+                for (int P = 0; P <= NPK; ++P) {
+                    if (P == NPK && !qjl) break;
+                    uint32_t wv[NW];
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) {
+                        uint32_t x = 0;
+                        if (P < NPK) {
+#pragma unroll
+                            for (int p = 0; p < KB; ++p)
+                                if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w];
+                        } else {
+                            x = sw[w];
+                        }
+                        wv[w] = x;
+                    }
+#pragma unroll
+                    for (int q = 0; q < NW / 4; ++q) {
+                        asm volatile("" : "+r"(wv[4 * q]), "+r"(wv[4 * q + 1]), "+r"(wv[4 * q + 2]), "+r"(wv[4 * q + 3]));
+                        uint32_t a32[32];
+#pragma unroll
+                        for (int w4 = 0; w4 < 4; ++w4) {
+                            const uint32_t x = wv[4 * q + w4];
+                            a32[8 * w4 + 0] = bit_operand<0>(x);
+                            a32[8 * w4 + 1] = bit_operand<1>(x);
+                            a32[8 * w4 + 2] = bit_operand<2>(x);
+                            a32[8 * w4 + 3] = bit_operand<3>(x);
+                            a32[8 * w4 + 4] = bit_operand<4>(x);
+                            a32[8 * w4 + 5] = bit_operand<5>(x);
+                            a32[8 * w4 + 6] = bit_operand<6>(x);
+                            a32[8 * w4 + 7] = bit_operand<7>(x);
+                        }
+                        tmem_st32(abase + P * NCOL + 32 * q, a32);
+                    }
+                }
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(aready));  // no block-wide barrier: a warp held up
+                                                         // issuing copies delays only itself
+                if (tid == 0) {
+                    ws_wait(B(aready), tseq & 1, dead, err);
+                    mbar_arrive(B(&empty[s]));  // the keys of this stage are read
+                    if (tseq >= 1) ws_wait(B(dfree), (tseq - 1) & 1, dead, err);  // accumulators read
+                    if (t == 0 && it.load) ws_wait(B(&bfull[it.slot]), it.lidx & 1, dead, err);
+                    tc_fence_after();
+                    const uint32_t dk = tmem;
+                    for (int P = 0; P < gm.npl; ++P)
+                        for (int kb = 0; kb < NW; ++kb) {
+                            const uint64_t bd = smem_desc(smem_u32(img) +
+                                                              (P * (D / 16) + 2 * kb) * 128,
+                                                          128, sbo);
+                            const uint32_t acc = P < NPK ? (P > 0 || kb > 0) : (kb > 0);
+                            mma_fp8_ts(P < NPK ? dk : dk + NCOLS, tmem + TA + P * NCOL + 8 * kb, bd, idesc,
+                                       acc);
+                        }
+                    tc_commit(B(mdone));
+                    if (t == it.n_tiles - 1 && it.release) tc_commit(B(&bempty[it.slot]));
+                }
+                if (tid == kIssuer) iss.issue_upto(tseq + S, tseq + 1, S);
+            }
+        }
+        // copies still in flight must land before the block exits
+        if (tid == kIssuer) {
+            bool d2 = false;
+            for (int k = max(0, iss.c_seq - S); k < iss.c_seq; ++k) ws_wait(B(&full[k % S]), (k / S) & 1, d2, err);
+            int nl[2] = {0, 0};
+            for (int k = 0; k < nk; ++k)
+                if (items[k].n_tiles > 0 && items[k].load && (k < iss.c_k || (k == iss.c_k && iss.c_img)))
+                    nl[items[k].slot] = items[k].lidx + 1;
+            for (int i = 0; i < 2; ++i)
+                if (nl[i] > 0) ws_wait(B(&bfull[i]), (nl[i] - 1) & 1, d2, err);
+        }
+    } else {
+        // ------------------------------------------------------ consumers
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(ws_regs_cons(D, NTH, G32)));
+        const int cw = warp - 4, ctid = tid - 128;
+        const int gq = lane >> 2, tq = lane & 3;
+        const int pj = ctid >> 4, r = ctid & 15;
+        const int pl = pj & 1, pair = r & 7, hf = r >> 3;
+        const uint32_t lane_base = (uint32_t)(32 * cw) << 16;
+        const bool qjl = L.k_qjl;
+        uint32_t* pbw = reinterpret_cast<uint32_t*>(smem + sl.pbuf) + cw * sl.pbuf_words;
+        float* zsm = reinterpret_cast<float*>(smem + sl.zsm) + cw * H4 * (D / 32);
+        float* red = reinterpret_cast<float*>(smem + sl.red);
+        for (int e = lane; e < sl.pbuf_words; e += 32) pbw[e] = 0u;
+        float v_dc = 0.f, v_beta[NPV];
+        if constexpr (!G32) {
+            v_dc = a.dp.v_walsh[0];
+#pragma unroll
+            for (int P = 0; P < NPV; ++P) {
+                v_beta[P] = -0.5f * a.dp.v_walsh[1 + P];
+                v_dc += 0.5f * a.dp.v_walsh[1 + P];
+            }
+        }
+        int tseq = 0;
+        for (int k = 0; k < nk; ++k) {
+            const WsItem it = items[k];
+            const float* cst = icst + k * H4 * 4;
+            float m_ref[H4], l_part[H4], zacc[H4][NZ];
+            float pv[NTH][NMT][4];
+#pragma unroll
+            for (int h = 0; h < H4; ++h) {
+                m_ref[h] = -INFINITY;
+                l_part[h] = 0.f;
+#pragma unroll
+                for (int z = 0; z < NZ; ++z) zacc[h][z] = 0.f;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) pv[nt][mt][0] = pv[nt][mt][1] = pv[nt][mt][2] = pv[nt][mt][3] = 0.f;
+            for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
+                const int s = tseq % S;
+                ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
+                ws_wait(B(mdone), tseq & 1, dead, err);
+                tc_fence_after();
+                const int p0 = t * kTilePages, np = min(kTilePages, it.n_pages - p0);
+                const uint8_t* tile = ring + s * sl.tile;
+                const int pos = it.t0 + (p0 + pj) * kBlock + r;
+                const bool valid = pj < np && pos < it.t1 && ((smask[s] >> pj) & 1);
+                const uint8_t* pg = tile + pj * L.page_bytes;
+
+                // ---------------- scores of this token (log2 units)
+                const float n16 = __half2float(*reinterpret_cast<const __half*>(pg + L.k_norm + 2 * r));
+                const float rho = qjl ? __half2float(*reinterpret_cast<const __half*>(pg + L.k_rnorm + 2 * r)) : 0.f;
+                float sc[H4];
+                {
+                    uint32_t acc[NCOLS];
+                    float sk[H4];
+                    const uint32_t dk = tmem + lane_base;
+#pragma unroll
+                    for (int q = 0; q < NCOLS / 16; ++q)
+                        tmem_ld16(dk + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&acc[16 * q]));
+                    tc_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < H4; ++h) sk[h] = piece_sum(&acc[kPieces * h]);
+                    if (qjl) {
+#pragma unroll
+                        for (int q = 0; q < NCOLS / 16; ++q)
+                            tmem_ld16(dk + NCOLS + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&acc[16 * q]));
+                        tc_wait_ld();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B(dfree));
+#pragma unroll
+                    for (int h = 0; h < H4; ++h) {
+                        float v = n16 * (cst[4 * h] + sk[h] * cst[4 * h + 2]);
+                        if (qjl) v += rho * (cst[4 * h + 1] + piece_sum(&acc[kPieces * h]) * cst[4 * h + 3]);
+                        sc[h] = (valid && h < hc) ? v : -INFINITY;
+                    }
+                }
+
+                // ---------------- online softmax per warp (lazy reference maximum)
+                float p[H4];
+#pragma unroll
+                for (int h = 0; h < H4; ++h) {
+                    const bool mv = sc[h] > m_ref[h] + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, mv)) {
+                        const float mx = warp_max(sc[h]);
+                        const float alpha = m_ref[h] == -INFINITY ? 0.f : fast_exp2(m_ref[h] - mx);
+                        l_part[h] *= alpha;
+#pragma unroll
+                        for (int z = 0; z < NZ; ++z) zacc[h][z] *= alpha;
+                        if (tq == (h & 3)) {
+#pragma unroll
+                            for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) pv[h >> 2][mt][e] *= alpha;
+                        }
+                        m_ref[h] = mx;
+                    }
+                    p[h] = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_ref[h]);
+                    l_part[h] += p[h];
+                }
+
+                // ---------------- probability operands (masked heads write zeros)
+                {
+                    __half* pb = reinterpret_cast<__half*>(pbw + pl * sl.pls) + hf;
+                    auto put = [&](int set, int h, float x) {
+                        const __half hi = __float2half_rn(x);
+                        const __half lo = __float2half_rn(x - __half2float(hi));
+                        const int wd = (set * H4 + h) * 24 + pair * 2;
+                        pb[2 * wd] = hi;
+                        pb[2 * wd + 2] = lo;
+                    };
+                    if constexpr (G32) {
+                        constexpr int MW = D / 32;
+                        uint32_t mw[MW];
+#pragma unroll
+                        for (int w4 = 0; w4 < MW; w4 += 4) {
+                            const uint4 u =
+                                *reinterpret_cast<const uint4*>(pg + L.v_meta + r * L.v_meta_row + 4 * w4);
+                            mw[w4] = u.x;
+                            mw[w4 + 1] = u.y;
+                            mw[w4 + 2] = u.z;
+                            mw[w4 + 3] = u.w;
+                        }
+#pragma unroll
+                        for (int gr = 0; gr < MW; ++gr) {
+                            const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&mw[gr]));
+                            const float sv = valid ? sz.x : 0.f, zv = valid ? sz.y : 0.f;
+#pragma unroll
+                            for (int h = 0; h < H4; ++h) {
+                                put(gr, h, p[h] * sv);
+                                zacc[h][gr] = fmaf(p[h], zv, zacc[h][gr]);
+                            }
+                        }
+                    } else {
+                        const float nv =
+                            valid ? __half2float(*reinterpret_cast<const __half*>(pg + L.v_meta + 2 * r)) : 0.f;
+#pragma unroll
+                        for (int h = 0; h < H4; ++h) {
+                            const float pn = p[h] * nv;
+#pragma unroll
+                            for (int P = 0; P < NPV; ++P) put(P, h, pn * v_beta[P]);
+                            zacc[h][0] = fmaf(v_dc, pn, zacc[h][0]);
+                        }
+                    }
+                }
+                __syncwarp();
+
+                // ---------------- values of this warp's two pages
+#pragma unroll
+                for (int pl2 = 0; pl2 < 2; ++pl2) {
+                    const int pjw = 2 * cw + pl2;
+                    if (pjw >= np) break;
+                    const uint8_t* pgw = tile + pjw * L.page_bytes;
+                    const uint32_t* pbr = pbw + pl2 * sl.pls + (gq >> 1) * 24 + (gq & 1) + 2 * tq;
+                    if constexpr (G32) {
+                        constexpr int TB = D * VB / 64;
+                        constexpr int TW = TB / 4;
+                        uint32_t va[TW], vb2[TW], vc[TW], vd[TW];
+                        const uint8_t* vrow = pgw + L.v_codes + TB * gq;
+#pragma unroll
+                        for (int w = 0; w < TW; ++w) {
+                            va[w] = *reinterpret_cast<const uint32_t*>(vrow + tq * L.v_code_row + 4 * w);
+                            vb2[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 8) * L.v_code_row + 4 * w);
+                            vc[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 4) * L.v_code_row + 4 * w);
+                            vd[w] = *reinterpret_cast<const uint32_t*>(vrow + (tq + 12) * L.v_code_row + 4 * w);
+                        }
+#pragma unroll
+                        for (int mt = 0; mt < NMT; ++mt) {
+                            const int gr = mt >> 1;
+                            const int byte = VB == 4 ? mt : (mt >> 1);
+                            const uint32_t sb = byte & 3;
+                            const uint32_t sel = sb | (sb << 4) | ((4 + sb) << 8) | ((4 + sb) << 12);
+                            const uint32_t r01 = prmt(va[byte >> 2], vb2[byte >> 2], sel);
+                            const uint32_t r89 = prmt(vc[byte >> 2], vd[byte >> 2], sel);
+                            uint32_t a0, a1, a2, a3;
+                            if constexpr (VB == 4) {
+                                a0 = r01 & 0x000F000Fu;
+                                a1 = r01 & 0x00F000F0u;
+                                a2 = r89 & 0x000F000Fu;
+                                a3 = r89 & 0x00F000F0u;
+                            } else {
+                                const int sh = 4 * (mt & 1);
+                                a0 = r01 & (0x00030003u << sh);
+                                a1 = r01 & (0x000C000Cu << sh);
+                                a2 = r89 & (0x00030003u << sh);
+                                a3 = r89 & (0x000C000Cu << sh);
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < NTH; ++nt) {
+                                const uint32_t* bp = pbr + (gr * H4 + 4 * nt) * 24;
+                                mma_f16(pv[nt][mt], a0, a1, a2, a3, bp[0], bp[8]);
+                            }
+                        }
+                    } else {
+                        constexpr int CB = D / 64;
+                        uint32_t wlo[VB][2], whi[VB][2];
+#pragma unroll
+                        for (int pp = 0; pp < VB; ++pp) {
+                            const uint8_t* base = pgw + L.v_codes + pp * kBlock * (D / 8) + CB * gq;
+                            if constexpr (CB == 2) {
+                                const uint32_t ra = *reinterpret_cast<const uint16_t*>(base + tq * (D / 8));
+                                const uint32_t rb = *reinterpret_cast<const uint16_t*>(base + (tq + 8) * (D / 8));
+                                const uint32_t rc = *reinterpret_cast<const uint16_t*>(base + (tq + 4) * (D / 8));
+                                const uint32_t rd = *reinterpret_cast<const uint16_t*>(base + (tq + 12) * (D / 8));
+                                wlo[pp][0] = ra | (rb << 16);
+                                whi[pp][0] = rc | (rd << 16);
+                                wlo[pp][1] = whi[pp][1] = 0;
+                            } else {
+                                const uint32_t ra = *reinterpret_cast<const uint32_t*>(base + tq * (D / 8));
+                                const uint32_t rb = *reinterpret_cast<const uint32_t*>(base + (tq + 8) * (D / 8));
+                                const uint32_t rc = *reinterpret_cast<const uint32_t*>(base + (tq + 4) * (D / 8));
+                                const uint32_t rd = *reinterpret_cast<const uint32_t*>(base + (tq + 12) * (D / 8));
+                                wlo[pp][0] = (ra & 0xFFFFu) | (rb << 16);
+                                wlo[pp][1] = (ra >> 16) | (rb & 0xFFFF0000u);
+                                whi[pp][0] = (rc & 0xFFFFu) | (rd << 16);
+                                whi[pp][1] = (rc >> 16) | (rd & 0xFFFF0000u);
+                            }
+                        }
+#pragma unroll
+                        for (int P = 0; P < NPV; ++P) {
+                            uint32_t ul[2] = {0, 0}, uh[2] = {0, 0};
+#pragma unroll
+                            for (int pp = 0; pp < VB; ++pp)
+                                if ((plane_subset(VB, P) >> pp) & 1) {
+                                    ul[0] ^= wlo[pp][0];
+                                    ul[1] ^= wlo[pp][1];
+                                    uh[0] ^= whi[pp][0];
+                                    uh[1] ^= whi[pp][1];
+                                }
+#pragma unroll
+                            for (int mt = 0; mt < NMT; ++mt) {
+                                const int wsel = mt >> 3, sh = 2 * (mt & 7);
+                                const uint32_t a0 = ((ul[wsel] << (15 - sh)) & 0x80008000u) | 0x3C003C00u;
+                                const uint32_t a1 = ((ul[wsel] << (14 - sh)) & 0x80008000u) | 0x3C003C00u;
+                                const uint32_t a2 = ((uh[wsel] << (15 - sh)) & 0x80008000u) | 0x3C003C00u;
+                                const uint32_t a3 = ((uh[wsel] << (14 - sh)) & 0x80008000u) | 0x3C003C00u;
+#pragma unroll
+                                for (int nt = 0; nt < NTH; ++nt) {
+                                    const uint32_t* bp = pbr + (P * H4 + 4 * nt) * 24;
+                                    mma_f16(pv[nt][mt], a0, a1, a2, a3, bp[0], bp[8]);
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(&empty[s]));
+            }
+
+            // ---------------- item end: per-warp partials -> merged split partial
+            named_sync(2, 128);  // every warp is done with its probability buffer
+#pragma unroll
+            for (int h = 0; h < H4; ++h) {
+                l_part[h] = warp_sum(l_part[h]);
+#pragma unroll
+                for (int z = 0; z < NZ; ++z) zacc[h][z] = warp_sum(zacc[h][z]);
+            }
+            if (lane == 0)
+#pragma unroll
+                for (int h = 0; h < H4; ++h) {
+#pragma unroll
+                    for (int z = 0; z < NZ; ++z) zsm[h * NZ + z] = zacc[h][z];
+                    red[(cw * H4 + h) * (D + 2) + D] = m_ref[h];
+                    red[(cw * H4 + h) * (D + 2) + D + 1] = l_part[h];
+                }
+            __syncwarp();
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) {
+                const int head = 4 * nt + tq;
+                float* my = red + (cw * H4 + head) * (D + 2);
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    float v0v = pv[nt][mt][0] + pv[nt][mt][1], v1v = pv[nt][mt][2] + pv[nt][mt][3];
+                    int c0;
+                    if constexpr (G32) {
+                        const float s0 = VB == 4 ? 16777216.f : ((mt & 1) ? 1048576.f : 16777216.f);
+                        const float s1 = VB == 4 ? 1048576.f : ((mt & 1) ? 262144.f : 4194304.f);
+                        const float zv = zsm[head * NZ + (mt >> 1)];
+                        c0 = 32 * (mt >> 1) + 4 * gq + 2 * (mt & 1);
+                        v0v = fmaf(v0v, s0, zv);
+                        v1v = fmaf(v1v, s1, zv);
+                    } else {
+                        const float zv = zsm[head * NZ];
+                        c0 = (D / 8) * gq + 2 * mt;
+                        v0v += zv;
+                        v1v += zv;
+                    }
+                    my[c0] = v0v;
+                    my[c0 + 1] = v1v;
+                }
+            }
+            named_sync(2, 128);
+            for (int e = ctid; e < hc * D; e += 128) {
+                const int h = e / D, i = e % D;
+                float M = -INFINITY;
+                for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * H4 + h) * (D + 2) + D]);
+                float acc = 0.f, l = 0.f;
+                for (int w = 0; w < 4; ++w) {
+                    const float* rr = red + (w * H4 + h) * (D + 2);
+                    if (rr[D] == -INFINITY) continue;
+                    const float wt = exp2f(rr[D] - M);
+                    acc = fmaf(wt, rr[i], acc);
+                    l = fmaf(wt, rr[D + 1], l);
+                }
+                const int64_t o =
+                    ((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc + h) * a.sp.n_splits + it.chunk;
+                a.ws_acc[o * D + i] = acc;
+                if (i == 0) {
+                    a.ws_ml[o * 2] = M;
+                    a.ws_ml[o * 2 + 1] = l;
+                }
+            }
+            named_sync(2, 128);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kWsTmemCols);
+}
+
+// Exact hybrid-tail tokens of every (KV head, sequence) as split n_chunks.
+template <int D>
+__global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int g = blockIdx.x, b = blockIdx.y;
+    if (b >= a.batch) return;
+    tail_split<D>(a, g, b, smem);
+}
+
+template <int D, int KB, bool G32, int VB, int NTH>
+inline tq_status launch_split_ws(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid) {
+    auto kern = split_ws_kernel<D, KB, G32, VB, NTH>;
+    static bool attr_set = false;  // once per kernel instance, before any capture
+    if (!attr_set) {
+        {
+            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+            if (fs != TQ_OK) return fs;
+        }
+        attr_set = true;
+    }
+    kern<<<grid, kWsThreads, smem, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaFuncAttributes fa{};
+        cudaFuncGetAttributes(&fa, kern);
+        return cuda_status_detail(e, "split_ws_kernel regs %d, max threads %d, static smem %zu, dynamic %zu, "
+                                     "block %d, grid %d", fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes,
+                                  smem, kWsThreads, grid);
+    }
+    return TQ_OK;
+}
+
+template <int D, int KB, int NTH>
+inline tq_status dispatch_ws_v(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid) {
+    if (a.lay.v_mode == TQ_V_G32)
+        return a.lay.v_bits == 4 ? launch_split_ws<D, KB, true, 4, NTH>(a, s, smem, grid)
+                                 : launch_split_ws<D, KB, true, 2, NTH>(a, s, smem, grid);
+    switch (a.lay.v_bits) {
+        case 2: return launch_split_ws<D, KB, false, 2, NTH>(a, s, smem, grid);
+        case 3: return launch_split_ws<D, KB, false, 3, NTH>(a, s, smem, grid);
+        default: return launch_split_ws<D, KB, false, 4, NTH>(a, s, smem, grid);
+    }
+}
+
+}  // namespace tq

@@ -6,6 +6,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cstdarg>
+#include <cstdio>
 #include <new>
 #include <vector>
 
@@ -301,7 +303,36 @@ static void lloyd_max_sphere(int d, int bits, std::vector<double>& c, std::vecto
 
 using namespace tq;
 
+namespace tq {
+static thread_local char g_cuda_msg[384] = "";
+tq_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return TQ_OK;
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return TQ_ERR_CUDA;
+}
+tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...) {
+    if (cuda_status(e) == TQ_OK) return TQ_OK;
+    const size_t n = strlen(g_cuda_msg);
+    if (n + 3 < sizeof g_cuda_msg) {
+        g_cuda_msg[n] = ' ';
+        g_cuda_msg[n + 1] = '(';
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(g_cuda_msg + n + 2, sizeof g_cuda_msg - n - 3, fmt, ap);
+        va_end(ap);
+        const size_t m = strlen(g_cuda_msg);
+        if (m + 1 < sizeof g_cuda_msg) {
+            g_cuda_msg[m] = ')';
+            g_cuda_msg[m + 1] = 0;
+        }
+    }
+    return TQ_ERR_CUDA;
+}
+}  // namespace tq
+
 extern "C" {
+
+const char* tq_last_cuda_error(void) { return tq::g_cuda_msg; }
 
 const char* tq_status_string(tq_status s) {
     switch (s) {

@@ -79,6 +79,12 @@ struct WorkspaceLayout {
     size_t q, bimg, cst, acc, ml, total;
 };
 
+// TQ_OK for cudaSuccess; otherwise records the runtime's message for
+// tq_last_cuda_error (per host thread) and returns TQ_ERR_CUDA
+tq_status cuda_status(cudaError_t e);
+// the same, with printf-style context appended to the message
+tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...);
+
 tq_status compute_layout(const tq_cache_config& c, Layout* lay);
 Splits compute_splits(const tq_cache_config& c);
 ParamsLayout params_layout(const tq_cache_config& c);

@@ -227,8 +227,10 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
     // one-time setup per kernel instance (before any stream capture)
     static int sms = 0;
     if (sms == 0) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return TQ_ERR_CUDA;
+        {
+            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            if (fs != TQ_OK) return fs;
+        }
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -238,7 +240,7 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
     kern<<<grid, 256, smem, s>>>(a);
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace tq
