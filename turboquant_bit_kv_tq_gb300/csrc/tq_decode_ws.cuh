@@ -3,13 +3,15 @@
 //
 // Two CTAs per SM (bulk-copy throughput is per CTA) each walk a list of work
 // items (one split of one KV head's head group of one sequence) as a stream of
-// 128-token tiles, with two warpgroups running concurrently and handing tiles
-// over through mbarriers:
+// 128-token tiles, with three warpgroups running concurrently and handing
+// tiles over through mbarriers:
+//   producer   (warp 8, one thread): bulk async copies of the tiles' pages into
+//              a ring of `stages` tiles and of each item's query operand image,
+//              each issued as soon as its buffer is released
 //   scores     (warps 0-3, thread t = token t of the tile): expand the key
-//              bit-planes into fp8 operands in tensor memory; thread 0 issues
-//              the tcgen05 MMAs into the accumulator columns, and the bulk
-//              async copies of the tiles' pages (a ring of `stages` tiles) and
-//              of each item's query operand image (two buffers) ahead of use
+//              bit-planes into fp8 operands in tensor memory, in two halves
+//   MMA        (warp 9, one thread): the tcgen05 MMAs of each half into the
+//              accumulator columns as soon as the half is stored
 //   consumers  (warps 4-7, same token mapping): read the scores, online exp2
 //              softmax, probability operands, value contraction of the warp's
 //              two pages on fp16 tensor cores, per-item merge of the partials
@@ -22,16 +24,16 @@
 
 namespace tq {
 
-constexpr int kWsWarps = 8;  // 4 score + 4 consumer
+constexpr int kWsWarps = 12;  // 4 score + 4 consumer + 4 producer (one thread)
 constexpr int kWsThreads = 32 * kWsWarps;
 constexpr int kWsMaxStages = 8;
 constexpr int kWsCtasPerSm = 2;   // bulk-copy throughput is per CTA: two CTAs per SM stream ~1.7x one
 constexpr int kWsTmemCols = 256;  // 512 / kWsCtasPerSm
-// setmaxnreg split of the 256 x 128 registers a CTA launches with (score
-// warpgroup + consumer warpgroup = 2 x 128): configurations with larger value
-// accumulators move more registers to the consumers
-__host__ __device__ constexpr int ws_regs_cons(int d, int nth, bool g32) { return (nth == 2 || (d == 256 && g32)) ? 184 : 152; }
-__host__ __device__ constexpr int ws_regs_score(int d, int nth, bool g32) { return 256 - ws_regs_cons(d, nth, g32); }
+// setmaxnreg split of the 3 x 80 registers per thread (three warpgroups) a
+// CTA launches with: the producer keeps 40, the score warpgroup 64, the
+// consumers take the rest
+constexpr int kWsRegsLaunch = 80, kWsRegsProducer = 40, kWsRegsScore = 64;
+constexpr int kWsRegsCons = 3 * kWsRegsLaunch - kWsRegsProducer - kWsRegsScore;
 
 // tensor-memory plan: one accumulator buffer of 2*score_cols (key | sign),
 // then one A operand buffer
@@ -87,7 +89,7 @@ __host__ __device__ inline WsLayout ws_layout(int page_bytes, const DecodeGeom& 
     l.smask = off;
     off = up(off + (size_t)stages * 4);
     l.bars = off;
-    off = up(off + (size_t)(2 * stages + 8) * 8);
+    off = up(off + (size_t)(2 * stages + 10) * 8);
     l.tslot = off;
     off = up(off + 4);
     l.total = off;
@@ -141,12 +143,13 @@ __device__ __forceinline__ void ws_wait(uint32_t bar, uint32_t parity, bool& dea
     if (!dead) dead = !mbar_wait(bar, parity, err);
 }
 
-// Copy issue cursor of a split CTA (one thread): walks the tiles of the CTA's
-// non-empty items in order, loading an item's query operand image before its
-// first tile when it needs one.  issue_upto runs up to limit_seq, blocking only
-// for tiles up to need_seq (whose stage releases depend on MMAs already
-// issued) and otherwise stopping at the first stage or image not yet free.
-// Out of line so that the kernel holds one copy of it.
+// Copy issue cursor of a split CTA, run by one whole warp: walks the tiles of
+// the CTA's non-empty items in order, loading an item's query operand image
+// before its first tile when it needs one; lane j issues the copy of a tile's
+// page j, so a tile costs a handful of warp instructions.  issue_upto runs up
+// to limit_seq, blocking only for tiles up to need_seq (whose stage releases
+// depend on MMAs already issued) and otherwise stopping at the first stage or
+// image not yet free.
 struct WsIssuer {
     const WsItem* items;
     const int32_t* ids;
@@ -167,60 +170,63 @@ struct WsIssuer {
         while (c_k < nk && items[c_k].n_tiles == 0) ++c_k;
     }
 
+    // warp-uniform wait: lane 0 waits (bounded), the others take its verdict
+    __device__ bool wait_uniform(uint64_t* bar, uint32_t par, bool block, int lane) {
+        int ok = 1;
+        if (lane == 0) {
+            if (block) {
+                if (!mbar_wait(smem_u32(bar), par, err)) {
+                    dead = true;
+                    ok = 0;
+                }
+            } else {
+                ok = mbar_test(smem_u32(bar), par);
+            }
+        }
+        dead = __shfl_sync(0xffffffffu, (int)dead, 0) != 0;
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+
     __device__ __noinline__ void issue_upto(int limit_seq, int need_seq, int max_tiles) {
+        const int lane = threadIdx.x & 31;
 #pragma unroll 1
         for (int n = 0; c_k < nk && c_seq <= limit_seq && !dead && (n < max_tiles || c_seq <= need_seq); ++n) {
             const WsItem& it = items[c_k];
             if (!c_img) {
                 if (it.load) {
                     if (it.lidx >= 1) {
-                        const uint32_t par = (it.lidx - 1) & 1;
-                        const uint32_t bar = smem_u32(&bempty[it.slot]);
-                        if (c_seq <= need_seq)
-                            dead = !mbar_wait(bar, par, err);
-                        else if (!mbar_test(bar, par))
+                        if (!wait_uniform(&bempty[it.slot], (it.lidx - 1) & 1, c_seq <= need_seq, lane) || dead)
                             break;
-                        if (dead) break;
                     }
-                    mbar_expect_tx(smem_u32(&bfull[it.slot]), bimg_bytes);
-                    bulk_copy(smem_u32(bimg + (size_t)it.slot * bimg_bytes),
-                              ws_bimg + (((int64_t)it.b * heads + it.g) * nhg + it.hgi) * bimg_bytes, bimg_bytes,
-                              smem_u32(&bfull[it.slot]));
+                    if (lane == 0) {
+                        mbar_expect_tx(smem_u32(&bfull[it.slot]), bimg_bytes);
+                        bulk_copy(smem_u32(bimg + (size_t)it.slot * bimg_bytes),
+                                  ws_bimg + (((int64_t)it.b * heads + it.g) * nhg + it.hgi) * bimg_bytes, bimg_bytes,
+                                  smem_u32(&bfull[it.slot]));
+                    }
                 }
                 c_img = true;
             }
             const int s = c_seq % S;
             if (c_seq >= S) {
-                const uint32_t par = ((c_seq / S) - 1) & 1;
-                if (c_seq <= need_seq)
-                    dead = !mbar_wait(smem_u32(&empty[s]), par, err);
-                else if (!mbar_test(smem_u32(&empty[s]), par))
-                    break;
-                if (dead) break;
+                if (!wait_uniform(&empty[s], ((c_seq / S) - 1) & 1, c_seq <= need_seq, lane) || dead) break;
             }
             // the consumers' reads of this stage happen-before the copies
             // through the empty barrier (release/acquire)
-            const int32_t* cid = ids + c_k * SB;
             const int p0 = c_t * kTilePages, np = min(kTilePages, it.n_pages - p0);
-            uint32_t bytes = 0, mask = 0;
-#pragma unroll 1
-            for (int j = 0; j < np; ++j) {
-                const int blk = cid[p0 + j];
-                if (blk >= 0 && blk < num_blocks) {
-                    bytes += page_bytes;
-                    mask |= 1u << j;
-                } else {
-                    set_error(err, TQ_DEVERR_BLOCK);
-                }
+            int blk = -1;
+            if (lane < np) blk = ids[c_k * SB + p0 + lane];
+            const bool ok = lane < np && blk >= 0 && blk < num_blocks;
+            const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+            if (lane < np && !ok) set_error(err, TQ_DEVERR_BLOCK);
+            if (lane == 0) {
+                smask[s] = mask;  // published by the arrive below
+                mbar_expect_tx(smem_u32(&full[s]), (uint32_t)__popc(mask) * page_bytes);
             }
-            smask[s] = mask;  // published by the arrive below
-            mbar_expect_tx(smem_u32(&full[s]), bytes);
-#pragma unroll 1
-            for (int j = 0; j < np; ++j)
-                if ((mask >> j) & 1)
-                    bulk_copy(smem_u32(ring + s * tile + (size_t)j * page_bytes),
-                              cache + ((int64_t)cid[p0 + j] * heads + it.g) * page_bytes, page_bytes,
-                              smem_u32(&full[s]));
+            __syncwarp();
+            if (ok)
+                bulk_copy(smem_u32(ring + s * tile + (size_t)lane * page_bytes),
+                          cache + ((int64_t)blk * heads + it.g) * page_bytes, page_bytes, smem_u32(&full[s]));
             ++c_seq;
             if (++c_t == it.n_tiles) {
                 c_t = 0;
@@ -232,8 +238,29 @@ struct WsIssuer {
     }
 };
 
+// The MMAs of score planes [P0, P1) of a tile, with addresses stepped
+// incrementally: the issuing thread shares its SM sub-partition with busy
+// warps, so each MMA gets a few instructions at most.  bd0 is the descriptor
+// of the operand image at plane 0, k-block 0.
+template <int D, int NPK, int NCOLS, int TA>
+__device__ __forceinline__ void ws_issue_planes(int P0, int P1, uint32_t tmem, uint64_t bd0, uint32_t idesc) {
+    constexpr int NW = D / 32, NCOL = D / 4;
+    uint32_t a_addr = tmem + TA + P0 * NCOL;
+    uint64_t bd = bd0 + (uint64_t)(P0 * (D / 16) * 8);
+#pragma unroll 1
+    for (int P = P0; P < P1; ++P) {
+        const uint32_t d = P < NPK ? tmem : tmem + NCOLS;
+        const uint32_t first = (P == 0 || P == NPK) ? 0u : 1u;  // a fresh accumulator starts at plane 0 / NPK
+#pragma unroll
+        for (int kb = 0; kb < NW; ++kb) mma_fp8_ts(d, a_addr + 8 * kb, bd + (uint64_t)(16 * kb), idesc, kb ? 1u : first);
+        a_addr += NCOL;
+        bd += (uint64_t)((D / 16) * 8);
+    }
+}
+
 template <int D, int KB, bool G32, int VB, int NTH>
 __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(DecodeArgs a) {
+    static_assert(kWsRegsCons <= 256 && kWsRegsCons % 8 == 0, "register split");
     constexpr int NPK = 1 << (KB - 1);
     constexpr int NW = D / 32;
     constexpr int NCOL = D / 4;
@@ -261,9 +288,11 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     uint64_t* empty = bars + S;          // [S]  tile released (4 consumer warps + score group)
     uint64_t* bfull = bars + 2 * S;      // [slot] operand image landed (tx)
     uint64_t* bempty = bfull + 2;        // [slot] operand image released (MMA commit)
-    uint64_t* mdone = bempty + 2;        // MMAs of a tile done (commit): scores ready, A operand free
-    uint64_t* dfree = mdone + 1;         // scores read (4 consumer warps)
-    uint64_t* aready = dfree + 1;        // A operand of a tile stored (4 score warps)
+    // the score planes of a tile go in two halves (planes [0, PX) and [PX, npl))
+    // so that the MMAs of one half overlap the expansion of the other
+    uint64_t* mdone = bempty + 2;        // [half] MMAs of a half done (commit); half 1: scores ready
+    uint64_t* dfree = mdone + 2;         // scores read (4 consumer warps)
+    uint64_t* aready = dfree + 1;        // [half] A operand half stored (4 score warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + sl.tslot);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint32_t* err = a.dp.err;
@@ -282,9 +311,11 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             mbar_init(B(&bfull[i]), 1);
             mbar_init(B(&bempty[i]), 1);
         }
-        mbar_init(B(mdone), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B(&mdone[i]), 1);
+            mbar_init(B(&aready[i]), 4);
+        }
         mbar_init(B(dfree), 4);
-        mbar_init(B(aready), 4);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(tslot, kWsTmemCols);
@@ -360,30 +391,65 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     const uint32_t tmem = *tslot;
     bool dead = false;
 
-    if (warp < 4) {
+    const int PX = (gm.npl + 1) / 2;  // planes in the first half
+    if (warp >= 8) {
+        // ------------------------------------------------------ producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWsRegsProducer));
+        if (tid == 288) {
+            // MMA issue (one thread; tcgen05.mma blocks while the tensor pipe is busy)
+            const uint32_t idesc = fp8_idesc(NCOLS);
+            const uint32_t sbo = 8u * (uint32_t)(gm.npl * D);
+            int tseq = 0;
+            for (int k = 0; k < nk; ++k) {
+                const WsItem it = items[k];
+                if (it.n_tiles == 0) continue;
+                const uint32_t img = smem_u32(bimg + (size_t)it.slot * gm.bimg_bytes);
+                for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
+                    const int s = tseq % S;
+                    if (t == 0 && it.load) ws_wait(B(&bfull[it.slot]), it.lidx & 1, dead, err);
+                    if (tseq >= 1) ws_wait(B(dfree), (tseq - 1) & 1, dead, err);  // accumulators read
+                    const uint64_t bd0 = smem_desc(img, 128, sbo);
+                    ws_wait(B(&aready[0]), tseq & 1, dead, err);
+                    tc_fence_after();
+                    ws_issue_planes<D, NPK, NCOLS, TA>(0, PX, tmem, bd0, idesc);
+                    tc_commit(B(&mdone[0]));
+                    ws_wait(B(&aready[1]), tseq & 1, dead, err);
+                    tc_fence_after();
+                    mbar_arrive(B(&empty[s]));  // the keys of this stage are read
+                    ws_issue_planes<D, NPK, NCOLS, TA>(PX, gm.npl, tmem, bd0, idesc);
+                    tc_commit(B(&mdone[1]));
+                    if (t == it.n_tiles - 1 && it.release) tc_commit(B(&bempty[it.slot]));
+                }
+            }
+        }
+        if (warp == 8) {
+            WsIssuer iss{items, ids, smask, ring, bimg, full, empty, bfull, bempty, a.cache, a.ws_bimg, err,
+                         sl.tile, nk, SB, S, L.page_bytes, gm.bimg_bytes, a.heads, gm.nhg, a.num_blocks};
+            iss.next_item();
+            iss.issue_upto(0x7fffffff, 0x7fffffff, 0x7fffffff);  // every wait blocks: nothing else to do
+            // copies still in flight must land before the block exits
+            bool d2 = lane != 0;  // lane 0 drains
+            for (int k = max(0, iss.c_seq - S); k < iss.c_seq; ++k) ws_wait(B(&full[k % S]), (k / S) & 1, d2, err);
+            int nl[2] = {0, 0};
+            for (int k = 0; k < nk; ++k)
+                if (items[k].n_tiles > 0 && items[k].load && (k < iss.c_k || (k == iss.c_k && iss.c_img)))
+                    nl[items[k].slot] = items[k].lidx + 1;
+            for (int i = 0; i < 2; ++i)
+                if (nl[i] > 0) ws_wait(B(&bfull[i]), (nl[i] - 1) & 1, d2, err);
+        }
+    } else if (warp < 4) {
         // ------------------------------------------------- score operands
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(ws_regs_score(D, NTH, G32)));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWsRegsScore));
         const int pj = tid >> 4, r = tid & 15;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const uint32_t idesc = fp8_idesc(NCOLS);
-        const uint32_t sbo = 8u * (uint32_t)(gm.npl * D);
         const bool qjl = L.k_qjl;
-        // copy issue cursor (thread 32), see WsIssuer
-        constexpr int kIssuer = 32;
-        WsIssuer iss{items, ids, smask, ring, bimg, full, empty, bfull, bempty, a.cache, a.ws_bimg, err,
-                     sl.tile, nk, SB, S, L.page_bytes, gm.bimg_bytes, a.heads, gm.nhg, a.num_blocks};
-        if (tid == kIssuer) iss.next_item();
-        if (tid == kIssuer) iss.issue_upto(S - 1, 0, S);
         int tseq = 0;
         for (int k = 0; k < nk; ++k) {
             const WsItem it = items[k];
             if (it.n_tiles == 0) continue;
-            const uint8_t* img = bimg + (size_t)it.slot * gm.bimg_bytes;
             for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
                 const int s = tseq % S;
                 ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
-                if (tseq >= 1) ws_wait(B(mdone), (tseq - 1) & 1, dead, err);  // A operand free
-                tc_fence_after();
                 const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
                 uint32_t kw[KB][NW], sw[NW];
 #pragma unroll
@@ -410,6 +476,18 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
 #pragma unroll
                 for (int P = 0; P <= NPK; ++P) {
                     if (P == NPK && !qjl) break;
+                    if (P == 0 || P == PX) {
+                        // half h of the A operand: wait until the previous tile's MMAs
+                        // of that half are done (after storing and publishing half 0)
+                        if (P == PX) {
+                            tc_wait_st();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(B(&aready[0]));
+                        }
+                        if (tseq >= 1) ws_wait(B(&mdone[P == 0 ? 0 : 1]), (tseq - 1) & 1, dead, err);
+                        tc_fence_after();
+                    }
                     uint32_t wv[NW];
 #pragma unroll
                     for (int w = 0; w < NW; ++w) {
@@ -445,44 +523,12 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(B(aready));  // no block-wide barrier: a warp held up
-                                                         // issuing copies delays only itself
-                if (tid == 0) {
-                    ws_wait(B(aready), tseq & 1, dead, err);
-                    mbar_arrive(B(&empty[s]));  // the keys of this stage are read
-                    if (tseq >= 1) ws_wait(B(dfree), (tseq - 1) & 1, dead, err);  // accumulators read
-                    if (t == 0 && it.load) ws_wait(B(&bfull[it.slot]), it.lidx & 1, dead, err);
-                    tc_fence_after();
-                    const uint32_t dk = tmem;
-                    for (int P = 0; P < gm.npl; ++P)
-                        for (int kb = 0; kb < NW; ++kb) {
-                            const uint64_t bd = smem_desc(smem_u32(img) +
-                                                              (P * (D / 16) + 2 * kb) * 128,
-                                                          128, sbo);
-                            const uint32_t acc = P < NPK ? (P > 0 || kb > 0) : (kb > 0);
-                            mma_fp8_ts(P < NPK ? dk : dk + NCOLS, tmem + TA + P * NCOL + 8 * kb, bd, idesc,
-                                       acc);
-                        }
-                    tc_commit(B(mdone));
-                    if (t == it.n_tiles - 1 && it.release) tc_commit(B(&bempty[it.slot]));
-                }
-                if (tid == kIssuer) iss.issue_upto(tseq + S, tseq + 1, S);
+                if (lane == 0) mbar_arrive(B(&aready[1]));
             }
-        }
-        // copies still in flight must land before the block exits
-        if (tid == kIssuer) {
-            bool d2 = false;
-            for (int k = max(0, iss.c_seq - S); k < iss.c_seq; ++k) ws_wait(B(&full[k % S]), (k / S) & 1, d2, err);
-            int nl[2] = {0, 0};
-            for (int k = 0; k < nk; ++k)
-                if (items[k].n_tiles > 0 && items[k].load && (k < iss.c_k || (k == iss.c_k && iss.c_img)))
-                    nl[items[k].slot] = items[k].lidx + 1;
-            for (int i = 0; i < 2; ++i)
-                if (nl[i] > 0) ws_wait(B(&bfull[i]), (nl[i] - 1) & 1, d2, err);
         }
     } else {
         // ------------------------------------------------------ consumers
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(ws_regs_cons(D, NTH, G32)));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kWsRegsCons));
         const int cw = warp - 4, ctid = tid - 128;
         const int gq = lane >> 2, tq = lane & 3;
         const int pj = ctid >> 4, r = ctid & 15;
@@ -522,7 +568,7 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
                 const int s = tseq % S;
                 ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
-                ws_wait(B(mdone), tseq & 1, dead, err);
+                ws_wait(B(&mdone[1]), tseq & 1, dead, err);
                 tc_fence_after();
                 const int p0 = t * kTilePages, np = min(kTilePages, it.n_pages - p0);
                 const uint8_t* tile = ring + s * sl.tile;
