@@ -125,18 +125,6 @@ __device__ __forceinline__ uint8_t float_to_e4m3(float x) {
     return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
-// piece k of x * scale: successive e4m3 roundings of the residual, each piece
-// scaled by 16 over the previous one
-__device__ __forceinline__ uint8_t e4m3_piece(float x, float scale, int k) {
-    float y = x * scale;
-    uint8_t p = 0;
-    for (int i = 0; i <= k; ++i) {
-        p = float_to_e4m3(y);
-        y = (y - e4m3_to_float(p)) * 16.f;
-    }
-    return p;
-}
-
 // 2^x for x <= 0 (softmax weights; approximate to ~2 ulp)
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -359,18 +347,24 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
         }
     }
     __syncthreads();
-    // score operand images, one 32-bit word (4 K indices) per step
+    // score operand images: a work unit is (head group, head row block, plane,
+    // tensor-memory column); it writes the kPieces words (4 K indices each) of
+    // the rows 5*hl + piece, computing the pieces of each value in one pass
     const int kt = gm.npl * D;           // K extent (bytes per row)
-    const int row_words = kt / 4;
-    const int img_words = gm.n_cols * row_words;
     const uint32_t sbo = 8u * kt;        // byte step between 8-row groups
+    const int hrows = (gm.n_cols + kPieces - 1) / kPieces;  // head row blocks (incl. padding)
+    const int units = gm.nhg * hrows * gm.npl * (D / 4);
     uint8_t* img0 = a.ws_bimg + ((int64_t)b * a.heads + g) * gm.nhg * gm.bimg_bytes;
-    for (int wi = tid; wi < gm.nhg * img_words; wi += blockDim.x) {
-        const int hgi = wi / img_words, rem = wi % img_words;
-        const int n = rem / row_words, kk0 = (rem % row_words) * 4;
-        const int P = kk0 / D, col = (kk0 % D) / 4;
-        const int hl = n / kPieces, piece = n % kPieces;
-        uint32_t word = 0;
+    for (int u = tid; u < units; u += blockDim.x) {
+        int x = u;
+        const int col = x % (D / 4);
+        x /= D / 4;
+        const int P = x % gm.npl;
+        x /= gm.npl;
+        const int hl = x % hrows, hgi = x / hrows;
+        uint32_t word[kPieces];
+#pragma unroll
+        for (int k = 0; k < kPieces; ++k) word[k] = 0;
         if (hl < gm.hc) {
             const int h = hgi * gm.hc + hl;
             const bool sign_plane = P == gm.npk;
@@ -381,11 +375,24 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int c = 32 * (col >> 3) + 8 * e + (col & 7);
-                word |= (uint32_t)e4m3_piece(beta * src[c] * bw, sc, piece) << (8 * e);
+                float y = beta * src[c] * bw * sc;
+#pragma unroll
+                for (int k = 0; k < kPieces; ++k) {
+                    const uint8_t pk = float_to_e4m3(y);
+                    word[k] |= (uint32_t)pk << (8 * e);
+                    y = (y - e4m3_to_float(pk)) * 16.f;
+                }
             }
         }
-        const uint32_t off = (n & 7) * 16 + (n >> 3) * sbo + (kk0 >> 4) * 128 + (kk0 & 15);
-        *reinterpret_cast<uint32_t*>(img0 + (size_t)hgi * gm.bimg_bytes + off) = word;
+        const int kk0 = P * D + 4 * col;
+        uint8_t* img = img0 + (size_t)hgi * gm.bimg_bytes;
+#pragma unroll
+        for (int k = 0; k < kPieces; ++k) {
+            const int n = kPieces * hl + k;
+            if (n < gm.n_cols)
+                *reinterpret_cast<uint32_t*>(img + (n & 7) * 16 + (n >> 3) * sbo + (kk0 >> 4) * 128 + (kk0 & 15)) =
+                    word[k];
+        }
     }
 }
 

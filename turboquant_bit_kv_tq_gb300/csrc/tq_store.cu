@@ -14,6 +14,8 @@
 
 namespace tq {
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 struct StoreArgs {
     const void* k;
     const void* v;
@@ -109,9 +111,17 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
     float* s_vb = s_vc + kMaxLevels;
 
     const Layout& L = a.lay;
-    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
-        const int j = e / D, i = e % D;
-        st[i * D + j] = a.dp.s_bf16[e];
+    // S^T (bf16, already transposed in the params) by one bulk copy
+    __shared__ __align__(8) uint64_t st_bar;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&st_bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&st_bar)), "r"(D * D * 2)
+                     : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_u32(st)),
+                     "l"(a.dp.st_bf16), "r"(D * D * 2), "r"(smem_u32(&st_bar))
+                     : "memory");
     }
     for (int e = threadIdx.x; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     for (int e = threadIdx.x; e < kMaxLevels; e += blockDim.x) {
@@ -121,6 +131,19 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         s_vb[e] = a.dp.v_bound[e];
     }
     __syncthreads();
+    {
+        bool landed = false;
+        for (int it = 0; it < (1 << 24) && !landed; ++it) {
+            uint32_t done;
+            asm volatile(
+                "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(done)
+                : "r"(smem_u32(&st_bar))
+                : "memory");
+            landed = done != 0;
+        }
+        if (!landed && threadIdx.x == 0) set_error(a.dp.err, TQ_DEVERR_TIMEOUT);
+    }
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float* r = rbuf + warp * D;
@@ -166,21 +189,42 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
             }
             const float rho = sqrtf(warp_sum(rr));
             __syncwarp();
-            // z_j = sum_i S[j][i] r_i for j = lane + 32k; bit j = [z_j >= 0]
+            // z_j = sum_i S[j][i] r_i for j = PER*lane + e (one 8- or 16-byte
+            // load of S^T per i); bit j = [z_j >= 0]
             float z[PER];
 #pragma unroll
-            for (int k = 0; k < PER; ++k) z[k] = 0.f;
+            for (int e = 0; e < PER; ++e) z[e] = 0.f;
+#pragma unroll 4
             for (int i = 0; i < D; ++i) {
                 const float ri = r[i];
+                uint32_t w[PER / 2];
+                if constexpr (PER == 4) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(st + i * D + PER * lane);
+                    w[0] = u.x;
+                    w[1] = u.y;
+                } else {
+                    const uint4 u = *reinterpret_cast<const uint4*>(st + i * D + PER * lane);
+                    w[0] = u.x;
+                    w[1] = u.y;
+                    w[2] = u.z;
+                    w[3] = u.w;
+                }
 #pragma unroll
-                for (int k = 0; k < PER; ++k) z[k] = fmaf(bf16_bits_to_float(st[i * D + lane + 32 * k]), ri, z[k]);
+                for (int e2 = 0; e2 < PER / 2; ++e2) {
+                    z[2 * e2] = fmaf(__uint_as_float(w[e2] << 16), ri, z[2 * e2]);
+                    z[2 * e2 + 1] = fmaf(__uint_as_float(w[e2] & 0xFFFF0000u), ri, z[2 * e2 + 1]);
+                }
             }
+            // lane l holds bits PER*l .. PER*l+PER-1; gather 32-bit words
+            uint32_t bits = 0;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) bits |= (z[e] >= 0.f ? 1u : 0u) << e;
+            constexpr int LPW = 32 / PER;  // lanes per output word
+            bits <<= PER * (lane % LPW);
+#pragma unroll
+            for (int o = 1; o < LPW; o <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
             uint32_t* srow = reinterpret_cast<uint32_t*>(page + L.k_signs + row * (D / 8));
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const uint32_t word = __ballot_sync(0xffffffffu, z[k] >= 0.f);
-                if (lane == k) srow[k] = word;
-            }
+            if (lane % LPW == 0) srow[lane / LPW] = bits;
             if (lane == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho);
         }
         __syncwarp();
