@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     __syncthreads();
     // score operand images: a work unit is (head group, head row block, plane,
     // tensor-memory column); it writes the kPieces words (4 K indices each) of
-    // the rows 5*hl + piece, computing the pieces of each value in one pass
+    // the rows kPieces*hl + piece, computing the pieces of each value in one pass
     const int kt = gm.npl * D;           // K extent (bytes per row)
     const uint32_t sbo = 8u * kt;        // byte step between 8-row groups
     const int hrows = (gm.n_cols + kPieces - 1) / kPieces;  // head row blocks (incl. padding)

@@ -548,7 +548,8 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 v_dc += 0.5f * a.dp.v_walsh[1 + P];
             }
         }
-        int tseq = 0;
+        int tseq = 0, st = 0;
+        uint32_t sph = 0;  // stage of tile tseq and the parity of its fill
         for (int k = 0; k < nk; ++k) {
             const WsItem it = items[k];
             const float* cst = icst + k * H4 * 4;
@@ -566,8 +567,8 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
 #pragma unroll
                 for (int mt = 0; mt < NMT; ++mt) pv[nt][mt][0] = pv[nt][mt][1] = pv[nt][mt][2] = pv[nt][mt][3] = 0.f;
             for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
-                const int s = tseq % S;
-                ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
+                const int s = st;
+                ws_wait(B(&full[s]), sph, dead, err);
                 ws_wait(B(&mdone[1]), tseq & 1, dead, err);
                 tc_fence_after();
                 const int p0 = t * kTilePages, np = min(kTilePages, it.n_pages - p0);
@@ -608,24 +609,37 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 }
 
                 // ---------------- online softmax per warp (lazy reference maximum)
+                if (t == 0) {
+                    // the item's first tile: nothing accumulated yet to rescale
+#pragma unroll
+                    for (int h = 0; h < H4; ++h) m_ref[h] = warp_max(sc[h]);
+                } else {
+                    // a reference moves only when a score passes it by kRescaleSlack
+                    bool mv = false;
+#pragma unroll
+                    for (int h = 0; h < H4; ++h) mv |= sc[h] > m_ref[h] + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, mv)) {
+#pragma unroll
+                        for (int h = 0; h < H4; ++h) {
+                            if (!__any_sync(0xffffffffu, sc[h] > m_ref[h] + kRescaleSlack)) continue;
+                            const float mx = warp_max(sc[h]);
+                            const float alpha = m_ref[h] == -INFINITY ? 0.f : fast_exp2(m_ref[h] - mx);
+                            m_ref[h] = mx;
+                            l_part[h] *= alpha;
+#pragma unroll
+                            for (int z = 0; z < NZ; ++z) zacc[h][z] *= alpha;
+                            if (tq == (h & 3)) {
+#pragma unroll
+                                for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) pv[h >> 2][mt][e] *= alpha;
+                            }
+                        }
+                    }
+                }
                 float p[H4];
 #pragma unroll
                 for (int h = 0; h < H4; ++h) {
-                    const bool mv = sc[h] > m_ref[h] + kRescaleSlack;
-                    if (__any_sync(0xffffffffu, mv)) {
-                        const float mx = warp_max(sc[h]);
-                        const float alpha = m_ref[h] == -INFINITY ? 0.f : fast_exp2(m_ref[h] - mx);
-                        l_part[h] *= alpha;
-#pragma unroll
-                        for (int z = 0; z < NZ; ++z) zacc[h][z] *= alpha;
-                        if (tq == (h & 3)) {
-#pragma unroll
-                            for (int mt = 0; mt < NMT; ++mt)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) pv[h >> 2][mt][e] *= alpha;
-                        }
-                        m_ref[h] = mx;
-                    }
                     p[h] = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_ref[h]);
                     l_part[h] += p[h];
                 }
@@ -776,6 +790,10 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B(&empty[s]));
+                if (++st == S) {
+                    st = 0;
+                    sph ^= 1u;
+                }
             }
 
             // ---------------- item end: per-warp partials -> merged split partial
@@ -821,25 +839,34 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 }
             }
             named_sync(2, 128);
+            // merge weights once per (warp, head): 2^(m_w - M) against the
+            // largest reference M; they go where the zero-point sums were
+            const int64_t o0 = ((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc) * a.sp.n_splits + it.chunk;
+            float* wts = reinterpret_cast<float*>(smem + sl.zsm);  // [warp][head]
+            if (ctid < hc) {
+                const int h = ctid;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * H4 + h) * (D + 2) + D]);
+                float l = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float mw = red[(w * H4 + h) * (D + 2) + D];
+                    const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                    wts[w * H4 + h] = wt;
+                    l = fmaf(wt, red[(w * H4 + h) * (D + 2) + D + 1], l);
+                }
+                const int64_t o = o0 + (int64_t)h * a.sp.n_splits;
+                a.ws_ml[o * 2] = M;
+                a.ws_ml[o * 2 + 1] = l;
+            }
+            named_sync(2, 128);
             for (int e = ctid; e < hc * D; e += 128) {
                 const int h = e / D, i = e % D;
-                float M = -INFINITY;
-                for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * H4 + h) * (D + 2) + D]);
-                float acc = 0.f, l = 0.f;
-                for (int w = 0; w < 4; ++w) {
-                    const float* rr = red + (w * H4 + h) * (D + 2);
-                    if (rr[D] == -INFINITY) continue;
-                    const float wt = exp2f(rr[D] - M);
-                    acc = fmaf(wt, rr[i], acc);
-                    l = fmaf(wt, rr[D + 1], l);
-                }
-                const int64_t o =
-                    ((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc + h) * a.sp.n_splits + it.chunk;
-                a.ws_acc[o * D + i] = acc;
-                if (i == 0) {
-                    a.ws_ml[o * 2] = M;
-                    a.ws_ml[o * 2 + 1] = l;
-                }
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) acc = fmaf(wts[w * H4 + h], red[(w * H4 + h) * (D + 2) + i], acc);
+                a.ws_acc[(o0 + (int64_t)h * a.sp.n_splits) * D + i] = acc;
             }
             named_sync(2, 128);
         }

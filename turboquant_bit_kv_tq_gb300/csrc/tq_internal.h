@@ -59,8 +59,9 @@ struct ParamsLayout {
 };
 
 // Query-side fp8 pieces of the score contraction: piece k carries the
-// residual of pieces 0..k-1 times 16^k, ~4 significant bits each (~20 in all).
-constexpr int kPieces = 5;
+// residual of pieces 0..k-1 times 16^k, ~4 significant bits each (~16 in all,
+// a relative error of ~2^-17 per operand element).
+constexpr int kPieces = 4;
 
 // Decode geometry.  One split CTA serves a head group of hc query heads
 // (nhg groups per KV head); its value contraction runs in nth n-tiles of 4
