@@ -237,6 +237,16 @@ enum { TQ_PROF_STORE = 0, TQ_PROF_DECODE_SPLIT = 1 };
 tq_status tq_set_profile_events(tq_cache* cache, int kernel, void* start_event, void* stop_event);
 
 /*
+ * Tuning: tq_store encodes at most `max_vectors` (token, KV head) vectors with
+ * one CTA per vector, without staging S in shared memory (the latency-bound
+ * shape of a decode step's new tokens), and larger calls with the persistent
+ * eight-vectors-per-CTA kernel.  Both write identical bytes.  A negative value
+ * restores the default, 16 x the device's SM count.  Process-wide; takes
+ * effect for later calls.  Returns TQ_OK.
+ */
+tq_status tq_set_store_small_max(int64_t max_vectors);
+
+/*
  * Read and clear the device error word (TQ_DEVERR_* bits).  Synchronises
  * `stream`; the only synchronising call besides tq_cache_create.
  */

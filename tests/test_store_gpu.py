@@ -64,8 +64,17 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["per_vector", "persistent"])
+def store_path(request):
+    """Run a store test through the one-CTA-per-vector kernel (the default for
+    a few thousand vectors) or the persistent kernel (forced)."""
+    tq.tq_set_store_small_max(-1 if request.param == "per_vector" else 0)
+    yield request.param
+    tq.tq_set_store_small_max(-1)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_store_parity_small(case):
+def test_store_parity_small(case, store_path):
     name, d, H, kb, vm, vb, dt, qjl, n_out, sc = case
     w = wl.Workload(name, d, H, H, kb, vm, vb, dt, n_out, sc, seed=11, k_qjl=qjl, batch=1, seq_lens=[300])
     T = 300
@@ -78,7 +87,7 @@ def test_store_parity_small(case):
     assert r["checked_bytes"] > 0
 
 
-def test_store_edge_vectors():
+def test_store_edge_vectors(store_path):
     # zero vectors, constant groups, identical keys, x1e3 outliers, ragged block
     w = wl.Workload("edges", 128, 2, 2, 3, "g32", 4, "bf16", 3, 10.0, seed=12, batch=1, seq_lens=[40])
     K, V = wl.kv_tokens(w, 0, 0, 40)
@@ -94,7 +103,7 @@ def test_store_edge_vectors():
     _check(w, K, V, slots, 4)
 
 
-def test_store_skip_and_bad_slot_sets_device_error():
+def test_store_skip_and_bad_slot_sets_device_error(store_path):
     w = wl.Workload("badslot", 128, 2, 2, 2, "mse", 2, "bf16", 3, 10.0, seed=13, batch=1, seq_lens=[20])
     K, V = wl.kv_tokens(w, 0, 0, 20)
     slots = np.arange(20, dtype=np.int64)

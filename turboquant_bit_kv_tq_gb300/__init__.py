@@ -19,7 +19,7 @@ __all__ = [
     "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
-    "tq_get_device_error", "TQCache",
+    "tq_get_device_error", "tq_set_store_small_max", "TQCache",
     "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT",
 ]
 
@@ -32,6 +32,7 @@ EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
     "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
+    "tq_set_store_small_max",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -106,6 +107,7 @@ def load_library():
             "tq_decode_attention_noalloc": (
                 i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_get_device_error": (i32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+            "tq_set_store_small_max": (i32, [i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -126,6 +128,12 @@ def tq_status_string(status):
 def tq_last_cuda_error():
     """The CUDA runtime message behind the last TQ_ERR_CUDA on this thread."""
     return load_library().tq_last_cuda_error().decode()
+
+
+def tq_set_store_small_max(max_vectors):
+    """Largest store (in token x KV-head vectors) encoded one vector per CTA;
+    negative restores the default (16 x the SM count)."""
+    _check(load_library().tq_set_store_small_max(int(max_vectors)), "tq_set_store_small_max")
 
 
 def _dptr(a):

@@ -11,13 +11,15 @@ template <int D>
 static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) {
     const size_t prep_smem = prep_smem_bytes<D>(a.group);
     static bool prep_attr = false;  // once per head dim, before any capture
+    constexpr size_t kPrepMax = prep_smem_bytes<D>(kMaxG);  // the largest head group's need
     if (!prep_attr) {
-        if (cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return TQ_ERR_CUDA;
+        const tq_status fs = cuda_status_detail(
+            cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepMax),
+            "prep_kernel dynamic shared memory %zu", kPrepMax);
+        if (fs != TQ_OK) return fs;
         prep_attr = true;
     }
-    if (prep_smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
+    if (prep_smem > kPrepMax) return TQ_ERR_UNSUPPORTED;
     size_t smem = 0;
     int grid = 0;
     if (ws_fits(a.gm, D)) {
@@ -62,7 +64,7 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     }
     if (st != TQ_OK) return st;
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
-    combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, 0, s>>>(a);
+    combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, (size_t)a.sp.n_splits * sizeof(float), s>>>(a);
     return cuda_status(cudaGetLastError());
 }
 

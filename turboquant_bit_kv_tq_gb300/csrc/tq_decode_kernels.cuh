@@ -262,16 +262,21 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
         bulk_copy(smem_u32(st), a.dp.st_bf16, D * D * 2, smem_u32(bar));
     }
     const int64_t hbase = (int64_t)b * a.q_heads + (int64_t)g * G;
+    // the queries, the rotation signs and the key codebook's Walsh terms load
+    // together (one memory latency), the S^T copy meanwhile
+    __shared__ float s_signs[D], s_kw[9];
     for (int e = tid; e < G * D; e += blockDim.x)
         qv[e] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[hbase * D + e]
                                           : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[hbase * D + e]);
+    for (int e = tid; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
+    if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
     __syncthreads();
     const float f = a.scale_log2e;
     // R q by an in-warp Hadamard transform (one warp per head)
     for (int h = warp; h < G; h += nwarps) {
         float x[D / 32];
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) x[k] = qv[h * D + lane + 32 * k] * a.dp.signs[lane + 32 * k];
+        for (int k = 0; k < D / 32; ++k) x[k] = qv[h * D + lane + 32 * k] * s_signs[lane + 32 * k];
         fwht_warp<D / 32>(x, lane);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) rq[h * D + lane + 32 * k] = x[k] * rsqrtf((float)D) * f;
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     }
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
-    const float* kw = a.dp.k_walsh;
+    const float* kw = s_kw;
     float bmax = 0.f, bsum = 0.f;
     for (int p = 0; p < gm.npk; ++p) {
         bmax = fmaxf(bmax, fabsf(kw[1 + p]));
@@ -1092,21 +1097,40 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     const int S = a.sp.n_splits;
     const int64_t base = ((int64_t)b * a.q_heads + h) * S;
     __shared__ float o[D];
+    __shared__ float red[2][4];
+    extern __shared__ float wgt[];  // [S] split weights 2^(m_s - M)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // every split's (m, l) at once; M = max m
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
-    float lsum = 0.f, acc[kPerThread];
+    for (int s = tid; s < S; s += 128) {
+        const float2 ml = reinterpret_cast<const float2*>(a.ws_ml)[base + s];
+        wgt[s] = ml.x;
+        M = fmaxf(M, ml.x);
+    }
+    M = warp_max(M);
+    if (lane == 0) red[0][warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+    float lpart = 0.f;
+    for (int s = tid; s < S; s += 128) {
+        const float m = wgt[s];
+        const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);  // empty split: 0
+        wgt[s] = w;
+        lpart = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lpart);
+    }
+    lpart = warp_sum(lpart);
+    if (lane == 0) red[1][warp] = lpart;
+    __syncthreads();
+    const float lsum = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+    float acc[kPerThread];
 #pragma unroll
     for (int p = 0; p < kPerThread; ++p) acc[p] = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const float m = a.ws_ml[(base + s) * 2];
-            if (m == -INFINITY) continue;  // empty split
-            const float w = exp2f(m - M);
-            lsum = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lsum);
+    const float* src = a.ws_acc + base * D + tid;
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) {
+        const float w = wgt[s];
 #pragma unroll
-            for (int p = 0; p < kPerThread; ++p)
-                acc[p] = fmaf(w, a.ws_acc[(base + s) * D + threadIdx.x + 128 * p], acc[p]);
-        }
+        for (int p = 0; p < kPerThread; ++p) acc[p] = fmaf(w, src[(int64_t)s * D + 128 * p], acc[p]);
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll

@@ -264,6 +264,141 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
     }
 }
 
+// Few vectors (a decode step's new tokens): one CTA of d threads per
+// (token, KV head).  Warp 0 encodes the key and the residual, warp 1 the
+// value, then warp w projects the residual onto rows 32w .. 32w+31 of S
+// (row-major bf16, read straight from L2) and writes that word of sign bits.
+// The sums run over i in the same order as store_kernel's.
+template <int D, typename Tin>
+__global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
+    constexpr int PER = D / 32;
+    constexpr int kChunk = 16;  // uint4 (8 bf16) loads of an S row held at once
+    __shared__ __align__(16) float r_s[D];
+    __shared__ float s_signs[D], s_kb[kMaxLevels], s_kc[kMaxLevels], s_vb[kMaxLevels];
+    __shared__ float rho_s;
+    __shared__ uint8_t cw_s[D];
+    const Layout& L = a.lay;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t w = blockIdx.x;
+    const int64_t t = w / a.heads;
+    const int h = (int)(w - t * a.heads);
+    const int64_t slot = a.slots[t];
+    if (slot < 0 || slot >= a.num_slots) {
+        if (slot != -1 && threadIdx.x == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
+        return;
+    }
+    const int row = (int)(slot & 15);
+    uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
+    const bool qjl = L.k_qjl;
+    // every load of the encoding at once: the input vector (warp 0: key,
+    // warp 1: value), the tables, and this warp's first S rows
+    float x[PER];
+    if (warp < 2) {
+        const Tin* in = static_cast<const Tin*>(warp == 0 ? a.k : a.v) + w * D;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) x[k] = load_as_float(in + lane + 32 * k);
+    }
+    s_signs[threadIdx.x] = __ldg(a.dp.signs + threadIdx.x);
+    if (threadIdx.x < kMaxLevels) {
+        s_kb[threadIdx.x] = __ldg(a.dp.k_bound + threadIdx.x);
+        s_kc[threadIdx.x] = __ldg(a.dp.k_cent + threadIdx.x);
+        s_vb[threadIdx.x] = __ldg(a.dp.v_bound + threadIdx.x);
+    }
+    const uint4* srow = reinterpret_cast<const uint4*>(a.dp.s_bf16 + (size_t)(32 * warp + lane) * D);
+    uint4 sv[kChunk];
+    if (qjl) {
+#pragma unroll
+        for (int q = 0; q < kChunk; ++q) sv[q] = __ldg(srow + q);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // ------------------------------------------------------------ key
+        int idx[PER];
+        const float n = mse_codes<D>(x, s_signs, s_kb, (1 << L.k_bits) - 1, lane, idx);
+        const __half n16 = __float2half_rn(n);
+        write_bit_planes<D>(idx, L.k_bits, page + L.k_codes, row, lane);
+        if (lane == 0) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
+        if (qjl) {
+            float c[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) c[k] = s_kc[idx[k]];
+            fwht_warp<PER>(c, lane);
+            const float n16f = __half2float(n16), rsd = rsqrtf((float)D);
+            float rr = 0.f;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = lane + 32 * k;
+                const float res = x[k] - n16f * (c[k] * s_signs[i] * rsd);
+                r_s[i] = res;
+                rr = fmaf(res, res, rr);
+            }
+            const float rho = sqrtf(warp_sum(rr));
+            if (lane == 0) rho_s = rho;
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- value
+        if (L.v_mode == TQ_V_MSE) {
+            int idx[PER];
+            const float vn = mse_codes<D>(x, s_signs, s_vb, (1 << L.v_bits) - 1, lane, idx);
+            write_bit_planes<D>(idx, L.v_bits, page + L.v_codes, row, lane);
+            if (lane == 0) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(vn);
+        } else {
+            const int top = (1 << L.v_bits) - 1;
+            uint32_t* meta = reinterpret_cast<uint32_t*>(page + L.v_meta + row * L.v_meta_row);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const float lo = warp_min(x[k]), hi = warp_max(x[k]);
+                const __half z16 = __float2half_rn(lo);
+                const __half s16 = __float2half_rn((hi - lo) / (float)top);
+                const float zf = __half2float(z16), sf = __half2float(s16);
+                int q = 0;
+                if (sf > 0.f) {
+                    const float tq = (x[k] - zf) / sf;
+                    const float fl = floorf(tq);
+                    q = (int)fl + ((tq - fl) >= 0.5f ? 1 : 0);
+                    q = min(max(q, 0), top);
+                }
+                cw_s[g32_slot<D>(lane + 32 * k)] = (uint8_t)q;
+                if (lane == k)
+                    meta[k] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+            }
+            __syncwarp();
+            pack_row(cw_s, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
+        }
+    }
+    if (!qjl) return;
+    __syncthreads();
+    // z_j = sum_i S[j][i] r_i for j = 32 warp + lane; bit j = [z_j >= 0]
+    float z = 0.f;
+#pragma unroll 1
+    for (int q0 = 0; q0 < D / 8; q0 += kChunk) {
+        if (q0 > 0) {
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) sv[q] = __ldg(srow + q0 + q);
+        }
+#pragma unroll
+        for (int q = 0; q < kChunk; ++q) {
+            const float4 ra = *reinterpret_cast<const float4*>(&r_s[8 * (q0 + q)]);
+            const float4 rb = *reinterpret_cast<const float4*>(&r_s[8 * (q0 + q) + 4]);
+            const uint4 u = sv[q];
+            z = fmaf(__uint_as_float(u.x << 16), ra.x, z);
+            z = fmaf(__uint_as_float(u.x & 0xFFFF0000u), ra.y, z);
+            z = fmaf(__uint_as_float(u.y << 16), ra.z, z);
+            z = fmaf(__uint_as_float(u.y & 0xFFFF0000u), ra.w, z);
+            z = fmaf(__uint_as_float(u.z << 16), rb.x, z);
+            z = fmaf(__uint_as_float(u.z & 0xFFFF0000u), rb.y, z);
+            z = fmaf(__uint_as_float(u.w << 16), rb.z, z);
+            z = fmaf(__uint_as_float(u.w & 0xFFFF0000u), rb.w, z);
+        }
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, z >= 0.f);
+    if (lane == 0) reinterpret_cast<uint32_t*>(page + L.k_signs + row * (D / 8))[warp] = bits;
+    if (threadIdx.x == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho_s);
+}
+
+// largest vector count for store_small_kernel; negative: 16 x the SM count
+static int64_t g_small_max = -1;
+
 template <int D, typename Tin>
 static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1) {
     const size_t smem = (size_t)D * D * 2 + 8 * D * 4 + 8 * D + (D + 4 * kMaxLevels) * 4;
@@ -279,10 +414,15 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    const int64_t want = (a.num_tokens * a.heads + 7) / 8;
-    const int grid = (int)std::min<int64_t>(want, (int64_t)sms * (D == 128 ? 4 : 1));
+    const int64_t nvec = a.num_tokens * a.heads;
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
-    kern<<<grid, 256, smem, s>>>(a);
+    if (nvec <= (g_small_max < 0 ? (int64_t)sms * 16 : g_small_max)) {
+        // few vectors: one CTA each (no shared copy of S to stage)
+        store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
+    } else {
+        const int grid = (int)std::min<int64_t>((nvec + 7) / 8, (int64_t)sms * (D == 128 ? 4 : 1));
+        kern<<<grid, 256, smem, s>>>(a);
+    }
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
     return cuda_status(cudaGetLastError());
 }
@@ -290,6 +430,11 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
 }  // namespace tq
 
 using namespace tq;
+
+extern "C" tq_status tq_set_store_small_max(int64_t max_vectors) {
+    g_small_max = max_vectors < 0 ? -1 : max_vectors;
+    return TQ_OK;
+}
 
 extern "C" tq_status tq_store(const tq_cache* c, const void* k, const void* v, int in_dtype, int64_t num_tokens,
                               const int64_t* slot_mapping, void* cache_buf, void* stream) {
