@@ -104,8 +104,9 @@ ParamsLayout params_layout(const tq_cache_config& c) {
 DecodeGeom decode_geom(const tq_cache_config& c) {
     DecodeGeom g;
     const int G = c.num_q_heads / c.num_kv_heads;
-    // value accumulators stay in registers: at most 8 heads at d=128, 4 at d=256
-    g.hc = G <= 4 ? G : (c.head_dim == 128 && G % 8 == 0 ? 8 : 4);
+    // head groups of at most 4 query heads (one n-tile: the warp-specialized
+    // split kernel's consumers hold one n-tile of value accumulators)
+    g.hc = G <= 4 ? G : 4;
     g.nhg = G / g.hc;
     g.nth = (g.hc + 3) / 4;
     g.npk = 1 << (c.k_bits - 1);
