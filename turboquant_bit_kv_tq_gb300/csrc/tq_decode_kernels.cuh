@@ -1126,11 +1126,15 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 #pragma unroll
     for (int p = 0; p < kPerThread; ++p) acc[p] = 0.f;
     const float* src = a.ws_acc + base * D + tid;
+    // an empty split (weight 0) may leave its partial unwritten: skip it
 #pragma unroll 8
     for (int s = 0; s < S; ++s) {
         const float w = wgt[s];
 #pragma unroll
-        for (int p = 0; p < kPerThread; ++p) acc[p] = fmaf(w, src[(int64_t)s * D + 128 * p], acc[p]);
+        for (int p = 0; p < kPerThread; ++p) {
+            const float v = src[(int64_t)s * D + 128 * p];
+            acc[p] = w > 0.f ? fmaf(w, v, acc[p]) : acc[p];
+        }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll

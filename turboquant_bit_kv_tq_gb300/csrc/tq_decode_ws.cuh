@@ -99,17 +99,18 @@ __host__ __device__ inline WsLayout ws_layout(int page_bytes, const DecodeGeom& 
 // a configuration runs here when all its score planes fit one A buffer
 __host__ __device__ inline bool ws_fits(const DecodeGeom& gm, int d) { return gm.npl * (d / 4) <= ws_acap(gm.nth); }
 
-// work item idx: head group fastest, then split, KV head, sequence; every CTA
-// takes a contiguous run of items, so consecutive items of a CTA mostly share
-// their query operand images and re-read the pages of the other head group
-// from L2
+// work item idx: split fastest, then head group, KV head, sequence; every CTA
+// takes a contiguous run of items, so consecutive items of a CTA are mostly
+// consecutive splits of one head group, which its consumers merge as one
+// (the other head group's CTAs, a few positions on, read the same pages at
+// about the same time and find them in L2)
 __device__ inline WsItem ws_item(const DecodeArgs& a, int idx, bool* len_bad) {
     WsItem it;
     const int nhg = a.gm.nhg, nch = a.sp.n_chunks;
-    it.hgi = idx % nhg;
-    idx /= nhg;
     it.chunk = idx % nch;
     idx /= nch;
+    it.hgi = idx % nhg;
+    idx /= nhg;
     it.g = idx % a.heads;
     it.b = idx / a.heads;
     int len = a.seq_lens[it.b];
@@ -550,22 +551,30 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
         }
         int tseq = 0, st = 0;
         uint32_t sph = 0;  // stage of tile tseq and the parity of its fill
+        // a run: consecutive items of one (sequence, KV head, head group), i.e.
+        // consecutive splits, accumulated as one and written as split run0
+        float m_ref[H4], l_part[H4], zacc[H4][NZ];
+        float pv[NTH][NMT][4];
+        int run0 = -1;
+        bool fresh = true;  // nothing accumulated in this run yet
         for (int k = 0; k < nk; ++k) {
             const WsItem it = items[k];
             const float* cst = icst + k * H4 * 4;
-            float m_ref[H4], l_part[H4], zacc[H4][NZ];
-            float pv[NTH][NMT][4];
+            if (run0 < 0) {
+                run0 = it.chunk;
+                fresh = true;
 #pragma unroll
-            for (int h = 0; h < H4; ++h) {
-                m_ref[h] = -INFINITY;
-                l_part[h] = 0.f;
+                for (int h = 0; h < H4; ++h) {
+                    m_ref[h] = -INFINITY;
+                    l_part[h] = 0.f;
 #pragma unroll
-                for (int z = 0; z < NZ; ++z) zacc[h][z] = 0.f;
+                    for (int z = 0; z < NZ; ++z) zacc[h][z] = 0.f;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+                    for (int mt = 0; mt < NMT; ++mt) pv[nt][mt][0] = pv[nt][mt][1] = pv[nt][mt][2] = pv[nt][mt][3] = 0.f;
             }
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-                for (int mt = 0; mt < NMT; ++mt) pv[nt][mt][0] = pv[nt][mt][1] = pv[nt][mt][2] = pv[nt][mt][3] = 0.f;
             for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
                 const int s = st;
                 ws_wait(B(&full[s]), sph, dead, err);
@@ -609,10 +618,11 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 }
 
                 // ---------------- online softmax per warp (lazy reference maximum)
-                if (t == 0) {
-                    // the item's first tile: nothing accumulated yet to rescale
+                if (fresh) {
+                    // the run's first tile: nothing accumulated yet to rescale
 #pragma unroll
                     for (int h = 0; h < H4; ++h) m_ref[h] = warp_max(sc[h]);
+                    fresh = false;
                 } else {
                     // a reference moves only when a score passes it by kRescaleSlack
                     bool mv = false;
@@ -796,7 +806,9 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 }
             }
 
-            // ---------------- item end: per-warp partials -> merged split partial
+            // ---------------- run end: per-warp partials -> merged split partial
+            if (k + 1 < nk && items[k + 1].b == it.b && items[k + 1].g == it.g && items[k + 1].hgi == it.hgi)
+                continue;  // the next item continues this run
             named_sync(2, 128);  // every warp is done with its probability buffer
 #pragma unroll
             for (int h = 0; h < H4; ++h) {
@@ -841,7 +853,12 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             named_sync(2, 128);
             // merge weights once per (warp, head): 2^(m_w - M) against the
             // largest reference M; they go where the zero-point sums were
-            const int64_t o0 = ((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc) * a.sp.n_splits + it.chunk;
+            const int64_t o0 = ((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc) * a.sp.n_splits + run0;
+            // the run's other splits are empty (m = -inf, l = 0)
+            for (int e = ctid; e < hc * (it.chunk - run0); e += 128) {
+                const int h = e / (it.chunk - run0), c = 1 + e % (it.chunk - run0);
+                reinterpret_cast<float2*>(a.ws_ml)[o0 + (int64_t)h * a.sp.n_splits + c] = make_float2(-INFINITY, 0.f);
+            }
             float* wts = reinterpret_cast<float*>(smem + sl.zsm);  // [warp][head]
             if (ctid < hc) {
                 const int h = ctid;
@@ -869,6 +886,7 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
                 a.ws_acc[(o0 + (int64_t)h * a.sp.n_splits) * D + i] = acc;
             }
             named_sync(2, 128);
+            run0 = -1;
         }
     }
     tc_fence_before();
