@@ -192,6 +192,21 @@ def test_decode_seq_len_beyond_table_is_flagged():
     assert c.device_error() & tq.TQ_DEVERR_SEQLEN
 
 
+def test_decode_negative_seq_len_is_flagged_and_empty():
+    # a negative length is flagged and read as 0; the other sequence is intact
+    w = _wl("llama8b_gqa4_b16_8k")
+    prob = Problem(w, [32, 64])
+    c = _make_cache(prob, 1)
+    q = _dev(prob.Q, w.dtype)
+    lens = torch.tensor([-5, 64], dtype=torch.int32, device="cuda")
+    out = c.decode(q, torch.from_numpy(prob.table).cuda(), lens)
+    torch.cuda.synchronize()
+    assert c.device_error() & tq.TQ_DEVERR_SEQLEN
+    got = out.cpu().numpy()
+    assert np.all(got[0] == 0)
+    _assert_close(got[1], prob.oracle()[1])
+
+
 def test_decode_cuda_graph_replay_with_new_lengths():
     # the grid depends only on the configuration: capture once, replay with
     # changed sequence lengths and block tables (fixed-grid requirement of

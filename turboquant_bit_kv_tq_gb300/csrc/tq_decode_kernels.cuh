@@ -1100,12 +1100,15 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     __shared__ float red[2][4];
     extern __shared__ float wgt[];  // [S] split weights 2^(m_s - M)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // every split's (m, l) at once; M = max m
+    // every split's (m, l) at once; M = max m.  Compressed splits past the
+    // sequence's length are empty and need not have been written.
+    const int len = max(0, min(a.seq_lens[b], a.max_blocks * kBlock));
+    const int nch = (len + a.split_blocks * kBlock - 1) / (a.split_blocks * kBlock);
     float M = -INFINITY;
     for (int s = tid; s < S; s += 128) {
-        const float2 ml = reinterpret_cast<const float2*>(a.ws_ml)[base + s];
-        wgt[s] = ml.x;
-        M = fmaxf(M, ml.x);
+        const float m = (s < a.sp.n_chunks && s >= nch) ? -INFINITY : a.ws_ml[(base + s) * 2];
+        wgt[s] = m;
+        M = fmaxf(M, m);
     }
     M = warp_max(M);
     if (lane == 0) red[0][warp] = M;
@@ -1116,7 +1119,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
         const float m = wgt[s];
         const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);  // empty split: 0
         wgt[s] = w;
-        lpart = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lpart);
+        if (w > 0.f) lpart = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lpart);
     }
     lpart = warp_sum(lpart);
     if (lane == 0) red[1][warp] = lpart;

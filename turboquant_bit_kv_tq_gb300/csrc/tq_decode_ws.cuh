@@ -99,23 +99,47 @@ __host__ __device__ inline WsLayout ws_layout(int page_bytes, const DecodeGeom& 
 // a configuration runs here when all its score planes fit one A buffer
 __host__ __device__ inline bool ws_fits(const DecodeGeom& gm, int d) { return gm.npl * (d / 4) <= ws_acap(gm.nth); }
 
-// work item idx: split fastest, then head group, KV head, sequence; every CTA
-// takes a contiguous run of items, so consecutive items of a CTA are mostly
-// consecutive splits of one head group, which its consumers merge as one
-// (the other head group's CTAs, a few positions on, read the same pages at
-// about the same time and find them in L2)
+// compressed length of sequence b, clamped to the block table (bad: out of range)
+__device__ __forceinline__ int ws_seq_len(const DecodeArgs& a, int b, bool* bad) {
+    const int len = a.seq_lens[b];
+    *bad = len < 0 || len > a.max_blocks * kBlock;
+    return max(0, min(len, a.max_blocks * kBlock));
+}
+// splits of sequence b that hold tokens
+__device__ __forceinline__ int ws_seq_chunks(const DecodeArgs& a, int len) {
+    const int st = a.split_blocks * kBlock;
+    return (len + st - 1) / st;
+}
+// work items: the non-empty splits of every (sequence, KV head, head group),
+// split fastest, then head group, KV head, sequence (empty splits are left to
+// the combine, which reads none beyond a sequence's length); every CTA takes
+// a contiguous run of items, so consecutive items of a CTA are mostly
+// consecutive splits of one head group, which its consumers merge as one (the
+// other head group's CTAs, a few positions on, read the same pages at about
+// the same time and find them in L2)
+__device__ inline int ws_item_count(const DecodeArgs& a) {
+    int n = 0;
+    for (int b = 0; b < a.batch; ++b) {
+        bool bad;
+        n += a.heads * a.gm.nhg * ws_seq_chunks(a, ws_seq_len(a, b, &bad));
+    }
+    return n;
+}
 __device__ inline WsItem ws_item(const DecodeArgs& a, int idx, bool* len_bad) {
     WsItem it;
-    const int nhg = a.gm.nhg, nch = a.sp.n_chunks;
+    const int nhg = a.gm.nhg;
+    int b = 0, len = 0, nch = 0;
+    for (;; ++b) {
+        len = ws_seq_len(a, b, len_bad);
+        nch = ws_seq_chunks(a, len);
+        if (idx < a.heads * nhg * nch || b == a.batch - 1) break;
+        idx -= a.heads * nhg * nch;
+    }
+    it.b = b;
     it.chunk = idx % nch;
     idx /= nch;
     it.hgi = idx % nhg;
-    idx /= nhg;
-    it.g = idx % a.heads;
-    it.b = idx / a.heads;
-    int len = a.seq_lens[it.b];
-    *len_bad = len < 0 || len > a.max_blocks * kBlock;
-    len = max(0, min(len, a.max_blocks * kBlock));
+    it.g = idx / nhg;
     it.t0 = it.chunk * a.split_blocks * kBlock;
     it.t1 = min(len, it.t0 + a.split_blocks * kBlock);
     it.n_pages = it.t1 > it.t0 ? (it.t1 - it.t0 + kBlock - 1) / kBlock : 0;
@@ -277,10 +301,13 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     const DecodeGeom gm = a.gm;
     const Layout& L = a.lay;
     const int S = a.stages;
-    const int n_items = a.batch * a.heads * gm.nhg * a.sp.n_chunks;
-    const int KI = ws_items_per_cta(n_items, gridDim.x);
-    const int k0 = blockIdx.x * KI;                 // this CTA's first item
-    const int nk = max(0, min(KI, n_items - k0));  // and its item count
+    // shared-memory arrays hold KI items (every split of every head group);
+    // the non-empty ones are dealt out KR per CTA
+    const int KI = ws_items_per_cta(a.batch * a.heads * gm.nhg * a.sp.n_chunks, gridDim.x);
+    const int n_items = ws_item_count(a);
+    const int KR = ws_items_per_cta(n_items, gridDim.x);
+    const int k0 = blockIdx.x * KR;                 // this CTA's first item
+    const int nk = max(0, min(KR, n_items - k0));  // and its item count
     const WsLayout sl = ws_layout<D>(L.page_bytes, gm, NSET, S, KI, a.split_blocks);
     uint8_t* ring = smem + sl.ring;
     uint8_t* bimg = smem + sl.bimg;
@@ -327,10 +354,14 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     const int hc = gm.hc, SB = a.split_blocks;
     for (int k = tid; k < nk; k += blockDim.x) {
         bool bad = false;
-        const WsItem it = ws_item(a, k0 + k, &bad);
-        items[k] = it;
-        if (bad && it.g == 0 && it.chunk == 0 && it.hgi == 0) set_error(err, TQ_DEVERR_SEQLEN);
+        items[k] = ws_item(a, k0 + k, &bad);
     }
+    if (blockIdx.x == 0)
+        for (int b = tid; b < a.batch; b += blockDim.x) {
+            bool bad = false;
+            ws_seq_len(a, b, &bad);
+            if (bad) set_error(err, TQ_DEVERR_SEQLEN);
+        }
     __syncthreads();
     if (tid == 0) {
         const int nimg = ws_nimg(gm);
