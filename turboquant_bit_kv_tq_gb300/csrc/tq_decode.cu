@@ -50,10 +50,20 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         const tq_status cfg = split_config<D>(a, &a.stages, &smem);
         if (cfg != TQ_OK) return cfg;
     }
-    prep_kernel<D><<<dim3(a.heads, a.batch), 256, prep_smem, s>>>(a);
+    {
+        // the split (and tail) and combine kernels launch programmatically
+        // (each one's prologue overlaps the previous kernel's tail) unless
+        // profiling events sit between the launches; the query prep launches
+        // in stream order (overlapping it with a preceding store measured
+        // slower)
+        a.pdl = ev0 == nullptr && ev1 == nullptr;
+        const cudaError_t e = launch_pdl(false, prep_kernel<D>, dim3(a.heads, a.batch), dim3(256), prep_smem, s, a);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     if (grid > 0 && a.tail_cap > 0) {
         const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
-        tail_kernel<D><<<dim3(a.heads, a.batch), 128, tail_smem, s>>>(a);
+        const cudaError_t e = launch_pdl(a.pdl, tail_kernel<D>, dim3(a.heads, a.batch), dim3(128), tail_smem, s, a);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
     tq_status st;
@@ -64,8 +74,8 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     }
     if (st != TQ_OK) return st;
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
-    combine_kernel<D><<<dim3(a.q_heads, a.batch), 128, (size_t)a.sp.n_splits * sizeof(float), s>>>(a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(a.pdl, combine_kernel<D>, dim3(a.q_heads, a.batch), dim3(128),
+                                  (size_t)a.sp.n_splits * sizeof(float), s, a));
 }
 
 tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1) {

@@ -65,6 +65,7 @@ struct DecodeArgs {
     int heads, q_heads, group;
     int max_blocks, split_blocks, tail_cap;
     int stages;  // split ring depth (tiles)
+    bool pdl;    // split and combine launch programmatically (no profiling events between them)
     Splits sp;
     Layout lay;
     DeviceParams dp;
@@ -245,6 +246,7 @@ __host__ __device__ constexpr size_t prep_smem_bytes(int G) {
 
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
+    pdl_launch_dependents();  // the split kernel's prologue may start
     const int g = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
     const int G = a.group, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -572,6 +574,8 @@ __host__ __device__ constexpr size_t split_red_bytes(int h4) {
 
 template <int D, int KB, bool G32, int VB, int NTH>
 __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the query prep's results
     constexpr int NPK = 1 << (KB - 1);  // key code planes
     constexpr int NW = D / 32;          // 32-bit words of a plane row
     constexpr int NCOL = D / 4;         // tensor-memory columns of one plane
@@ -1091,6 +1095,8 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
 // --------------------------------------------------------------- combine
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the split partials
     constexpr int kPerThread = D / 128;
     const int h = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
@@ -1186,7 +1192,12 @@ inline tq_status launch_split(const DecodeArgs& a, cudaStream_t s, size_t smem) 
         }
         attr_set = true;
     }
-    kern<<<dim3(a.sp.n_splits, a.heads * a.gm.nhg, a.batch), 32 * kWarpsPerGroup, smem, s>>>(a);
+    {
+        const cudaError_t e =
+            launch_pdl(a.pdl, kern, dim3(a.sp.n_splits, a.heads * a.gm.nhg, a.batch), dim3(32 * kWarpsPerGroup), smem,
+                       s, a);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     return cuda_status(cudaGetLastError());
 }
 

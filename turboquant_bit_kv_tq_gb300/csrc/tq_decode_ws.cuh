@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(tslot, kWsTmemCols);
+    pdl_launch_dependents();
 
     // prologue: this CTA's items, their per-head constants and block ids into
     // shared memory (batches of independent loads), so that the tile loop
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             last[sl_] = k;
         }
     }
+    pdl_wait();  // the query prep's results (and, through it, the stored pages)
     for (int base = tid; base < nk * H4 * 4; base += blockDim.x * 4) {
         float v[4];
 #pragma unroll
@@ -928,6 +930,8 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
 // Exact hybrid-tail tokens of every (KV head, sequence) as split n_chunks.
 template <int D>
 __global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the query prep's results
     extern __shared__ __align__(16) uint8_t smem[];
     const int g = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
@@ -945,8 +949,7 @@ inline tq_status launch_split_ws(const DecodeArgs& a, cudaStream_t s, size_t sme
         }
         attr_set = true;
     }
-    kern<<<grid, kWsThreads, smem, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(a.pdl, kern, dim3(grid), dim3(kWsThreads), smem, s, a);
     if (e != cudaSuccess) {
         cudaFuncAttributes fa{};
         cudaFuncGetAttributes(&fa, kern);
