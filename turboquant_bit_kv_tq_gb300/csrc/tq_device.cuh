@@ -70,11 +70,12 @@ template <int PER>
 __device__ __forceinline__ void fwht_warp(float (&x)[PER], int lane) {
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
-        const bool upper = lane & h;
+        // lower lane: x + other; upper lane: other - x (one exact fma by +-1)
+        const float sgn = (lane & h) ? -1.f : 1.f;
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const float other = __shfl_xor_sync(0xffffffffu, x[k], h);
-            x[k] = upper ? other - x[k] : x[k] + other;
+            x[k] = fmaf(sgn, x[k], other);
         }
     }
 #pragma unroll

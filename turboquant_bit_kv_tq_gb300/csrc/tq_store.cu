@@ -5,8 +5,9 @@
 // quantises, packs and writes the paged KV cache).
 //
 // One warp encodes one (token, KV head) vector at a time; lane l holds
-// coordinates l + 32k.  The QJL projection S r runs on CUDA cores from a
-// shared-memory copy of S^T.
+// coordinates l + 32k.  In bulk the QJL projection S r of eight vectors at a
+// time runs on tensor cores (mma.sync bf16, S as the A operand from shared
+// memory); for a few vectors, on CUDA cores from S rows in L2.
 
 #include <algorithm>
 
@@ -88,22 +89,70 @@ __device__ __forceinline__ float mse_codes(const float (&v)[D / 32], const float
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const float yk = y[k] * inv;
+        // number of boundaries strictly below yk: a binary search over the
+        // sorted boundaries (nb = 2^b - 1, b steps)
         int c = 0;
-        for (int j = 0; j < nb; ++j) c += yk > bound[j];
+        for (int step = (nb + 1) >> 1; step > 0; step >>= 1)
+            if (yk > bound[c + step - 1]) c += step;
         idx[k] = c;
     }
     return n;
 }
 
+// Bulk store (bulk appends): each warp encodes its vectors NB = 8 at a time.
+// Phase A encodes one (token, KV head) vector at a time (lane l holds
+// coordinates l + 32k), up to the key residual r, which it leaves in shared
+// memory as three bf16 pieces (r = hi + mid + lo to ~24 significant bits).
+// Phase B projects the eight residuals at once on tensor cores: z = S [r_0 ..
+// r_7] as (d/16)^2 m16n8k16 tiles per piece, with S (bf16, exact) as the A
+// operand from a padded shared copy; bit j of vector v is [z_jv >= 0], and
+// lane (v, w) assembles sign word w of vector v from the tiles' ballots.
+constexpr int kStoreNB = 8;  // vectors per warp batch (the MMA's N)
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// bits 4g (g = 0..7) of x -> bits g
+__device__ __forceinline__ uint32_t gather_nibble_bits(uint32_t x) {
+    x &= 0x11111111u;
+    x = (x | (x >> 3)) & 0x03030303u;
+    x = (x | (x >> 6)) & 0x000F000Fu;
+    return (x | (x >> 12)) & 0xFFu;
+}
+
+template <int D>
+struct StoreBulkLayout {
+    static constexpr int kWarps = D == 128 ? 8 : 4;
+    static constexpr int SP = 2 * D + 16;             // padded S row (bytes)
+    static constexpr int VS = 3 * 2 * D + 16;         // one vector's residual pieces (bytes, padded)
+    static constexpr size_t s_off = 0;
+    static constexpr size_t rp_off = s_off + (size_t)D * SP;
+    static constexpr size_t sg_off = rp_off + (size_t)kWarps * kStoreNB * VS;
+    static constexpr size_t cw_off = sg_off + (size_t)kWarps * kStoreNB * 8;
+    static constexpr size_t tab_off = cw_off + (size_t)kWarps * D;
+    static constexpr size_t total = tab_off + (size_t)(D + 4 * kMaxLevels) * 4;
+};
+
 template <int D, typename Tin>
-__global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
+__global__ void __launch_bounds__(StoreBulkLayout<D>::kWarps * 32) store_kernel(StoreArgs a) {
+    using SL = StoreBulkLayout<D>;
     constexpr int PER = D / 32;
-    constexpr int kWarps = 8;
+    constexpr int kWarps = SL::kWarps;
+    constexpr int NT = D / 16;  // m16n8k16 tiles per dimension
     extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t* st = reinterpret_cast<uint16_t*>(smem);                    // S^T, bf16 [D][D]
-    float* rbuf = reinterpret_cast<float*>(smem + D * D * 2);            // [warps][D]
-    uint8_t* codes = smem + D * D * 2 + kWarps * D * 4;                  // [warps][D]
-    float* tables = reinterpret_cast<float*>(codes + kWarps * D);        // signs, k/v cent, k/v bound
+    uint8_t* s_rows = smem + SL::s_off;                                   // S, bf16 [D][D], padded rows
+    uint8_t* rp_all = smem + SL::rp_off;                                  // [warp][NB] residual pieces
+    uint8_t** sg_all = reinterpret_cast<uint8_t**>(smem + SL::sg_off);    // [warp][NB] sign rows (or null)
+    uint8_t* codes = smem + SL::cw_off;                                   // [warp][D]
+    float* tables = reinterpret_cast<float*>(smem + SL::tab_off);
     float* s_signs = tables;
     float* s_kc = tables + D;
     float* s_kb = s_kc + kMaxLevels;
@@ -111,17 +160,11 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
     float* s_vb = s_vc + kMaxLevels;
 
     const Layout& L = a.lay;
-    // S^T (bf16, already transposed in the params) by one bulk copy
-    __shared__ __align__(8) uint64_t st_bar;
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&st_bar)) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&st_bar)), "r"(D * D * 2)
-                     : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                         smem_u32(st)),
-                     "l"(a.dp.st_bf16), "r"(D * D * 2), "r"(smem_u32(&st_bar))
-                     : "memory");
+    // S (row-major bf16) into padded rows: 16-byte chunks
+    for (int e = threadIdx.x; e < D * D / 8; e += blockDim.x) {
+        const int row = e / (D / 8), ch = e % (D / 8);
+        *reinterpret_cast<uint4*>(s_rows + row * SL::SP + 16 * ch) =
+            __ldg(reinterpret_cast<const uint4*>(a.dp.s_bf16) + e);
     }
     for (int e = threadIdx.x; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     for (int e = threadIdx.x; e < kMaxLevels; e += blockDim.x) {
@@ -131,134 +174,178 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         s_vb[e] = a.dp.v_bound[e];
     }
     __syncthreads();
-    {
-        bool landed = false;
-        for (int it = 0; it < (1 << 24) && !landed; ++it) {
-            uint32_t done;
-            asm volatile(
-                "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}\n"
-                : "=r"(done)
-                : "r"(smem_u32(&st_bar))
-                : "memory");
-            landed = done != 0;
-        }
-        if (!landed && threadIdx.x == 0) set_error(a.dp.err, TQ_DEVERR_TIMEOUT);
-    }
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float* r = rbuf + warp * D;
+    const int gq = lane >> 2, tq = lane & 3;
+    uint8_t* rp = rp_all + (size_t)warp * kStoreNB * SL::VS;
+    uint8_t** sg = sg_all + warp * kStoreNB;
     uint8_t* cw = codes + warp * D;
     const float rsd = rsqrtf((float)D);
+    const bool qjl = L.k_qjl;
     const int64_t nvec = a.num_tokens * a.heads;
-    for (int64_t w = (int64_t)blockIdx.x * kWarps + warp; w < nvec; w += (int64_t)gridDim.x * kWarps) {
-        const int64_t t = w / a.heads;
-        const int h = (int)(w - t * a.heads);
-        const int64_t slot = a.slots[t];
-        if (slot < 0 || slot >= a.num_slots) {
-            if (slot != -1 && lane == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
-            continue;
-        }
-        const int row = (int)(slot & 15);
-        uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
-        const Tin* kin = static_cast<const Tin*>(a.k) + w * D;
-        const Tin* vin = static_cast<const Tin*>(a.v) + w * D;
-
-        // ------------------------------------------------------------ key
-        float x[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) x[k] = load_as_float(kin + lane + 32 * k);
-        int idx[PER];
-        const float n = mse_codes<D>(x, s_signs, s_kb, (1 << L.k_bits) - 1, lane, idx);
-        const __half n16 = __float2half_rn(n);
-        write_bit_planes<D>(idx, L.k_bits, page + L.k_codes, row, lane);
-        if (lane == 0) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
-        if (L.k_qjl) {
-            // residual r = k - n16 R^T c[idx], with R^T c = D H c / sqrt(d)
-            float c[PER];
-#pragma unroll
-            for (int k = 0; k < PER; ++k) c[k] = s_kc[idx[k]];
-            fwht_warp<PER>(c, lane);
-            const float n16f = __half2float(n16);
-            float rr = 0.f;
+    const int64_t wstep = (int64_t)gridDim.x * kWarps * kStoreNB;
+    // the next vector's key, value and slot load while the current one is
+    // encoded (one vector ahead, across batches)
+    float nxk[PER], nxv[PER];
+    int64_t nslot = -1;
+    auto prefetch = [&](int64_t w) {
+        if (w < nvec) {
+            const Tin* kin = static_cast<const Tin*>(a.k) + w * D;
+            const Tin* vin = static_cast<const Tin*>(a.v) + w * D;
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
-                const int i = lane + 32 * k;
-                const float res = x[k] - n16f * (c[k] * s_signs[i] * rsd);
-                r[i] = res;
-                rr = fmaf(res, res, rr);
+                nxk[k] = load_as_float(kin + lane + 32 * k);
+                nxv[k] = load_as_float(vin + lane + 32 * k);
             }
-            const float rho = sqrtf(warp_sum(rr));
-            __syncwarp();
-            // z_j = sum_i S[j][i] r_i for j = PER*lane + e (one 8- or 16-byte
-            // load of S^T per i); bit j = [z_j >= 0]
-            float z[PER];
+            nslot = a.slots[w / a.heads];
+        }
+    };
+    prefetch(((int64_t)blockIdx.x * kWarps + warp) * kStoreNB);
+    for (int64_t w0 = ((int64_t)blockIdx.x * kWarps + warp) * kStoreNB; w0 < nvec; w0 += wstep) {
+        // ---------------------------------------------- phase A: per vector
+#pragma unroll 1
+        for (int v = 0; v < kStoreNB; ++v) {
+            const int64_t w = w0 + v;
+            uint8_t* srow = nullptr;  // this vector's sign row, if it is written
+            __nv_bfloat16* pv = reinterpret_cast<__nv_bfloat16*>(rp + v * SL::VS);
+            float x[PER], xv[PER];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) z[e] = 0.f;
-#pragma unroll 4
-            for (int i = 0; i < D; ++i) {
-                const float ri = r[i];
-                uint32_t w[PER / 2];
-                if constexpr (PER == 4) {
-                    const uint2 u = *reinterpret_cast<const uint2*>(st + i * D + PER * lane);
-                    w[0] = u.x;
-                    w[1] = u.y;
+            for (int k = 0; k < PER; ++k) {
+                x[k] = nxk[k];
+                xv[k] = nxv[k];
+            }
+            const int64_t slot = nslot;
+            prefetch(v + 1 < kStoreNB ? w + 1 : w0 + wstep);
+            if (w < nvec) {
+                const int64_t t = nvec < (int64_t)1 << 31 ? (int64_t)((uint32_t)w / (uint32_t)a.heads) : w / a.heads;
+                const int h = (int)(w - t * a.heads);
+                if (slot < 0 || slot >= a.num_slots) {
+                    if (slot != -1 && lane == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
                 } else {
-                    const uint4 u = *reinterpret_cast<const uint4*>(st + i * D + PER * lane);
-                    w[0] = u.x;
-                    w[1] = u.y;
-                    w[2] = u.z;
-                    w[3] = u.w;
-                }
-#pragma unroll
-                for (int e2 = 0; e2 < PER / 2; ++e2) {
-                    z[2 * e2] = fmaf(__uint_as_float(w[e2] << 16), ri, z[2 * e2]);
-                    z[2 * e2 + 1] = fmaf(__uint_as_float(w[e2] & 0xFFFF0000u), ri, z[2 * e2 + 1]);
-                }
-            }
-            // lane l holds bits PER*l .. PER*l+PER-1; gather 32-bit words
-            uint32_t bits = 0;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) bits |= (z[e] >= 0.f ? 1u : 0u) << e;
-            constexpr int LPW = 32 / PER;  // lanes per output word
-            bits <<= PER * (lane % LPW);
-#pragma unroll
-            for (int o = 1; o < LPW; o <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
-            uint32_t* srow = reinterpret_cast<uint32_t*>(page + L.k_signs + row * (D / 8));
-            if (lane % LPW == 0) srow[lane / LPW] = bits;
-            if (lane == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho);
-        }
-        __syncwarp();
+                    const int row = (int)(slot & 15);
+                    uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
 
-        // ---------------------------------------------------------- value
+                    // -------------------------------------------------- key
+                    int idx[PER];
+                    const float n = mse_codes<D>(x, s_signs, s_kb, (1 << L.k_bits) - 1, lane, idx);
+                    const __half n16 = __float2half_rn(n);
+                    write_bit_planes<D>(idx, L.k_bits, page + L.k_codes, row, lane);
+                    if (lane == 0) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
+                    if (qjl) {
+                        // residual r = k - n16 R^T c[idx] as three bf16 pieces
+                        float c[PER];
 #pragma unroll
-        for (int k = 0; k < PER; ++k) x[k] = load_as_float(vin + lane + 32 * k);
-        if (L.v_mode == TQ_V_MSE) {
-            const float vn = mse_codes<D>(x, s_signs, s_vb, (1 << L.v_bits) - 1, lane, idx);
-            write_bit_planes<D>(idx, L.v_bits, page + L.v_codes, row, lane);
-            if (lane == 0) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(vn);
-        } else {
-            // group g = coordinates [32g, 32g+32) = slot k of every lane
-            const int top = (1 << L.v_bits) - 1;
-            uint32_t* meta = reinterpret_cast<uint32_t*>(page + L.v_meta + row * L.v_meta_row);
+                        for (int k = 0; k < PER; ++k) c[k] = s_kc[idx[k]];
+                        fwht_warp<PER>(c, lane);
+                        const float n16f = __half2float(n16);
+                        float rr = 0.f;
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const float lo = warp_min(x[k]), hi = warp_max(x[k]);
-                const __half z16 = __float2half_rn(lo);
-                const __half s16 = __float2half_rn((hi - lo) / (float)top);
-                const float zf = __half2float(z16), sf = __half2float(s16);
-                int q = 0;
-                if (sf > 0.f) {
-                    const float tq = (x[k] - zf) / sf;
-                    const float fl = floorf(tq);
-                    q = (int)fl + ((tq - fl) >= 0.5f ? 1 : 0);
-                    q = min(max(q, 0), top);
+                        for (int k = 0; k < PER; ++k) {
+                            const int i = lane + 32 * k;
+                            const float res = x[k] - n16f * (c[k] * s_signs[i] * rsd);
+                            rr = fmaf(res, res, rr);
+                            const __nv_bfloat16 p0 = __float2bfloat16_rn(res);
+                            const float r1 = res - __bfloat162float(p0);
+                            const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+                            const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+                            pv[i] = p0;
+                            pv[D + i] = p1;
+                            pv[2 * D + i] = p2;
+                        }
+                        const float rho = sqrtf(warp_sum(rr));
+                        if (lane == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho);
+                        srow = page + L.k_signs + row * (D / 8);
+                    }
+
+                    // ------------------------------------------------ value
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) x[k] = xv[k];
+                    if (L.v_mode == TQ_V_MSE) {
+                        const float vn = mse_codes<D>(x, s_signs, s_vb, (1 << L.v_bits) - 1, lane, idx);
+                        write_bit_planes<D>(idx, L.v_bits, page + L.v_codes, row, lane);
+                        if (lane == 0) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(vn);
+                    } else {
+                        // group g = coordinates [32g, 32g+32) = slot k of every lane
+                        const int top = (1 << L.v_bits) - 1;
+                        uint32_t* meta = reinterpret_cast<uint32_t*>(page + L.v_meta + row * L.v_meta_row);
+#pragma unroll
+                        for (int k = 0; k < PER; ++k) {
+                            const float lo = warp_min(x[k]), hi = warp_max(x[k]);
+                            const __half z16 = __float2half_rn(lo);
+                            const __half s16 = __float2half_rn((hi - lo) / (float)top);
+                            const float zf = __half2float(z16), sf = __half2float(s16);
+                            int q = 0;
+                            if (sf > 0.f) {
+                                const float tqv = (x[k] - zf) / sf;
+                                const float fl = floorf(tqv);
+                                q = (int)fl + ((tqv - fl) >= 0.5f ? 1 : 0);
+                                q = min(max(q, 0), top);
+                            }
+                            cw[g32_slot<D>(lane + 32 * k)] = (uint8_t)q;
+                            if (lane == k)
+                                meta[k] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+                        }
+                        __syncwarp();
+                        pack_row(cw, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
+                    }
                 }
-                cw[g32_slot<D>(lane + 32 * k)] = (uint8_t)q;
-                if (lane == k)
-                    meta[k] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
             }
+            if (srow == nullptr && qjl) {
+                // a vector with no sign row still feeds the batch: zero residual
+#pragma unroll
+                for (int k = 0; k < PER; ++k) {
+                    const int i = lane + 32 * k;
+                    pv[i] = pv[D + i] = pv[2 * D + i] = __float2bfloat16_rn(0.f);
+                }
+            }
+            if (lane == 0) sg[v] = srow;
             __syncwarp();
-            pack_row(cw, D, L.v_bits, page + L.v_codes + row * L.v_code_row, lane);
+        }
+        if (!qjl) continue;
+
+        // ------------------------------------- phase B: z = S [r_0 .. r_7]
+        // lane (v, w) writes sign words w = (lane & 3) + 4 q of vector v = lane >> 2
+        constexpr int NWQ = D / 128;  // sign words per lane
+        uint32_t word[NWQ];
+#pragma unroll
+        for (int q = 0; q < NWQ; ++q) word[q] = 0u;
+        const uint32_t s_base = smem_u32(s_rows) + (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * SL::SP +
+                                                              ((lane >> 4) * 8) * 2);
+        const uint8_t* rv = rp + gq * SL::VS;  // B operand: vector n = gq
+#pragma unroll 1
+        for (int mt = 0; mt < NT; ++mt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int kt = 0; kt < NT; ++kt) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(s_base + (uint32_t)(16 * mt * SL::SP + 32 * kt), a0, a1, a2, a3);
+#pragma unroll
+                for (int p = 0; p < 3; ++p) {
+                    const uint8_t* bp = rv + p * 2 * D + (16 * kt + 2 * tq) * 2;
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 16);
+                    mma_bf16(acc, a0, a1, a2, a3, b0, b1);
+                }
+            }
+            // acc: z(16 mt + gq, 2 tq), z(.., 2 tq + 1), z(16 mt + gq + 8, 2 tq), z(.., 2 tq + 1)
+            const uint32_t bl0 = __ballot_sync(0xffffffffu, acc[0] >= 0.f);
+            const uint32_t bl1 = __ballot_sync(0xffffffffu, acc[1] >= 0.f);
+            const uint32_t bl2 = __ballot_sync(0xffffffffu, acc[2] >= 0.f);
+            const uint32_t bl3 = __ballot_sync(0xffffffffu, acc[3] >= 0.f);
+            // vector v = gq of this lane: column 2 tq' + e with tq' = v >> 1, e = v & 1
+            const int v = gq, sh = v >> 1;
+            const uint32_t lo8 = gather_nibble_bits(((v & 1) ? bl1 : bl0) >> sh);  // rows 16 mt + 0..7
+            const uint32_t hi8 = gather_nibble_bits(((v & 1) ? bl3 : bl2) >> sh);  // rows 16 mt + 8..15
+            const int wsel = mt >> 1;  // word of rows 32 wsel .. 32 wsel + 31
+            const uint32_t bits16 = (lo8 | (hi8 << 8)) << (16 * (mt & 1));
+#pragma unroll
+            for (int q = 0; q < NWQ; ++q)
+                if (wsel == tq + 4 * q) word[q] |= bits16;
+        }
+        uint8_t* dst = sg[gq];
+        if (dst != nullptr) {
+#pragma unroll
+            for (int q = 0; q < NWQ; ++q) reinterpret_cast<uint32_t*>(dst)[tq + 4 * q] = word[q];
         }
         __syncwarp();
     }
@@ -401,7 +488,7 @@ static int64_t g_small_max = -1;
 
 template <int D, typename Tin>
 static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1) {
-    const size_t smem = (size_t)D * D * 2 + 8 * D * 4 + 8 * D + (D + 4 * kMaxLevels) * 4;
+    const size_t smem = StoreBulkLayout<D>::total;
     auto kern = store_kernel<D, Tin>;
     // one-time setup per kernel instance (before any stream capture)
     static int sms = 0;
@@ -420,8 +507,9 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
         // few vectors: one CTA each (no shared copy of S to stage)
         store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
     } else {
-        const int grid = (int)std::min<int64_t>((nvec + 7) / 8, (int64_t)sms * (D == 128 ? 4 : 1));
-        kern<<<grid, 256, smem, s>>>(a);
+        constexpr int kPerCta = StoreBulkLayout<D>::kWarps * kStoreNB;  // vectors per CTA pass
+        const int grid = (int)std::min<int64_t>((nvec + kPerCta - 1) / kPerCta, (int64_t)sms * (D == 128 ? 2 : 1));
+        kern<<<grid, StoreBulkLayout<D>::kWarps * 32, smem, s>>>(a);
     }
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
     return cuda_status(cudaGetLastError());
