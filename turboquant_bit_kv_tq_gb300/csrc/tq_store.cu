@@ -130,7 +130,7 @@ __device__ __forceinline__ uint32_t gather_nibble_bits(uint32_t x) {
 
 template <int D>
 struct StoreBulkLayout {
-    static constexpr int kWarps = D == 128 ? 8 : 4;
+    static constexpr int kWarps = D == 128 ? 24 : 4;
     static constexpr int SP = 2 * D + 16;             // padded S row (bytes)
     static constexpr int VS = 3 * 2 * D + 16;         // one vector's residual pieces (bytes, padded)
     static constexpr size_t s_off = 0;
@@ -508,7 +508,7 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
         store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
     } else {
         constexpr int kPerCta = StoreBulkLayout<D>::kWarps * kStoreNB;  // vectors per CTA pass
-        const int grid = (int)std::min<int64_t>((nvec + kPerCta - 1) / kPerCta, (int64_t)sms * (D == 128 ? 2 : 1));
+        const int grid = (int)std::min<int64_t>((nvec + kPerCta - 1) / kPerCta, (int64_t)sms);
         kern<<<grid, StoreBulkLayout<D>::kWarps * 32, smem, s>>>(a);
     }
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
