@@ -43,6 +43,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--split-blocks", type=int, default=0, help="KV blocks per decode split (0: per workload)")
+    p.add_argument("--no-qjl", action="store_true",
+                   help="ablation: MSE-only keys (no QJL sign plane or residual norm) on the same workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-store-workload", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -381,6 +383,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
     tq.load_library()
     w = wl.config(args.workload)
+    if args.no_qjl:
+        w = wl.scaled(w, k_qjl=False)
     split_blocks = args.split_blocks or (64 if max(w.seq_lens) > 16384 else 32)
     c, st, table = _setup_decode(w, split_blocks, torch, tq, wl, device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)

@@ -77,6 +77,15 @@ enum {
 };
 
 enum { TQ_DTYPE_F32 = 0, TQ_DTYPE_BF16 = 1 };
+/*
+ * Decode output flag, OR-ed into out_dtype: with MSE-quantised values, return
+ * the attention output in the rotated space, R out = sum_t p_t n16_t c_v[idx_t],
+ * leaving the inverse rotation R^T = D H / sqrt(d) to be folded into the
+ * caller's output projection ([Roadmap] §3.2: the rotation can be absorbed
+ * into the neighbouring weights).  TQ_ERR_INVALID_ARG with group-32 values
+ * (their output is not rotated).
+ */
+enum { TQ_OUT_ROTATED = 0x100 };
 enum { TQ_V_MSE = 0, TQ_V_G32 = 1 };
 
 /* Device error bits (tq_get_device_error). */
@@ -218,7 +227,8 @@ tq_status tq_store(const tq_cache* cache, const void* k, const void* v, int in_d
  *   tail_k/v    device bf16 [batch][H_kv][tail_cap][d] or NULL (no tail)
  *   tail_lens   device int32 [batch] or NULL (no tail)
  *   scale       softmax scale; <= 0 means 1/sqrt(d)
- *   out         device [batch][H_q][d], out_dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16)
+ *   out         device [batch][H_q][d], out_dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16,
+ *               optionally | TQ_OUT_ROTATED)
  * 1 <= batch <= max_batch.  The grid is fixed by (max_batch, H_kv, split count).
  */
 tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype, const void* cache_buf,

@@ -114,6 +114,9 @@ CASES = [
     ("mse3_tail", "d256_gqa8_b8_32k", dict(v_bits=3, k_bits=4, tail=32), [40, 0], [7, 32], 32, 1),
     ("g32v2_k2", "llama8b_gqa4_b16_8k", dict(v_bits=2, k_bits=2), [129, 64], None, 0, 2),
     ("f32_gqa1", "single_head_d128_1k", dict(q_heads=2, kv_heads=2), [77, 255], None, 0, 3),
+    # MSE-only keys (no QJL plane): the ablation of the residual correction
+    ("no_qjl_g32", "llama8b_gqa4_b16_8k", dict(k_qjl=False), [300, 129, 17], None, 0, 4),
+    ("no_qjl_d256_mse", "d256_gqa8_b8_32k", dict(k_qjl=False), [200, 33], None, 0, 4),
 ]
 
 
@@ -129,6 +132,27 @@ def test_decode_parity_small(case):
     assert c.device_error() == 0
     if sum(comp) + (sum(tail) if tail else 0) > 0:
         assert np.abs(ref).max() > 0.1  # non-trivial output
+
+
+def test_decode_rotated_output_is_R_times_out():
+    # MSE values with TQ_OUT_ROTATED: the output stays in the rotated space, so
+    # it must equal R times the oracle's output (R orthogonal: the same error
+    # bar applies); group-32 values reject the flag
+    w = _wl("d256_gqa8_b8_32k")
+    prob = Problem(w, [300, 45])
+    c = _make_cache(prob, 4)
+    inp = prob.gpu_inputs()
+    q = _dev(prob.Q, w.dtype)
+    got = c.decode(q, inp["block_table"], inp["seq_lens"], rotated=True)
+    torch.cuda.synchronize()
+    ref = prob.oracle() @ prob.P.R.T  # out @ R^T = (R out) per row
+    _assert_close(got.cpu().numpy(), ref)
+    w2 = _wl("llama8b_gqa4_b16_8k")
+    prob2 = Problem(w2, [40])
+    c2 = _make_cache(prob2, 2)
+    inp2 = prob2.gpu_inputs()
+    with pytest.raises(tq.TQError):
+        c2.decode(_dev(prob2.Q, w2.dtype), inp2["block_table"], inp2["seq_lens"], rotated=True)
 
 
 def test_decode_empty_sequences_give_zero():

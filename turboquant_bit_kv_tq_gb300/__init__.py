@@ -14,7 +14,7 @@ import os
 import numpy as np
 
 __all__ = [
-    "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_V_MSE", "TQ_V_G32",
+    "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_OUT_ROTATED", "TQ_V_MSE", "TQ_V_G32",
     "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
     "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
@@ -24,6 +24,7 @@ __all__ = [
 ]
 
 TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
+TQ_OUT_ROTATED = 0x100
 TQ_V_MSE, TQ_V_G32 = 0, 1
 TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 
@@ -233,9 +234,10 @@ def tq_store(handle, k, v, slot_mapping, cache, stream=None):
 
 
 def tq_decode_attention(handle, q, cache, block_table, seq_lens, out, tail_k=None, tail_v=None, tail_lens=None,
-                        scale=0.0, stream=None):
+                        scale=0.0, stream=None, rotated=False):
     """q [B, H_q, d] (f32/bf16); block_table int32 [B, max_blocks_per_seq];
-    seq_lens int32 [B]; out [B, H_q, d] (f32/bf16); optional bf16 tail."""
+    seq_lens int32 [B]; out [B, H_q, d] (f32/bf16); optional bf16 tail;
+    rotated: MSE values only, out in the rotated space (R out)."""
     import torch
 
     if tail_k is not None:
@@ -244,8 +246,8 @@ def tq_decode_attention(handle, q, cache, block_table, seq_lens, out, tail_k=Non
     _check(load_library().tq_decode_attention(
         handle, _dev(q, "q"), _dtype_code(q), _dev(cache, "cache"), _dev(block_table, "block_table", torch.int32),
         _dev(seq_lens, "seq_lens", torch.int32), _dev(tail_k, "tail_k"), _dev(tail_v, "tail_v"),
-        _dev(tail_lens, "tail_lens", torch.int32), float(scale), q.shape[0], _dev(out, "out"), _dtype_code(out),
-        _stream_ptr(stream)), "tq_decode_attention")
+        _dev(tail_lens, "tail_lens", torch.int32), float(scale), q.shape[0], _dev(out, "out"),
+        _dtype_code(out) | (TQ_OUT_ROTATED if rotated else 0), _stream_ptr(stream)), "tq_decode_attention")
 
 
 def tq_decode_attention_noalloc(handle, q, cache, block_table, seq_lens, out, tail_k=None, tail_v=None,
@@ -305,13 +307,13 @@ class TQCache:
         tq_store(self.handle, k, v, slot_mapping, self.cache, stream)
 
     def decode(self, q, block_table, seq_lens, out=None, tail_k=None, tail_v=None, tail_lens=None, scale=0.0,
-               stream=None, out_dtype=None):
+               stream=None, out_dtype=None, rotated=False):
         import torch
 
         if out is None:
             out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
         tq_decode_attention(self.handle, q, self.cache, block_table, seq_lens, out, tail_k, tail_v, tail_lens,
-                            scale, stream)
+                            scale, stream, rotated)
         return out
 
     def device_error(self, stream=None):

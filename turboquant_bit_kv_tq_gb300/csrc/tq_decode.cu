@@ -93,7 +93,10 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     if (!c || !q || !cache_buf || !block_table || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
     if (batch < 1 || batch > c->cfg.max_batch) return TQ_ERR_INVALID_ARG;
     if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+    const bool out_rot = (out_dtype & TQ_OUT_ROTATED) != 0;
+    out_dtype &= ~TQ_OUT_ROTATED;
     if (out_dtype != TQ_DTYPE_F32 && out_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+    if (out_rot && c->cfg.v_mode != TQ_V_MSE) return TQ_ERR_INVALID_ARG;
     const bool has_tail = tail_k != nullptr || tail_v != nullptr || tail_lens != nullptr;
     if (has_tail && (!tail_k || !tail_v || !tail_lens || c->cfg.tail_cap == 0)) return TQ_ERR_INVALID_ARG;
     if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
@@ -108,6 +111,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     a.tail_lens = tail_lens;
     a.out = out;
     a.out_dtype = out_dtype;
+    a.out_rotated = out_rot;
     const int d = c->cfg.head_dim;
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
     a.scale_log2e = sc * 1.4426950408889634f;

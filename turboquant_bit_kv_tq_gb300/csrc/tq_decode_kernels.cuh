@@ -59,6 +59,7 @@ struct DecodeArgs {
     const int32_t* tail_lens;
     void* out;
     int out_dtype;
+    bool out_rotated;  // MSE values: leave the output in the rotated space (no R^T)
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -1150,7 +1151,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     for (int p = 0; p < kPerThread; ++p) o[threadIdx.x + 128 * p] = acc[p] * inv;
     __syncthreads();
     const int64_t ob = ((int64_t)b * a.q_heads + h) * D;
-    if (a.lay.v_mode == TQ_V_MSE) {
+    if (a.lay.v_mode == TQ_V_MSE && !a.out_rotated) {
         // out = R^T o = D H o / sqrt(d): in-warp Hadamard transform, warp 0
         if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
