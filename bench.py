@@ -385,7 +385,10 @@ def run_ours(args):
     w = wl.config(args.workload)
     if args.no_qjl:
         w = wl.scaled(w, k_qjl=False)
-    split_blocks = args.split_blocks or (64 if max(w.seq_lens) > 16384 else 32)
+    # blocks per decode split: longer splits for long contexts; a short one
+    # (a few work items in all) needs short splits to spread over the SMs
+    longest = max(w.seq_lens)
+    split_blocks = args.split_blocks or (64 if longest > 16384 else 32 if longest > 2048 else 8)
     c, st, table = _setup_decode(w, split_blocks, torch, tq, wl, device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
