@@ -148,6 +148,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x, device):
+    """The largest of every rank's x (the job's step time is its slowest
+    replica's); x itself on one process."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world_size, units_per_rank, ms):
+    """Whole-job throughput of world_size replicas that each process
+    units_per_rank units in ms milliseconds (weak scaling)."""
+    return world_size * units_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------ CPU baseline
 _CPU_SNIPPET = r"""
 import json, os, sys, time
@@ -408,21 +426,17 @@ def run_ours(args):
         # its decode kernels programmatically, and their times are reported
         # beside the headline
         free_ms = []
-        while time.perf_counter() - t_clk < 0.6:
+        while not free_ms or time.perf_counter() - t_clk < 0.6:
             free_ms += _time_steps(torch, tq, c, st, stream, 20, flush, split_events=False)[0]
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     if c.device_error():
         raise RuntimeError("device error during the timed steps")
-    ms = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), device)
 
     attended = sum(w.compressed_lens()) + sum(w.tail_lens())
-    value = ws * attended / (ms * 1e-3)
+    value = job_value(ws, attended, ms)
     # algorithmic bytes of the split-KV kernel: the compressed bytes of every
     # attended token-head, the block-table entries and the exact tail K/V
     per_token_head = c.page_bytes // 16
@@ -443,11 +457,8 @@ def run_ours(args):
     ws_path = (w.d == 128 and w.k_bits <= 3) or (w.d == 256 and w.k_bits == 2)
     split_kernel_name = "tq::split_ws_kernel" if ws_path else "tq::split_kernel"
     e2e_ms, h2d, d2h = _e2e(torch, c, st, w, stream, args.steps, max(3, args.warmup), flush)
-    e2e_ms_max = e2e_ms
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms_max = float(t.item())
+    e2e_ms_max = max_over_ranks(e2e_ms, device)
+    free_ms_max = max_over_ranks(statistics.mean(free_ms), device)
 
     store_line = None
     if not args.no_store_workload and rank == 0:
@@ -481,12 +492,12 @@ def run_ours(args):
                          "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9},
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "e2e": {"value": ws * attended / (e2e_ms_max * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_value(ws, attended, e2e_ms_max), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
             # the same device-timed step without the split kernel's profiling
             # events between the launches (how a caller runs it)
-            "no_profiling_events": {"ms_per_step": statistics.mean(free_ms) if free_ms else None,
-                                    "value": ws * attended / (statistics.mean(free_ms) * 1e-3) if free_ms else None,
+            "no_profiling_events": {"ms_per_step": free_ms_max,
+                                    "value": job_value(ws, attended, free_ms_max),
                                     "unit": UNIT, "steps": len(free_ms)},
             "gpu_launches": 4 * args.steps,
             "store_workload": store_line,

@@ -1,0 +1,55 @@
+"""The benchmark's multi-replica path on CPU: two gloo ranks on 127.0.0.1
+reduce their step times to the slowest one, and the job value counts every
+replica's units (weak scaling).  The decode path does not shard across GPUs
+(replicas only), so this reduction is its whole multi-rank logic."""
+
+import os
+import socket
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, local = bench._dist()
+        step_ms = 1.5 if rank == 0 else 2.25  # rank 1 is the slowest replica
+        ms = bench.max_over_ranks(step_ms, torch.device("cpu"))
+        torch.distributed.barrier()
+        results[rank] = (ws, r, local, ms, bench.job_value(ws, 131072, ms))
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_to_the_slowest_replica():
+    world = 2
+    with mp.Manager() as mgr:
+        results = mgr.dict()
+        mp.spawn(_rank_main, args=(world, _free_port(), results), nprocs=world, join=True)
+        got = dict(results)
+    for rank in range(world):
+        ws, r, local, ms, value = got[rank]
+        assert (ws, r, local) == (world, rank, rank)
+        assert ms == 2.25
+        assert value == pytest.approx(world * 131072 / 2.25e-3)
+
+
+def test_single_process_keeps_its_own_time():
+    assert bench.max_over_ranks(3.0, torch.device("cpu")) == 3.0
+    assert bench.job_value(1, 1000, 2.0) == pytest.approx(5e5)
