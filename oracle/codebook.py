@@ -12,6 +12,12 @@ levels alternates two conditions until neither moves (Lloyd 1957/1982,
 Max 1960):
   * each decision boundary is the midpoint of its two neighbouring centroids;
   * each centroid is the conditional mean of t over its cell.
+
+[Roadmap] §4.3 describes a second, "uniform" dequantisation mode (SGLang's
+tq4u): the centroids lie on a linear grid, so a code dequantises as
+idx * step + c0 with no table.  The pages do not say how the grid is chosen;
+the reading taken here is the distortion-optimal symmetric uniform quantiser
+for the same density (Max 1960, Table II gives it for a Gaussian source).
 """
 
 import numpy as np
@@ -110,3 +116,58 @@ def per_vector_mse(d, centroids):
     edges = np.concatenate([[-1.0], b, [1.0]])
     p = dist.mass(edges[:-1], edges[1:])
     return 1.0 - d * np.sum(p * centroids**2)
+
+
+def uniform_quantiser(dist, levels, tol=1e-14, max_iter=10000):
+    """Distortion-optimal symmetric uniform quantiser for a symmetric density.
+
+    Centroids c_i = step * k_i with k_i = i - (L-1)/2 (so c0 = -step*(L-1)/2),
+    decision boundaries at the midpoints.  Two conditions alternate, as in the
+    Lloyd iteration but with one free parameter:
+      * for a fixed step the nearest-neighbour cells (midpoints) are best;
+      * for fixed cells the distortion sum_i int_cell (t - step k_i)^2 f is a
+        quadratic in step, least at step = sum_i k_i M_i / sum_i k_i^2 P_i
+        (P_i the cell's mass, M_i its first moment).
+    Starts from the step whose outer centroid is the (L - 1/2)/L quantile and
+    stops when the step moves by less than ``tol`` relative.  Returns
+    (centroids ascending, boundaries, step, iterations).
+    """
+    k = np.arange(levels) - (levels - 1) / 2.0
+    step = 2.0 * dist.quantile((levels - 0.5) / levels) / (levels - 1)
+    for it in range(1, max_iter + 1):
+        c = step * k
+        edges = np.concatenate([[dist.lo], 0.5 * (c[:-1] + c[1:]), [dist.hi]])
+        p = dist.mass(edges[:-1], edges[1:])
+        m = dist.moment(edges[:-1], edges[1:])
+        new = np.sum(k * m) / np.sum(k * k * p)
+        moved = abs(new - step)
+        step = new
+        if moved < tol * step:
+            break
+    c = step * k
+    return c, 0.5 * (c[:-1] + c[1:]), step, it
+
+
+def sphere_uniform_codebook(d, bits):
+    """Uniform-grid centroids (2^bits, ascending) and boundaries for f_d."""
+    c, b, _, _ = uniform_quantiser(SphereCoordinate(d), 2**bits)
+    return c, b
+
+
+def sphere_codebook_of_kind(d, bits, kind):
+    """kind "lloyd" (Lloyd-Max, [Hub] step 2) or "uniform" ([Roadmap] §4.3)."""
+    if kind == "lloyd":
+        return sphere_codebook(d, bits)
+    if kind == "uniform":
+        return sphere_uniform_codebook(d, bits)
+    raise ValueError(f"unknown codebook kind {kind!r}")
+
+
+def nearest_neighbour_mse(dist, second_moment, centroids):
+    """E[(t - Q(t))^2] of the nearest-neighbour quantiser with these sorted
+    centroids, for any codebook (not only a Lloyd fixed point):
+    E[t^2] - sum_i (2 c_i M_i - c_i^2 P_i) over the midpoint cells."""
+    edges = np.concatenate([[dist.lo], 0.5 * (centroids[:-1] + centroids[1:]), [dist.hi]])
+    p = dist.mass(edges[:-1], edges[1:])
+    m = dist.moment(edges[:-1], edges[1:])
+    return second_moment - np.sum(2.0 * centroids * m - centroids**2 * p)

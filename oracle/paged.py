@@ -133,7 +133,10 @@ def bytes_f16(b):
 class CacheParams:
     """Everything one cache's quantisers need, generated by the oracle itself."""
 
-    def __init__(self, d, k_bits, k_qjl, v_mode, v_bits, seed_rot, seed_qjl):
+    def __init__(self, d, k_bits, k_qjl, v_mode, v_bits, seed_rot, seed_qjl, k_codebook="lloyd",
+                 v_codebook="lloyd"):
+        """k_codebook / v_codebook: "lloyd" (Lloyd-Max, [Hub] step 2) or
+        "uniform" (equally spaced centroids, [Roadmap] §4.3)."""
         from . import codebook, prng, rotation
 
         self.layout = PageLayout(d, k_bits, k_qjl, v_mode, v_bits)
@@ -141,9 +144,9 @@ class CacheParams:
         self.signs = prng.rotation_signs(d, seed_rot)
         self.R = rotation.rotation_matrix(self.signs)
         self.S = prng.qjl_matrix(d, seed_qjl)
-        self.k_centroids, self.k_boundaries = codebook.sphere_codebook(d, k_bits)
+        self.k_centroids, self.k_boundaries = codebook.sphere_codebook_of_kind(d, k_bits, k_codebook)
         if v_mode == "mse":
-            self.v_centroids, self.v_boundaries = codebook.sphere_codebook(d, v_bits)
+            self.v_centroids, self.v_boundaries = codebook.sphere_codebook_of_kind(d, v_bits, v_codebook)
         else:
             self.v_centroids = self.v_boundaries = None
 

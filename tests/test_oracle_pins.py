@@ -162,10 +162,80 @@ def test_mse_cosine_consistent_with_hub_quality_table():
     assert abs(np.sqrt(1 - D2) - table["value2"]) < 0.005
 
 
+def test_gaussian_uniform_quantiser_matches_max_1960():
+    for row in _rows("max1960_gaussian_uniform.txt"):
+        L, step, mse = int(row[0]), float(row[1]), float(row[2])
+        c, b, got_step, _ = codebook.uniform_quantiser(codebook.StandardNormal(), L)
+        assert abs(got_step - step) < 6e-4
+        assert np.allclose(np.diff(c), got_step, rtol=1e-12) and abs(c[0] + c[-1]) < 1e-12
+        got = codebook.nearest_neighbour_mse(codebook.StandardNormal(), 1.0, c)
+        assert abs(got - mse) / mse < 1e-3
+
+
+@pytest.mark.parametrize("d", [16, 128, 256])
+def test_one_bit_uniform_is_the_lloyd_quantiser(d):
+    # two levels are always equally spaced: the uniform quantiser is then the
+    # Lloyd-Max one, +-E|t| in closed form
+    c, b = codebook.sphere_uniform_codebook(d, 1)
+    expect = np.exp(special.gammaln(d / 2) - special.gammaln((d + 1) / 2)) / np.sqrt(np.pi)
+    assert abs(c[1] - expect) < 1e-13 and abs(c[0] + expect) < 1e-13 and b[0] == 0.0
+
+
+def _distortion_by_quadrature(dist, c):
+    """int (t - Q(t))^2 f over [-1, 1], cell by cell with Gauss-Legendre
+    (independent of the closed-form masses and moments)."""
+    x, w = _LEGGAUSS_400
+    edges = np.concatenate([[-1.0], 0.5 * (c[:-1] + c[1:]), [1.0]])
+    lo, hi = edges[:-1, None], edges[1:, None]
+    t = 0.5 * (hi - lo) * x + 0.5 * (hi + lo)
+    return float(np.sum(0.5 * (hi - lo)[:, 0] * np.sum(w * (t - c[:, None]) ** 2 * dist.density(t), axis=1)))
+
+
+_LEGGAUSS_400 = np.polynomial.legendre.leggauss(400)
+
+
+@pytest.mark.parametrize("d,bits", [(128, 2), (128, 3), (128, 4), (256, 4)])
+def test_uniform_step_is_the_brute_force_minimum(d, bits):
+    dist = codebook.SphereCoordinate(d)
+    c, b, step, _ = codebook.uniform_quantiser(dist, 2**bits)
+    k = np.arange(2**bits) - (2**bits - 1) / 2.0
+    best = _distortion_by_quadrature(dist, c)
+    # the generic distortion formula agrees with direct integration
+    assert abs(codebook.nearest_neighbour_mse(dist, 1.0 / d, c) - best) < 1e-12
+    # a grid search over steps finds nothing lower, and its minimum sits next to step
+    grid = step * np.linspace(0.5, 1.5, 201)
+    vals = np.array([_distortion_by_quadrature(dist, s * k) for s in grid])
+    assert vals.min() >= best - 1e-15
+    assert abs(grid[np.argmin(vals)] - step) <= step * 0.005 + 1e-15
+    # and it is a strict local minimum
+    for f in (1 - 1e-3, 1 + 1e-3):
+        assert _distortion_by_quadrature(dist, f * step * k) > best
+
+
+def test_uniform_sphere_quantiser_tends_to_gaussian_table():
+    rows = {int(r[0]): float(r[1]) for r in _rows("max1960_gaussian_uniform.txt")}
+    for bits in (2, 3, 4):
+        _, _, step, _ = codebook.uniform_quantiser(codebook.SphereCoordinate(8192), 2**bits)
+        assert abs(np.sqrt(8192) * step - rows[2**bits]) < 2e-3
+
+
+def test_uniform_costs_little_distortion_at_four_bits():
+    # [Roadmap] §4.3: at 4 bits the uniform grid costs almost nothing in
+    # accuracy against the Lloyd codebook; in distortion it is above Lloyd-Max
+    # (which is optimal among all 16-level quantisers) but close to it
+    d = 128
+    dist = codebook.SphereCoordinate(d)
+    lloyd = codebook.per_vector_mse(d, codebook.sphere_codebook(d, 4)[0])
+    unif = d * codebook.nearest_neighbour_mse(dist, 1.0 / d, codebook.sphere_uniform_codebook(d, 4)[0])
+    assert lloyd < unif < 1.3 * lloyd
+    assert np.sqrt(1 - unif) > 0.99
+
+
 def test_nearest_centroid_is_brute_force_argmin():
     rng = np.random.default_rng(5)
-    for d, bits in [(4, 2), (8, 3), (16, 4), (128, 3)]:
-        c, b = codebook.sphere_codebook(d, bits)
+    for d, bits, kind in [(4, 2, "lloyd"), (8, 3, "lloyd"), (16, 4, "lloyd"), (128, 3, "lloyd"), (8, 3, "uniform"),
+                          (128, 4, "uniform")]:
+        c, b = codebook.sphere_codebook_of_kind(d, bits, kind)
         y = rng.uniform(-1.2 * c[-1], 1.2 * c[-1], size=(200, d))
         idx = quant.nearest_centroid(y, b)
         brute = np.argmin(np.abs(y[..., None] - c), axis=-1)
