@@ -45,6 +45,9 @@ def _args():
     p.add_argument("--split-blocks", type=int, default=0, help="KV blocks per decode split (0: per workload)")
     p.add_argument("--no-qjl", action="store_true",
                    help="ablation: MSE-only keys (no QJL sign plane or residual norm) on the same workload")
+    p.add_argument("--k-bits", type=int, default=0, help="key code bits (0: the workload's)")
+    p.add_argument("--codebook", choices=["lloyd", "uniform"], default="lloyd",
+                   help="codebook of the keys (and of MSE values): Lloyd-Max or the uniform grid")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-store-workload", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -175,7 +178,7 @@ from oracle import paged
 from turboquant_bit_kv_tq_gb300 import workloads as wl
 w = wl.config({name!r})
 cap = {cap}
-P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl)
+P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
 n = min(w.compressed_lens()[0], cap)
 nb = (n + 15) // 16
 cache = np.zeros((nb, w.kv_heads, P.layout.page_bytes), np.uint8)
@@ -403,6 +406,10 @@ def run_ours(args):
     w = wl.config(args.workload)
     if args.no_qjl:
         w = wl.scaled(w, k_qjl=False)
+    if args.k_bits:
+        w = wl.scaled(w, k_bits=args.k_bits)
+    if args.codebook != "lloyd":
+        w = wl.scaled(w, k_codebook=args.codebook, v_codebook=args.codebook if w.v_mode == "mse" else "lloyd")
     # blocks per decode split: longer splits for long contexts; a short one
     # (a few work items in all) needs short splits to spread over the SMs
     longest = max(w.seq_lens)
@@ -454,7 +461,7 @@ def run_ours(args):
     # the warp-specialized split kernel serves every configuration whose score
     # planes fit its tensor-memory plan (d=128 with 2- or 3-bit keys, d=256
     # with 2-bit keys); the one-warpgroup kernel the rest
-    ws_path = (w.d == 128 and w.k_bits <= 3) or (w.d == 256 and w.k_bits == 2)
+    ws_path = (w.d == 128 and (w.k_bits <= 3 or w.k_codebook == "uniform")) or (w.d == 256 and w.k_bits == 2)
     split_kernel_name = "tq::split_ws_kernel" if ws_path else "tq::split_kernel"
     e2e_ms, h2d, d2h = _e2e(torch, c, st, w, stream, args.steps, max(3, args.warmup), flush)
     e2e_ms_max = max_over_ranks(e2e_ms, device)
@@ -479,6 +486,7 @@ def run_ours(args):
             "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
                        "head_dim": w.d, "context_lens": sorted(set(w.seq_lens)), "tail": w.tail,
                        "k_bits": w.k_bits, "k_qjl": w.k_qjl, "v_mode": w.v_mode, "v_bits": w.v_bits,
+                       "k_codebook": w.k_codebook, "v_codebook": w.v_codebook,
                        "split_blocks": split_blocks, "out_dtype": "bf16",
                        "l2": "flushed: 256 MiB buffer written between timed steps (outside the events)",
                        "clocks": "sampled every 50 ms over the timed steps plus untimed steps of the same "

@@ -87,6 +87,15 @@ enum { TQ_DTYPE_F32 = 0, TQ_DTYPE_BF16 = 1 };
  */
 enum { TQ_OUT_ROTATED = 0x100 };
 enum { TQ_V_MSE = 0, TQ_V_G32 = 1 };
+/*
+ * Codebook of the rotated-coordinate quantiser (keys, and MSE values).
+ * TQ_CODEBOOK_LLOYD: Lloyd-Max for the Beta-distributed coordinate ([Hub]
+ * "Technical principle" step 2).  TQ_CODEBOOK_UNIFORM: equally spaced
+ * centroids, a code dequantising as idx * step + c0 ([Roadmap] §4.3, SGLang's
+ * "tq4u" mode), with the step that minimises the same distortion
+ * (tq_make_uniform_codebook).  The cache layout is the same for both.
+ */
+enum { TQ_CODEBOOK_LLOYD = 0, TQ_CODEBOOK_UNIFORM = 1 };
 
 /* Device error bits (tq_get_device_error). */
 enum {
@@ -114,6 +123,8 @@ typedef struct tq_cache_config {
     int32_t max_blocks_per_seq; /* columns of the block table */
     int32_t split_blocks;       /* cache blocks per decode split (fixed split-KV grid); >= 1 */
     int32_t tail_cap;           /* max exact bf16 "newest tokens" per sequence (0 = none) */
+    int32_t k_codebook;         /* TQ_CODEBOOK_LLOYD (0) or TQ_CODEBOOK_UNIFORM */
+    int32_t v_codebook;         /* the same for TQ_V_MSE values; must be 0 with TQ_V_G32 */
 } tq_cache_config;
 
 typedef struct tq_cache tq_cache;
@@ -140,6 +151,19 @@ const char* tq_last_cuda_error(void);
  * d >= 3, 1 <= bits <= 8.  Buffers are caller-owned host memory.
  */
 tq_status tq_make_codebook(int d, int bits, double* centroids, double* boundaries, double* mse);
+
+/*
+ * Uniform codebook for the same coordinate ([Roadmap] §4.3 "uniform" mode):
+ * centroids c_i = step * (i - (2^bits - 1)/2), boundaries at the midpoints,
+ * and the step that minimises the per-vector distortion.  For a fixed step
+ * the nearest-neighbour cells are optimal; for fixed cells the distortion is
+ * a quadratic in the step; the two alternate to the fixed point.
+ *   centroids  [2^bits]   ascending, symmetric
+ *   boundaries [2^bits-1]
+ *   mse        per-unit-vector distortion d * E[(t - Q(t))^2] (nullable)
+ * d >= 3, 1 <= bits <= 8.  Buffers are caller-owned host memory.
+ */
+tq_status tq_make_uniform_codebook(int d, int bits, double* centroids, double* boundaries, double* mse);
 
 /*
  * The seeded parameters of a cache, host only (the library's own generator:

@@ -53,6 +53,41 @@ def test_codebook_matches_oracle(d, bits):
     assert abs(mse - codebook.per_vector_mse(d, oc)) < 1e-10
 
 
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_uniform_codebook_matches_oracle(d, bits):
+    c, b, mse = tq.tq_make_uniform_codebook(d, bits)
+    oc, ob = codebook.sphere_uniform_codebook(d, bits)
+    assert np.max(np.abs(c - oc)) < 1e-11
+    assert np.max(np.abs(b - ob)) < 1e-11
+    assert np.array_equal(c.astype(np.float32), oc.astype(np.float32))
+    assert np.array_equal(b.astype(np.float32), ob.astype(np.float32))
+    step = c[1] - c[0]
+    assert np.allclose(np.diff(c), step, rtol=1e-12, atol=0)
+    assert abs(mse - d * codebook.nearest_neighbour_mse(codebook.SphereCoordinate(d), 1.0 / d, oc)) < 1e-10
+
+
+def test_uniform_codebook_high_bits_is_stationary():
+    # 8 bits: the step the library finds makes the distortion stationary
+    # (sum k M = step sum k^2 P over the midpoint cells), checked with the
+    # oracle's density functions
+    d, L = 128, 256
+    c, b, _ = tq.tq_make_uniform_codebook(d, 8)
+    dist = codebook.SphereCoordinate(d)
+    k = np.arange(L) - (L - 1) / 2.0
+    step = (c[-1] - c[0]) / (L - 1)
+    edges = np.concatenate([[-1.0], b, [1.0]])
+    g = np.sum(k * dist.moment(edges[:-1], edges[1:])) - step * np.sum(k * k * dist.mass(edges[:-1], edges[1:]))
+    assert abs(g) < 1e-9 * step * np.sum(k * k * dist.mass(edges[:-1], edges[1:]))
+
+
+def test_page_bytes_do_not_depend_on_the_codebook():
+    base = dict(head_dim=128, num_kv_heads=1, num_q_heads=1, num_blocks=2, k_bits=4, v_mode=0, v_bits=3,
+                max_blocks_per_seq=2)
+    uni = tq.tq_cache_sizes(tq.tq_cache_config(**base, k_codebook=1, v_codebook=1))
+    assert uni == tq.tq_cache_sizes(tq.tq_cache_config(**base))
+
+
 @pytest.mark.parametrize("d,seed", [(128, 2), (256, 2), (128, 12345)])
 def test_rotation_signs_match_oracle(d, seed):
     assert np.array_equal(tq.tq_make_rotation_signs(d, seed), prng.rotation_signs(d, seed).astype(np.float32))
@@ -84,7 +119,8 @@ def test_bad_configs_are_rejected_on_the_host():
     for bad, status in [(dict(head_dim=64), -2), (dict(k_bits=5), -2), (dict(v_bits=1), -2), (dict(block_size=32), -2),
                         (dict(num_q_heads=30), -1), (dict(num_blocks=0), -1), (dict(v_mode=7), -2),
                         (dict(split_blocks=0), -1), (dict(tail_cap=-1), -1), (dict(v_mode=1, v_bits=3), -2),
-                        (dict(num_q_heads=48), -2)]:
+                        (dict(num_q_heads=48), -2), (dict(k_codebook=2), -1), (dict(v_codebook=-1), -1),
+                        (dict(v_codebook=1), -1)]:
         with pytest.raises(tq.TQError) as e:
             tq.tq_cache_sizes(tq.tq_cache_config(**{**ok, **bad}))
         assert e.value.status == status, bad

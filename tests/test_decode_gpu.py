@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _params(w):
-    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl)
+    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
 
 
 def _dev(x, dtype):
@@ -117,6 +117,18 @@ CASES = [
     # MSE-only keys (no QJL plane): the ablation of the residual correction
     ("no_qjl_g32", "llama8b_gqa4_b16_8k", dict(k_qjl=False), [300, 129, 17], None, 0, 4),
     ("no_qjl_d256_mse", "d256_gqa8_b8_32k", dict(k_qjl=False), [200, 33], None, 0, 4),
+    # uniform codebooks (single-bit score planes only on the warp-specialized
+    # kernel at d=128; every plane elsewhere)
+    ("uniform_k3_g32", "llama8b_gqa4_b16_8k", dict(k_codebook="uniform"), [300, 129, 17], None, 0, 4),
+    ("uniform_k4_v4mse", "llama8b_gqa4_b16_8k",
+     dict(k_bits=4, k_codebook="uniform", v_mode="mse", v_bits=4, v_codebook="uniform"), [300, 33, 0, 1], None, 0, 4),
+    ("uniform_k4_no_qjl", "llama8b_gqa4_b16_8k", dict(k_bits=4, k_codebook="uniform", k_qjl=False), [257, 64], None,
+     0, 2),
+    ("uniform_k4_hybrid", "llama70b_gqa8_b4_ragged131k_hybrid", dict(k_bits=4, k_codebook="uniform"), [15, 500],
+     [5, 128], 128, 4),
+    ("uniform_d256_k3", "d256_gqa8_b8_32k", dict(k_bits=3, k_codebook="uniform", v_codebook="uniform"), [200, 33],
+     None, 0, 4),
+    ("uniform_k2_f32", "single_head_d128_1k", dict(k_codebook="uniform", v_codebook="uniform"), [1024], None, 0, 8),
 ]
 
 
@@ -260,12 +272,12 @@ def test_decode_cuda_graph_replay_with_new_lengths():
         _assert_close(out.cpu().numpy(), ref)
 
 
-def _sampled_full_size(name, picks, split_blocks):
+def _sampled_full_size(name, picks, split_blocks, changes=None):
     """Full-size workload in the benchmark's launch configuration: every
     sequence's cache is filled by the GPU store (not compared), then the pages
     of the sampled (sequence, KV head) pairs are overwritten with the oracle's
     encoding and those query-head outputs are compared."""
-    w = wl.config(name)
+    w = wl.scaled(wl.config(name), **(changes or {}))
     P = _params(w)
     table, num_blocks = wl.block_table(w)
     comp = w.compressed_lens()
@@ -328,6 +340,11 @@ def test_decode_full_size_llama8b_sampled():
 
 def test_decode_full_size_d256_sampled():
     _sampled_full_size("d256_gqa8_b8_32k", [(3, 1), (7, 3)], split_blocks=64)
+
+
+def test_decode_full_size_llama8b_uniform_k4_sampled():
+    _sampled_full_size("llama8b_gqa4_b16_8k", [(2, 1), (12, 6)], split_blocks=32,
+                       changes=dict(k_bits=4, k_codebook="uniform"))
 
 
 def test_decode_full_size_hybrid131k_sampled():

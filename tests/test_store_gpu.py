@@ -18,7 +18,7 @@ def _cache_for(w, num_blocks):
 
 
 def _oracle_params(w):
-    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl)
+    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
 
 
 def _to_dev(x, dtype):
@@ -53,7 +53,7 @@ def _check(w, K, V, slots, num_blocks, expect_err=0):
 
 
 CASES = [
-    # name, d, H, k_bits, v_mode, v_bits, dtype, qjl, n_out, scale
+    # name, d, H, k_bits, v_mode, v_bits, dtype, qjl, n_out, scale[, codebook]
     ("c1_like_f32", 128, 1, 2, "mse", 2, "f32", True, 4, 20.0),
     ("c2_like", 128, 8, 3, "g32", 4, "bf16", True, 3, 10.0),
     ("c3_like_d256", 256, 4, 2, "mse", 2, "bf16", True, 5, 15.0),
@@ -61,6 +61,8 @@ CASES = [
     ("d256_f32_k3_g32v2", 256, 2, 3, "g32", 2, "f32", True, 5, 15.0),
     ("no_qjl_v4mse", 128, 2, 3, "mse", 4, "bf16", False, 3, 10.0),
     ("k4_v3mse_d256", 256, 1, 4, "mse", 3, "bf16", True, 5, 15.0),
+    ("uniform_k4_v4mse", 128, 2, 4, "mse", 4, "bf16", True, 3, 10.0, "uniform"),
+    ("uniform_k3_v2mse_d256", 256, 1, 3, "mse", 2, "f32", True, 5, 15.0, "uniform"),
 ]
 
 
@@ -75,8 +77,10 @@ def store_path(request):
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_store_parity_small(case, store_path):
-    name, d, H, kb, vm, vb, dt, qjl, n_out, sc = case
-    w = wl.Workload(name, d, H, H, kb, vm, vb, dt, n_out, sc, seed=11, k_qjl=qjl, batch=1, seq_lens=[300])
+    name, d, H, kb, vm, vb, dt, qjl, n_out, sc = case[:10]
+    cb = case[10] if len(case) > 10 else "lloyd"
+    w = wl.Workload(name, d, H, H, kb, vm, vb, dt, n_out, sc, seed=11, k_qjl=qjl, batch=1, seq_lens=[300],
+                    k_codebook=cb, v_codebook=cb if vm == "mse" else "lloyd")
     T = 300
     K, V = wl.kv_tokens(w, 0, 0, T)
     num_blocks = 24  # 384 slots, 300 used + ragged

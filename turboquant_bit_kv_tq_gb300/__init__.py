@@ -15,6 +15,7 @@ import numpy as np
 
 __all__ = [
     "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_OUT_ROTATED", "TQ_V_MSE", "TQ_V_G32",
+    "TQ_CODEBOOK_LLOYD", "TQ_CODEBOOK_UNIFORM", "tq_make_uniform_codebook",
     "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
     "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
@@ -26,6 +27,7 @@ __all__ = [
 TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
 TQ_OUT_ROTATED = 0x100
 TQ_V_MSE, TQ_V_G32 = 0, 1
+TQ_CODEBOOK_LLOYD, TQ_CODEBOOK_UNIFORM = 0, 1
 TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 
 # every function include/tq_kv.h declares
@@ -33,7 +35,7 @@ EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
     "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
-    "tq_set_store_small_max",
+    "tq_set_store_small_max", "tq_make_uniform_codebook",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -64,6 +66,8 @@ class tq_cache_config(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int32),
         ("split_blocks", ctypes.c_int32),
         ("tail_cap", ctypes.c_int32),
+        ("k_codebook", ctypes.c_int32),
+        ("v_codebook", ctypes.c_int32),
     ]
 
     def __init__(self, **kw):
@@ -96,6 +100,7 @@ def load_library():
             "tq_status_string": (ctypes.c_char_p, [i32]),
             "tq_last_cuda_error": (ctypes.c_char_p, []),
             "tq_make_codebook": (i32, [i32, i32, dp, dp, dp]),
+            "tq_make_uniform_codebook": (i32, [i32, i32, dp, dp, dp]),
             "tq_make_rotation_signs": (i32, [i32, u64, ctypes.POINTER(ctypes.c_float)]),
             "tq_make_qjl_matrix": (i32, [i32, u64, ctypes.POINTER(ctypes.c_uint16)]),
             "tq_cache_sizes": (i32, [cfgp, sz, sz, sz, sz]),
@@ -147,6 +152,16 @@ def tq_make_codebook(d, bits):
     b = np.zeros(2**bits - 1)
     mse = ctypes.c_double()
     _check(load_library().tq_make_codebook(d, bits, _dptr(c), _dptr(b), ctypes.byref(mse)), "tq_make_codebook")
+    return c, b, mse.value
+
+
+def tq_make_uniform_codebook(d, bits):
+    """Uniform-grid (centroids, boundaries, per-vector mse) as float64."""
+    c = np.zeros(2**bits)
+    b = np.zeros(2**bits - 1)
+    mse = ctypes.c_double()
+    _check(load_library().tq_make_uniform_codebook(d, bits, _dptr(c), _dptr(b), ctypes.byref(mse)),
+           "tq_make_uniform_codebook")
     return c, b, mse.value
 
 

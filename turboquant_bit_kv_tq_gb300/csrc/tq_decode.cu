@@ -22,7 +22,16 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     if (prep_smem > kPrepMax) return TQ_ERR_UNSUPPORTED;
     size_t smem = 0;
     int grid = 0;
-    if (ws_fits(a.gm, D)) {
+    // a uniform key codebook expands over its k_bits single-bit planes only
+    // (every multi-bit Walsh term is zero), so its score contraction is
+    // shorter; the warp-specialized kernel has instances for that at d = 128
+    DecodeGeom gw = a.gm;
+    if (D == 128 && a.k_uniform && gw.npk > a.lay.k_bits) {
+        gw.npk = a.lay.k_bits;
+        gw.npl = gw.npk + (a.lay.k_qjl ? 1 : 0);
+        gw.bimg_bytes = gw.n_cols * gw.npl * D;
+    }
+    if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel
         static int sms = 0;
@@ -38,13 +47,14 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         const int nsets = a.lay.v_mode == TQ_V_G32 ? D / 32 : (1 << (a.lay.v_bits - 1));
         a.stages = 0;
         for (int st = kWsMaxStages; st >= 2 && a.stages == 0; --st) {
-            const WsLayout wl = ws_layout<D>(a.lay.page_bytes, a.gm, nsets, st, kitems, a.split_blocks);
+            const WsLayout wl = ws_layout<D>(a.lay.page_bytes, gw, nsets, st, kitems, a.split_blocks);
             if (wl.total <= 112 * 1024) {
                 a.stages = st;
                 smem = std::max(wl.total, (size_t)77 * 1024);  // never a third CTA per SM (tensor memory)
             }
         }
         if (a.stages == 0) grid = 0;  // too many items per CTA for the staged schedule
+        if (grid > 0) a.gm = gw;      // (the other kernels keep every plane)
     }
     if (grid == 0) {
         const tq_status cfg = split_config<D>(a, &a.stages, &smem);
@@ -112,6 +122,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     a.out = out;
     a.out_dtype = out_dtype;
     a.out_rotated = out_rot;
+    a.k_uniform = c->cfg.k_codebook == TQ_CODEBOOK_UNIFORM;
     const int d = c->cfg.head_dim;
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
     a.scale_log2e = sc * 1.4426950408889634f;

@@ -60,6 +60,7 @@ struct DecodeArgs {
     void* out;
     int out_dtype;
     bool out_rotated;  // MSE values: leave the output in the rotated space (no R^T)
+    bool k_uniform;    // the key codebook is a uniform grid
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;

@@ -71,6 +71,7 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache* c, const void* 
     a.out = out;
     a.out_dtype = out_dtype;
     a.out_rotated = out_rot;
+    a.k_uniform = c->cfg.k_codebook == TQ_CODEBOOK_UNIFORM;
     const int d = c->cfg.head_dim;
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
     a.scale_log2e = sc * 1.4426950408889634f;

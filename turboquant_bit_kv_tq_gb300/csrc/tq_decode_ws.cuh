@@ -283,10 +283,12 @@ __device__ __forceinline__ void ws_issue_planes(int P0, int P1, uint32_t tmem, u
     }
 }
 
-template <int D, int KB, bool G32, int VB, int NTH>
+// KU: the key codebook is a uniform grid, whose expansion over XOR bit-planes
+// has only the KB single-bit terms (plane_subset lists those first)
+template <int D, int KB, bool KU, bool G32, int VB, int NTH>
 __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(DecodeArgs a) {
     static_assert(kWsRegsCons <= 256 && kWsRegsCons % 8 == 0, "register split");
-    constexpr int NPK = 1 << (KB - 1);
+    constexpr int NPK = KU ? KB : 1 << (KB - 1);
     constexpr int NW = D / 32;
     constexpr int NCOL = D / 4;
     constexpr int NMT = D / 16;
@@ -938,9 +940,9 @@ __global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
     tail_split<D>(a, g, b, smem);
 }
 
-template <int D, int KB, bool G32, int VB, int NTH>
+template <int D, int KB, bool KU, bool G32, int VB, int NTH>
 inline tq_status launch_split_ws(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid) {
-    auto kern = split_ws_kernel<D, KB, G32, VB, NTH>;
+    auto kern = split_ws_kernel<D, KB, KU, G32, VB, NTH>;
     static bool attr_set = false;  // once per kernel instance, before any capture
     if (!attr_set) {
         {
@@ -960,16 +962,22 @@ inline tq_status launch_split_ws(const DecodeArgs& a, cudaStream_t s, size_t sme
     return TQ_OK;
 }
 
-template <int D, int KB, int NTH>
+template <int D, int KB, bool KU, int NTH>
 inline tq_status dispatch_ws_v(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid) {
+    if (a.gm.nth != NTH || a.gm.npk != (KU ? KB : 1 << (KB - 1))) return TQ_ERR_UNSUPPORTED;
     if (a.lay.v_mode == TQ_V_G32)
-        return a.lay.v_bits == 4 ? launch_split_ws<D, KB, true, 4, NTH>(a, s, smem, grid)
-                                 : launch_split_ws<D, KB, true, 2, NTH>(a, s, smem, grid);
+        return a.lay.v_bits == 4 ? launch_split_ws<D, KB, KU, true, 4, NTH>(a, s, smem, grid)
+                                 : launch_split_ws<D, KB, KU, true, 2, NTH>(a, s, smem, grid);
     switch (a.lay.v_bits) {
-        case 2: return launch_split_ws<D, KB, false, 2, NTH>(a, s, smem, grid);
-        case 3: return launch_split_ws<D, KB, false, 3, NTH>(a, s, smem, grid);
-        default: return launch_split_ws<D, KB, false, 4, NTH>(a, s, smem, grid);
+        case 2: return launch_split_ws<D, KB, KU, false, 2, NTH>(a, s, smem, grid);
+        case 3: return launch_split_ws<D, KB, KU, false, 3, NTH>(a, s, smem, grid);
+        default: return launch_split_ws<D, KB, KU, false, 4, NTH>(a, s, smem, grid);
     }
 }
+
+// the uniform-key (KU) instances of the warp-specialized kernel, compiled in
+// their own translation units
+template <int D, int KB>
+tq_status dispatch_ws_uniform(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid);
 
 }  // namespace tq

@@ -24,6 +24,9 @@ tq_status compute_layout(const tq_cache_config& c, Layout* lay) {
     // group-32 values pack 2 or 4 bits per coordinate ([Hub] step 4)
     if (c.v_mode == TQ_V_G32 && c.v_bits != 2 && c.v_bits != 4) return TQ_ERR_UNSUPPORTED;
     if (c.k_qjl != 0 && c.k_qjl != 1) return TQ_ERR_INVALID_ARG;
+    if (c.k_codebook != TQ_CODEBOOK_LLOYD && c.k_codebook != TQ_CODEBOOK_UNIFORM) return TQ_ERR_INVALID_ARG;
+    if (c.v_codebook != TQ_CODEBOOK_LLOYD && c.v_codebook != TQ_CODEBOOK_UNIFORM) return TQ_ERR_INVALID_ARG;
+    if (c.v_mode == TQ_V_G32 && c.v_codebook != TQ_CODEBOOK_LLOYD) return TQ_ERR_INVALID_ARG;
     if (c.num_kv_heads < 1 || c.num_q_heads < c.num_kv_heads || c.num_q_heads % c.num_kv_heads) return TQ_ERR_INVALID_ARG;
     {
         const int G = c.num_q_heads / c.num_kv_heads;  // grouped query heads per KV head
@@ -255,7 +258,9 @@ struct SphereDensity {
 // u_S = XOR of the bits of i in S:  c[i] = alpha + sum_S beta_S u_S(i) with
 // alpha = sum_S chat_S, beta_S = -2 chat_S.  out = {alpha, beta_S...} in the
 // order of plane_subset().
-static void walsh_planes(const std::vector<double>& c, int bits, float* out) {
+// A uniform codebook c[i] = step (i - (L-1)/2) is linear in the bits of i, so
+// every multi-bit term is zero: those are set to exactly zero (single_bits).
+static void walsh_planes(const std::vector<double>& c, int bits, float* out, bool single_bits = false) {
     const int L = 1 << bits, planes = 1 << (bits - 1);
     double alpha = 0.0;
     for (int pi = 0; pi < planes; ++pi) {
@@ -263,6 +268,7 @@ static void walsh_planes(const std::vector<double>& c, int bits, float* out) {
         double chat = 0.0;
         for (int i = 0; i < L; ++i) chat += (__builtin_popcount(i & S) & 1) ? -c[i] : c[i];
         chat /= L;
+        if (single_bits && __builtin_popcount(S) > 1) chat = 0.0;
         alpha += chat;
         out[1 + pi] = (float)(-2.0 * chat);
     }
@@ -347,6 +353,71 @@ const char* tq_status_string(tq_status s) {
     }
 }
 
+// Distortion-optimal uniform grid c[i] = step k_i, k_i = i - (L-1)/2, with
+// midpoint boundaries.  The distortion's derivative in the step is
+// -2 g(step), g = sum_i k_i M_i - step sum_i k_i^2 P_i over the midpoint cells
+// (M, P: first moment and mass of a cell; the boundary terms cancel because
+// the integrand is continuous at a midpoint).  g > 0 for a tiny step and
+// g < 0 once the outer centroids pass +-1; the optimum is its root, found by
+// bisection to machine precision.
+static void uniform_sphere(int d, int bits, std::vector<double>& c, std::vector<double>& b, double* mse) {
+    const int L = 1 << bits;
+    const SphereDensity dens(d);
+    std::vector<double> k(L), edges(L + 1), P(L), M(L);
+    for (int i = 0; i < L; ++i) k[i] = i - 0.5 * (L - 1);
+    auto cells = [&](double st) {
+        edges[0] = -1.0;
+        edges[L] = 1.0;
+        for (int i = 0; i + 1 < L; ++i) edges[i + 1] = std::max(-1.0, std::min(1.0, st * (k[i] + 0.5)));
+        for (int i = 0; i < L; ++i) {
+            P[i] = dens.mass(edges[i], edges[i + 1]);
+            M[i] = dens.moment(edges[i], edges[i + 1]);
+        }
+    };
+    auto g = [&](double st) {
+        cells(st);
+        double num = 0.0, den = 0.0;
+        for (int i = 0; i < L; ++i) {
+            num += k[i] * M[i];
+            den += k[i] * k[i] * P[i];
+        }
+        return num - st * den;
+    };
+    double lo = 1e-6 / sqrt((double)d), hi = 2.0 / (L - 1);
+    for (int it = 0; it < 200 && hi - lo > 1e-16 * hi; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        (g(mid) > 0.0 ? lo : hi) = mid;
+    }
+    const double step = 0.5 * (lo + hi);
+    c.resize(L);
+    b.resize(L - 1);
+    for (int i = 0; i < L; ++i) c[i] = step * k[i];
+    for (int i = 0; i + 1 < L; ++i) b[i] = 0.5 * (c[i] + c[i + 1]);
+    if (mse) {
+        // d E[(t - Q t)^2] = 1 - d sum_i (2 c_i M_i - c_i^2 P_i), E[t^2] = 1/d
+        cells(step);
+        double s = 0.0;
+        for (int i = 0; i < L; ++i) s += 2.0 * c[i] * M[i] - c[i] * c[i] * P[i];
+        *mse = 1.0 - d * s;
+    }
+}
+
+static void make_codebook(int kind, int d, int bits, std::vector<double>& c, std::vector<double>& b) {
+    if (kind == TQ_CODEBOOK_UNIFORM)
+        uniform_sphere(d, bits, c, b, nullptr);
+    else
+        lloyd_max_sphere(d, bits, c, b, nullptr);
+}
+
+tq_status tq_make_uniform_codebook(int d, int bits, double* centroids, double* boundaries, double* mse) {
+    if (d < 3 || bits < 1 || bits > 8 || !centroids || !boundaries) return TQ_ERR_INVALID_ARG;
+    std::vector<double> c, b;
+    uniform_sphere(d, bits, c, b, mse);
+    std::copy(c.begin(), c.end(), centroids);
+    std::copy(b.begin(), b.end(), boundaries);
+    return TQ_OK;
+}
+
 tq_status tq_make_codebook(int d, int bits, double* centroids, double* boundaries, double* mse) {
     if (d < 3 || bits < 1 || bits > 8 || !centroids || !boundaries) return TQ_ERR_INVALID_ARG;
     std::vector<double> c, b;
@@ -401,8 +472,8 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     const int d = cfg->head_dim;
     make_signs(d, cfg->seed_rot, h->signs);
     make_qjl(d, cfg->seed_qjl, h->s_bf16);
-    lloyd_max_sphere(d, cfg->k_bits, h->k_cent, h->k_bound, nullptr);
-    if (cfg->v_mode == TQ_V_MSE) lloyd_max_sphere(d, cfg->v_bits, h->v_cent, h->v_bound, nullptr);
+    make_codebook(cfg->k_codebook, d, cfg->k_bits, h->k_cent, h->k_bound);
+    if (cfg->v_mode == TQ_V_MSE) make_codebook(cfg->v_codebook, d, cfg->v_bits, h->v_cent, h->v_bound);
 
     // stage the device tables on the host, then one copy
     const ParamsLayout pl = params_layout(*cfg);
@@ -430,8 +501,9 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     put(pl.k_bound, h->k_bound);
     put(pl.v_cent, h->v_cent);
     put(pl.v_bound, h->v_bound);
-    walsh_planes(h->k_cent, cfg->k_bits, (float*)(img.data() + pl.k_walsh));
-    if (cfg->v_mode == TQ_V_MSE) walsh_planes(h->v_cent, cfg->v_bits, (float*)(img.data() + pl.v_walsh));
+    walsh_planes(h->k_cent, cfg->k_bits, (float*)(img.data() + pl.k_walsh), cfg->k_codebook == TQ_CODEBOOK_UNIFORM);
+    if (cfg->v_mode == TQ_V_MSE)
+        walsh_planes(h->v_cent, cfg->v_bits, (float*)(img.data() + pl.v_walsh), cfg->v_codebook == TQ_CODEBOOK_UNIFORM);
     cudaStream_t s = (cudaStream_t)stream;
     if (cudaMemcpyAsync(params_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {

@@ -40,12 +40,13 @@ struct DeviceParams {
     uint32_t* err;           // device error word
 };
 
-// Odd-size subsets of the code bits, in increasing mask order: the planes of a
-// b-bit symmetric codebook (2^(b-1) of them).
+// Odd-size subsets of the code bits: the planes of a b-bit symmetric codebook
+// (2^(b-1) of them), the b single bits first (all a uniform codebook has), then
+// the rest in increasing mask order.
 __host__ __device__ constexpr int plane_subset(int bits, int i) {
     return bits == 2 ? (i == 0 ? 1 : 2)
          : bits == 3 ? (i == 0 ? 1 : i == 1 ? 2 : i == 2 ? 4 : 7)
-                     : (i == 0 ? 1 : i == 1 ? 2 : i == 2 ? 4 : i == 3 ? 7 : i == 4 ? 8 : i == 5 ? 11 : i == 6 ? 13 : 14);
+                     : (i == 0 ? 1 : i == 1 ? 2 : i == 2 ? 4 : i == 3 ? 8 : i == 4 ? 7 : i == 5 ? 11 : i == 6 ? 13 : 14);
 }
 
 // Split-KV geometry of a configuration.

@@ -39,6 +39,8 @@ class Workload:
     seed_rot: int = 2
     seed_qjl: int = 1
     k_qjl: bool = True
+    k_codebook: str = "lloyd"  # "lloyd" | "uniform"
+    v_codebook: str = "lloyd"
     # decode shape
     batch: int = 0
     seq_lens: list = field(default_factory=list)  # total tokens per sequence (compressed + tail)
@@ -219,4 +221,5 @@ def cache_config_kwargs(w, num_blocks, max_blocks, max_batch=None, split_blocks=
     return dict(head_dim=w.d, num_kv_heads=w.kv_heads, num_q_heads=w.q_heads, num_blocks=num_blocks,
                 k_bits=w.k_bits, k_qjl=int(w.k_qjl), v_mode=0 if w.v_mode == "mse" else 1, v_bits=w.v_bits,
                 seed_rot=w.seed_rot, seed_qjl=w.seed_qjl, max_batch=max_batch or max(1, w.batch),
-                max_blocks_per_seq=max_blocks, split_blocks=split_blocks, tail_cap=w.tail)
+                max_blocks_per_seq=max_blocks, split_blocks=split_blocks, tail_cap=w.tail,
+                k_codebook=0 if w.k_codebook == "lloyd" else 1, v_codebook=0 if w.v_codebook == "lloyd" else 1)
