@@ -296,3 +296,32 @@ def decode_attention(cache, P, Q, block_table, seq_lens, scale=None, tail_k=None
                 p /= p.sum()
                 out[b, h] = p @ values
     return out
+
+
+def extend_attention(cache, P, Q, block_table, prefix_lens, cu_q, chunk_k, chunk_v, scale=None):
+    """Extend (prefill) attention over the compressed paged cache ([Roadmap]
+    §4.1: SGLang's fused extend kernel reads the compressed pool like the
+    decode kernel does).
+
+    Sequence b brings n_b = cu_q[b+1] - cu_q[b] new tokens, rows
+    cu_q[b] .. cu_q[b+1]-1 of Q [T, H_q, d] and of the exact new keys and
+    values chunk_k / chunk_v [T, H_kv, d].  Its first prefix_lens[b] tokens
+    are already in the cache (block table row b).  New token j (0-based within
+    its chunk) attends to every prefix token through the compressed scores and
+    values, and to new tokens 0..j exactly (causal):
+
+      out[cu_q[b] + j] = decode attention of that query over the prefix, with
+                         the new tokens 0..j as exact tail tokens.
+
+    Returns fp64 [T, H_q, d]."""
+    T, Hq, d = Q.shape
+    out = np.zeros((T, Hq, d))
+    for b in range(len(prefix_lens)):
+        lo, hi = int(cu_q[b]), int(cu_q[b + 1])
+        for j in range(hi - lo):
+            t = lo + j
+            tk = np.asarray(chunk_k[lo:t + 1], np.float64).transpose(1, 0, 2)[None]
+            tv = np.asarray(chunk_v[lo:t + 1], np.float64).transpose(1, 0, 2)[None]
+            out[t] = decode_attention(cache, P, Q[t:t + 1], block_table[b:b + 1], [prefix_lens[b]], scale=scale,
+                                      tail_k=tk, tail_v=tv, tail_lens=[j + 1])[0]
+    return out

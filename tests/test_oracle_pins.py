@@ -515,3 +515,90 @@ def test_store_with_no_tokens_is_a_noop():
     paged.store(cache, P, empty, empty, np.zeros(0, np.int64))
     paged.store(cache, P, np.ones((3, 8, 128)), np.ones((3, 8, 128)), np.full(3, -1))
     assert not cache.any()
+
+
+# ------------------------------------------------------------------ extend
+def _extend_problem(v_mode, prefix, chunks, seed=4):
+    """Two sequences sharing nothing: sequence b has prefix[b] tokens in the
+    cache and chunks[b] new exact tokens."""
+    P = paged.CacheParams(128, 3, True, v_mode, 4, 2, 1)
+    H, Hq, d = 2, 4, 128
+    rng = np.random.default_rng(seed)
+    nblk = sum((n + 15) // 16 for n in prefix) + 2
+    cache = np.zeros((nblk, H, P.layout.page_bytes), np.uint8)
+    perm = rng.permutation(nblk)
+    width = max(1, max((n + 15) // 16 for n in prefix))
+    table = np.zeros((len(prefix), width), np.int64)
+    at = 0
+    for b, n in enumerate(prefix):
+        k = (n + 15) // 16
+        table[b, :k] = perm[at:at + k]
+        at += k
+        K = rng.standard_normal((n, H, d))
+        K[..., :3] *= 10
+        V = rng.standard_normal((n, H, d))
+        t = np.arange(n)
+        paged.store(cache, P, K, V, table[b, t // 16] * 16 + t % 16)
+    cu = np.concatenate([[0], np.cumsum(chunks)])
+    T = int(cu[-1])
+    Q = rng.standard_normal((T, Hq, d))
+    ck = rng.standard_normal((T, H, d))
+    cv = rng.standard_normal((T, H, d))
+    return P, cache, table, cu, Q, ck, cv
+
+
+def test_extend_without_prefix_is_textbook_causal_attention():
+    # Special-case reduction: no cached prefix leaves plain causal softmax
+    # attention over the new tokens, written here as one masked matrix product.
+    P, cache, table, cu, Q, ck, cv = _extend_problem("g32", [0, 0], [5, 9])
+    out = paged.extend_attention(cache, P, Q, table, [0, 0], cu, ck, cv)
+    for b in range(2):
+        lo, hi = cu[b], cu[b + 1]
+        for h in range(4):
+            g = h // 2
+            s = Q[lo:hi, h] @ ck[lo:hi, g].T / np.sqrt(128)
+            s[np.triu_indices(hi - lo, 1)] = -np.inf
+            assert np.max(np.abs(special.softmax(s, axis=1) @ cv[lo:hi, g] - out[lo:hi, h])) < 1e-12
+
+
+@pytest.mark.parametrize("v_mode", ["mse", "g32"])
+def test_extend_is_masked_attention_over_prefix_and_new_tokens(v_mode):
+    # With a prefix: one softmax over [dequantised prefix keys; exact new keys]
+    # with a causal mask on the new-token block, built as a single matrix.
+    P, cache, table, cu, Q, ck, cv = _extend_problem(v_mode, [40, 17], [6, 3])
+    prefix = [40, 17]
+    out = paged.extend_attention(cache, P, Q, table, prefix, cu, ck, cv)
+    d = 128
+    for b in range(2):
+        lo, hi = cu[b], cu[b + 1]
+        n = hi - lo
+        for g in range(2):
+            f = paged.read_tokens(cache, P, table[b], prefix[b], g)
+            k_hat = quant.mse_reconstruct(f["k_n16"], f["k_idx"], P.R, P.k_centroids)
+            k_hat += f["k_rho16"].astype(float)[:, None] * np.sqrt(np.pi / 2) / d * ((2.0 * f["k_bits"] - 1) @ P.S)
+            if v_mode == "mse":
+                v_hat = quant.mse_reconstruct(f["v_n16"], f["v_codes"], P.R, P.v_centroids)
+            else:
+                v_hat = quant.group32_reconstruct(f["v_s16"], f["v_z16"], f["v_codes"])
+            keys = np.concatenate([k_hat, ck[lo:hi, g]])
+            vals = np.concatenate([v_hat, cv[lo:hi, g]])
+            mask = np.zeros((n, prefix[b] + n), bool)
+            mask[:, prefix[b]:] = np.triu(np.ones((n, n), bool), 1)
+            for h in (2 * g, 2 * g + 1):
+                s = Q[lo:hi, h] @ keys.T / np.sqrt(d)
+                s[mask] = -np.inf
+                ref = special.softmax(s, axis=1) @ vals
+                assert np.max(np.abs(ref - out[lo:hi, h])) < 1e-10
+
+
+def test_extend_last_token_of_a_chunk_sees_every_new_token():
+    # the chunk's first token sees only itself among the new tokens: changing
+    # a later new token leaves its output unchanged, and changes the last one
+    P, cache, table, cu, Q, ck, cv = _extend_problem("g32", [20], [4])
+    a = paged.extend_attention(cache, P, Q, table, [20], cu, ck, cv)
+    ck2, cv2 = ck.copy(), cv.copy()
+    ck2[3] += 5.0
+    cv2[3] -= 3.0
+    b = paged.extend_attention(cache, P, Q, table, [20], cu, ck2, cv2)
+    assert np.array_equal(a[:3], b[:3])
+    assert np.max(np.abs(a[3] - b[3])) > 1e-3
