@@ -50,6 +50,7 @@ def _args():
                    help="codebook of the keys (and of MSE values): Lloyd-Max or the uniform grid")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-store-workload", action="store_true")
+    p.add_argument("--no-extend-workload", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -387,6 +388,49 @@ def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak):
             "launches": steps}
 
 
+def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4):
+    """Extend (prefill) attention on the 8B shape (context line): batch
+    sequences, each with `prefix` compressed tokens and `chunk` new exact
+    tokens that attend causally among themselves."""
+    import numpy as np
+
+    w = wl.scaled(wl.config("llama8b_gqa4_b16_8k"), batch=batch, seq_lens=[prefix] * batch)
+    table, num_blocks = wl.block_table(w)
+    T = batch * chunk
+    c = tq.TQCache(device=device, **{**wl.cache_config_kwargs(w, num_blocks=num_blocks, max_blocks=table.shape[1],
+                                                               max_batch=T, split_blocks=32), "tail_cap": chunk})
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    for b in range(batch):
+        t = np.arange(prefix)
+        slots = torch.from_numpy(table[b, t // 16].astype(np.int64) * 16 + t % 16).to(device)
+        K, V = wl.kv_tokens_device(w, prefix, gen, device)
+        c.store(K, V, slots)
+    new_k, new_v = wl.kv_tokens_device(w, T, gen, device)
+    q = (torch.randn((T, w.q_heads, w.d), generator=gen, device=device)).to(torch.bfloat16)
+    tab = torch.from_numpy(table).to(device)
+    pl = torch.full((batch,), prefix, dtype=torch.int32, device=device)
+    cu = torch.arange(0, T + 1, chunk, dtype=torch.int32, device=device)
+    out = torch.empty((T, w.q_heads, w.d), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        c.extend(q, tab, pl, cu, new_k, new_v, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        c.extend(q, tab, pl, cu, new_k, new_v, out=out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if c.device_error():
+        raise RuntimeError("device error during the extend workload")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    attended = T * prefix + batch * chunk * (chunk + 1) // 2
+    return {"workload": f"llama8b_gqa4 extend: {batch} seqs x {prefix}-token compressed prefix + {chunk} new tokens",
+            "new_tokens_per_s": T / (ms * 1e-3), "attended_kv_tokens_per_s": attended / (ms * 1e-3), "ms": ms,
+            "calls": steps}
+
+
 def run_ours(args):
     import torch
 
@@ -467,9 +511,11 @@ def run_ours(args):
     e2e_ms_max = max_over_ranks(e2e_ms, device)
     free_ms_max = max_over_ranks(statistics.mean(free_ms), device)
 
-    store_line = None
+    store_line = extend_line = None
     if not args.no_store_workload and rank == 0:
         store_line = _store_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush, peak)
+    if not args.no_extend_workload and rank == 0:
+        extend_line = _extend_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush)
 
     if rank == 0:
         cpu = None
@@ -509,6 +555,7 @@ def run_ours(args):
                                     "unit": UNIT, "steps": len(free_ms)},
             "gpu_launches": 4 * args.steps,
             "store_workload": store_line,
+            "extend_workload": extend_line,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

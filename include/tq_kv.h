@@ -103,7 +103,8 @@ enum {
     TQ_DEVERR_BLOCK = 1u << 1,     /* decode: block id outside [0, num_blocks); block skipped */
     TQ_DEVERR_SEQLEN = 1u << 2,    /* decode: seq_len < 0 or > 16*max_blocks_per_seq; clamped */
     TQ_DEVERR_TAIL = 1u << 3,      /* decode: tail_len < 0 or > tail_cap; clamped */
-    TQ_DEVERR_TIMEOUT = 1u << 4    /* decode: a bounded wait for a staged page gave up; split abandoned */
+    TQ_DEVERR_TIMEOUT = 1u << 4,   /* decode: a bounded wait for a staged page gave up; split abandoned */
+    TQ_DEVERR_CHUNK = 1u << 5      /* extend: a token row outside every sequence's chunk (cu_q); its output is 0 */
 };
 
 typedef struct tq_cache_config {
@@ -258,6 +259,37 @@ tq_status tq_store(const tq_cache* cache, const void* k, const void* v, int in_d
 tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype, const void* cache_buf,
                               const int32_t* block_table, const int32_t* seq_lens, const void* tail_k,
                               const void* tail_v, const int32_t* tail_lens, float scale, int batch, void* out,
+                              int out_dtype, void* stream);
+
+/*
+ * Extend (prefill) attention over the compressed paged cache ([Roadmap] §4.1:
+ * the extend kernel, like the decode kernel, reads the compressed pool
+ * directly).  Sequence b < batch brings n_b = cu_q[b+1] - cu_q[b] new tokens:
+ * rows cu_q[b] .. cu_q[b+1]-1 of q, new_k and new_v.  Its first
+ * prefix_lens[b] tokens are in the cache (block-table row b).  New token j of
+ * the chunk attends to every prefix token as tq_decode_attention scores it and
+ * to new tokens 0..j with their exact bf16 keys and values (causal), in one
+ * softmax:
+ *   out[cu_q[b] + j][h] = tq_decode_attention of that query over the prefix
+ *                         with new tokens 0..j as its tail.
+ * (The new tokens are stored into the cache separately, by tq_store.)
+ *   q            device [n_tokens][H_q][d], q_dtype
+ *   block_table  device int32 [batch][max_blocks_per_seq]
+ *   prefix_lens  device int32 [batch], 0..16*max_blocks_per_seq
+ *   cu_q         device int32 [batch+1], non-decreasing, cu_q[0] = 0,
+ *                cu_q[batch] = n_tokens.  A row of q that no chunk holds gets
+ *                out = 0 and sets TQ_DEVERR_CHUNK; every row a chunk names
+ *                lies in [0, n_tokens).
+ *   new_k/new_v  device bf16 [n_tokens][H_kv][d]
+ *   scale, out_dtype as for tq_decode_attention; out device [n_tokens][H_q][d]
+ * Each token is one entry of the decode grid: n_tokens <= max_batch, and a
+ * chunk may hold at most tail_cap tokens (tail_cap >= 1; a longer chunk is
+ * clamped and sets TQ_DEVERR_TAIL).  Uses the cache's workspace, like
+ * tq_decode_attention.  n_tokens == 0 is a no-op.
+ */
+tq_status tq_extend_attention(const tq_cache* cache, const void* q, int q_dtype, const void* cache_buf,
+                              const int32_t* block_table, const int32_t* prefix_lens, const int32_t* cu_q,
+                              const void* new_k, const void* new_v, float scale, int batch, int n_tokens, void* out,
                               int out_dtype, void* stream);
 
 /*

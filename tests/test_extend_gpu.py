@@ -1,0 +1,145 @@
+"""GPU parity of tq_extend_attention against the oracle's extend attention on
+the same compressed cache (written by the oracle's store and uploaded): every
+new token attends to its sequence's compressed prefix and, causally, to the
+exact new tokens.  Same error bar as the decode: max-abs 2e-3, relative L2
+1e-3 on an fp32 output."""
+
+import numpy as np
+import pytest
+
+import parity
+import turboquant_bit_kv_tq_gb300 as tq
+from oracle import paged
+from turboquant_bit_kv_tq_gb300 import workloads as wl
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+class Extend:
+    """Sequences with prefix[b] cached tokens (oracle-encoded) and chunk[b]
+    new exact bf16 tokens; queries for every new token."""
+
+    def __init__(self, w, prefix, chunk, spare_blocks=2):
+        self.w, self.prefix, self.chunk = w, list(prefix), list(chunk)
+        self.P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook,
+                                   w.v_codebook)
+        B = len(prefix)
+        need = [(n + 15) // 16 for n in prefix]
+        self.max_blocks = max(1, max(need))
+        self.num_blocks = sum(need) + spare_blocks
+        rng = np.random.default_rng((w.seed, 91))
+        perm = rng.permutation(self.num_blocks)
+        self.table = np.zeros((B, self.max_blocks), np.int32)
+        at = 0
+        for b, n in enumerate(need):
+            self.table[b, :n] = perm[at:at + n]
+            at += n
+        self.cache = np.zeros((self.num_blocks, w.kv_heads, self.P.layout.page_bytes), np.uint8)
+        ks, vs = [], []
+        for b in range(B):
+            K, V = wl.kv_tokens(w, b, 0, prefix[b])
+            t = np.arange(prefix[b])
+            paged.store(self.cache, self.P, K, V, self.table[b, t // 16].astype(np.int64) * 16 + t % 16)
+            K, V = wl.kv_tokens(w, b, prefix[b], chunk[b])
+            ks.append(wl.round_bf16(K))
+            vs.append(wl.round_bf16(V))
+        self.cu = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+        self.T = int(self.cu[-1])
+        self.ck = np.concatenate(ks) if self.T else np.zeros((0, w.kv_heads, w.d), np.float32)
+        self.cv = np.concatenate(vs) if self.T else np.zeros((0, w.kv_heads, w.d), np.float32)
+        self.Q = wl.queries(w, max(1, self.T))[: self.T]
+
+    def oracle(self):
+        return paged.extend_attention(self.cache, self.P, self.Q.astype(np.float64), self.table, self.prefix,
+                                      self.cu, self.ck, self.cv)
+
+    def make_cache(self, split_blocks, tail_cap=None, max_batch=None):
+        kw = wl.cache_config_kwargs(self.w, num_blocks=self.num_blocks, max_blocks=self.max_blocks,
+                                    max_batch=max_batch or max(1, self.T), split_blocks=split_blocks)
+        kw["tail_cap"] = tail_cap or max(1, max(self.chunk))
+        c = tq.TQCache(**kw)
+        c.cache.copy_(torch.from_numpy(self.cache.reshape(-1)))
+        return c
+
+    def run(self, c, cu=None, out_dtype=torch.float32):
+        dt = torch.bfloat16 if self.w.dtype == "bf16" else torch.float32
+        q = torch.from_numpy(np.ascontiguousarray(self.Q)).to("cuda", dt)
+        bf = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda", torch.bfloat16)  # noqa: E731
+        cu = self.cu if cu is None else cu
+        out = c.extend(q, torch.from_numpy(self.table).cuda(),
+                       torch.tensor(self.prefix, dtype=torch.int32, device="cuda"),
+                       torch.from_numpy(np.asarray(cu, np.int32)).cuda(), bf(self.ck), bf(self.cv),
+                       out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy()
+
+
+def _assert_close(got, ref):
+    max_abs, rel = parity.output_errors(got, ref)
+    assert max_abs <= parity.MAX_ABS and rel <= parity.REL_L2, (max_abs, rel)
+
+
+CASES = [
+    # id, workload, changes, prefix lens, chunk lens, split blocks
+    ("gqa4_g32", "llama8b_gqa4_b16_8k", {}, [300, 0, 17], [5, 9, 1], 4),
+    ("gqa4_long_chunk", "llama8b_gqa4_b16_8k", {}, [129], [40], 2),
+    ("d256_mse", "d256_gqa8_b8_32k", {}, [200, 33], [7, 3], 4),
+    ("uniform_k4_gqa8", "llama70b_gqa8_b4_ragged131k_hybrid", dict(k_bits=4, k_codebook="uniform", tail=0),
+     [64, 500], [12, 2], 8),
+    ("f32_single_head", "single_head_d128_1k", {}, [1024], [8], 8),
+    ("prefill_only", "llama8b_gqa4_b16_8k", {}, [0, 0], [16, 3], 4),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_extend_parity(case):
+    cid, name, changes, prefix, chunk, sb = case
+    w = wl.scaled(wl.config(name), **changes)
+    e = Extend(w, prefix, chunk)
+    c = e.make_cache(sb)
+    got = e.run(c)
+    ref = e.oracle()
+    _assert_close(got, ref)
+    assert c.device_error() == 0
+    assert np.abs(ref).max() > 0.1
+
+
+def test_extend_rows_outside_every_chunk_are_zero_and_flagged():
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [40, 20], [3, 4])
+    c = e.make_cache(4)
+    bad_cu = np.array([0, 3, 5], np.int32)  # rows 5 and 6 belong to no chunk
+    got = e.run(c, cu=bad_cu)
+    assert c.device_error() == tq.TQ_DEVERR_CHUNK
+    assert np.all(got[5:] == 0)
+    # rows 0..4 are the extend of sequences with chunks [3, 2]
+    ref = paged.extend_attention(e.cache, e.P, e.Q[:5].astype(np.float64), e.table, e.prefix, bad_cu, e.ck[:5],
+                                 e.cv[:5])
+    _assert_close(got[:5], ref)
+
+
+def test_extend_chunk_longer_than_tail_cap_is_flagged():
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [32], [6])
+    c = e.make_cache(4, tail_cap=4)
+    got = e.run(c)
+    assert c.device_error() == tq.TQ_DEVERR_TAIL
+    _assert_close(got[:4], e.oracle()[:4])  # tokens within the cap are exact
+
+
+def test_extend_more_tokens_than_max_batch_is_rejected():
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [16], [5])
+    c = e.make_cache(4, max_batch=4)
+    with pytest.raises(tq.TQError):
+        e.run(c)
+
+
+def test_extend_bf16_output():
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [100], [6])
+    c = e.make_cache(4)
+    got = e.run(c, out_dtype=torch.bfloat16)
+    ref = e.oracle()
+    assert np.max(np.abs(got - ref)) <= 8e-3 * max(1.0, np.abs(ref).max())

@@ -20,7 +20,7 @@ __all__ = [
     "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
-    "tq_get_device_error", "tq_set_store_small_max", "TQCache",
+    "tq_get_device_error", "tq_set_store_small_max", "tq_extend_attention", "TQ_DEVERR_CHUNK", "TQCache",
     "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT",
 ]
 
@@ -28,14 +28,14 @@ TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
 TQ_OUT_ROTATED = 0x100
 TQ_V_MSE, TQ_V_G32 = 0, 1
 TQ_CODEBOOK_LLOYD, TQ_CODEBOOK_UNIFORM = 0, 1
-TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT, TQ_DEVERR_CHUNK = 1, 2, 4, 8, 16, 32
 
 # every function include/tq_kv.h declares
 EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
     "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
-    "tq_set_store_small_max", "tq_make_uniform_codebook",
+    "tq_set_store_small_max", "tq_make_uniform_codebook", "tq_extend_attention",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -110,6 +110,7 @@ def load_library():
             "tq_store": (i32, [_P, _P, _P, i32, i64, _P, _P, _P]),
             "tq_decode_attention": (i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_set_profile_events": (i32, [_P, i32, _P, _P]),
+            "tq_extend_attention": (i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, i32, _P, i32, _P]),
             "tq_decode_attention_noalloc": (
                 i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_get_device_error": (i32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
@@ -281,6 +282,26 @@ def tq_decode_attention_noalloc(handle, q, cache, block_table, seq_lens, out, ta
         _stream_ptr(stream)), "tq_decode_attention_noalloc")
 
 
+def tq_extend_attention(handle, q, cache, block_table, prefix_lens, cu_q, new_k, new_v, out, scale=0.0, stream=None,
+                        rotated=False):
+    """q [T, H_q, d] (f32/bf16); block_table int32 [B, max_blocks_per_seq];
+    prefix_lens int32 [B]; cu_q int32 [B+1]; new_k, new_v bf16 [T, H_kv, d];
+    out [T, H_q, d] (f32/bf16)."""
+    import torch
+
+    T = q.shape[0]
+    if new_k.shape != new_v.shape or new_k.shape[0] != T or out.shape != q.shape:
+        raise ValueError("q, new_k, new_v and out must share the token count (out shaped like q)")
+    if cu_q.shape[0] != prefix_lens.shape[0] + 1 or block_table.shape[0] < prefix_lens.shape[0]:
+        raise ValueError("cu_q must have batch+1 entries and block_table at least batch rows")
+    _check(load_library().tq_extend_attention(
+        handle, _dev(q, "q"), _dtype_code(q), _dev(cache, "cache"), _dev(block_table, "block_table", torch.int32),
+        _dev(prefix_lens, "prefix_lens", torch.int32), _dev(cu_q, "cu_q", torch.int32),
+        _dev(new_k, "new_k", torch.bfloat16), _dev(new_v, "new_v", torch.bfloat16), float(scale),
+        prefix_lens.shape[0], q.shape[0], _dev(out, "out"), _dtype_code(out) | (TQ_OUT_ROTATED if rotated else 0),
+        _stream_ptr(stream)), "tq_extend_attention")
+
+
 def tq_set_profile_events(handle, kernel, start=None, stop=None):
     """Record torch.cuda.Event pairs around the store (kernel=0) or decode
     split-KV (kernel=1) launch of later calls; None switches it off."""
@@ -329,6 +350,16 @@ class TQCache:
             out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
         tq_decode_attention(self.handle, q, self.cache, block_table, seq_lens, out, tail_k, tail_v, tail_lens,
                             scale, stream, rotated)
+        return out
+
+    def extend(self, q, block_table, prefix_lens, cu_q, new_k, new_v, out=None, scale=0.0, stream=None,
+               out_dtype=None, rotated=False):
+        import torch
+
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
+        tq_extend_attention(self.handle, q, self.cache, block_table, prefix_lens, cu_q, new_k, new_v, out, scale,
+                            stream, rotated)
         return out
 
     def device_error(self, stream=None):

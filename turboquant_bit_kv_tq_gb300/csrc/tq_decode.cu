@@ -147,3 +147,103 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     void *e0 = c->prof_start[TQ_PROF_DECODE_SPLIT], *e1 = c->prof_stop[TQ_PROF_DECODE_SPLIT];
     return launch_decode(a, s, e0, e1);
 }
+
+namespace tq {
+
+// One thread per new token t: find the sequence whose chunk holds row t (the
+// last b with cu_q[b] <= t) and write the token's decode-entry view: compressed
+// length = the prefix, block-table row b, exact tail = chunk rows
+// cu_q[b] .. t.  A row outside every chunk gets no token at all (output 0)
+// and sets TQ_DEVERR_CHUNK; the rows it names always lie in [0, t].
+__global__ void extend_entries_kernel(const int32_t* __restrict__ prefix_lens, const int32_t* __restrict__ cu_q,
+                                      int batch, int n_tokens, int32_t* seq_len, int32_t* tail_len, int32_t* row_of,
+                                      int32_t* tail_base, uint32_t* err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_tokens) return;
+    int lo = 0, hi = batch - 1, b = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cu_q[mid] <= t) {
+            b = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    const int start = b >= 0 ? cu_q[b] : -1;
+    if (b < 0 || start < 0 || t >= cu_q[b + 1]) {
+        seq_len[t] = tail_len[t] = row_of[t] = tail_base[t] = 0;
+        set_error(err, TQ_DEVERR_CHUNK);
+        return;
+    }
+    seq_len[t] = prefix_lens[b];
+    tail_len[t] = t - start + 1;
+    row_of[t] = b;
+    tail_base[t] = start;
+}
+
+}  // namespace tq
+
+extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
+                                         const int32_t* block_table, const int32_t* prefix_lens, const int32_t* cu_q,
+                                         const void* new_k, const void* new_v, float scale, int batch, int n_tokens,
+                                         void* out, int out_dtype, void* stream) {
+    if (!c || !q || !cache_buf || !block_table || !prefix_lens || !cu_q || !new_k || !new_v || !out)
+        return TQ_ERR_INVALID_ARG;
+    if (batch < 1 || n_tokens < 0 || n_tokens > c->cfg.max_batch || c->cfg.tail_cap < 1) return TQ_ERR_INVALID_ARG;
+    if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+    const bool out_rot = (out_dtype & TQ_OUT_ROTATED) != 0;
+    out_dtype &= ~TQ_OUT_ROTATED;
+    if (out_dtype != TQ_DTYPE_F32 && out_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+    if (out_rot && c->cfg.v_mode != TQ_V_MSE) return TQ_ERR_INVALID_ARG;
+    if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
+    if (n_tokens == 0) return TQ_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int B = c->cfg.max_batch;
+    int32_t* seq_len = c->ws_ext;
+    int32_t* tail_len = seq_len + B;
+    int32_t* row_of = tail_len + B;
+    int32_t* tail_base = row_of + B;
+    extend_entries_kernel<<<(n_tokens + 255) / 256, 256, 0, s>>>(prefix_lens, cu_q, batch, n_tokens, seq_len,
+                                                                 tail_len, row_of, tail_base, c->dp.err);
+    {
+        const tq_status st = cuda_status(cudaGetLastError());
+        if (st != TQ_OK) return st;
+    }
+    DecodeArgs a;
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.cache = static_cast<const uint8_t*>(cache_buf);
+    a.block_table = block_table;
+    a.seq_lens = seq_len;
+    a.tail_k = static_cast<const uint16_t*>(new_k);
+    a.tail_v = static_cast<const uint16_t*>(new_v);
+    a.tail_lens = tail_len;
+    a.row_of = row_of;
+    a.tail_base = tail_base;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.out_rotated = out_rot;
+    a.k_uniform = c->cfg.k_codebook == TQ_CODEBOOK_UNIFORM;
+    const int d = c->cfg.head_dim;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    a.scale_log2e = sc * 1.4426950408889634f;
+    a.batch = n_tokens;
+    a.num_blocks = c->cfg.num_blocks;
+    a.heads = c->cfg.num_kv_heads;
+    a.q_heads = c->cfg.num_q_heads;
+    a.group = a.q_heads / a.heads;
+    a.max_blocks = c->cfg.max_blocks_per_seq;
+    a.split_blocks = c->cfg.split_blocks;
+    a.tail_cap = c->cfg.tail_cap;
+    a.sp = c->splits;
+    a.lay = c->lay;
+    a.dp = c->dp;
+    a.gm = c->geom;
+    a.ws_q = c->ws_q;
+    a.ws_bimg = c->ws_bimg;
+    a.ws_cst = c->ws_cst;
+    a.ws_acc = c->ws_acc;
+    a.ws_ml = c->ws_ml;
+    return launch_decode(a, s, c->prof_start[TQ_PROF_DECODE_SPLIT], c->prof_stop[TQ_PROF_DECODE_SPLIT]);
+}

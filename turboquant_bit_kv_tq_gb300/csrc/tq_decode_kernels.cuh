@@ -61,6 +61,12 @@ struct DecodeArgs {
     int out_dtype;
     bool out_rotated;  // MSE values: leave the output in the rotated space (no R^T)
     bool k_uniform;    // the key codebook is a uniform grid
+    // extend attention: batch entry b is one new token; row_of[b] is its
+    // sequence's block-table row, and its exact tail tokens are rows
+    // tail_base[b] + i of a token-major [tokens][H_kv][d] buffer.  Both null
+    // for decode (row b; tail [B][H_kv][tail_cap][d]).
+    const int32_t* row_of = nullptr;
+    const int32_t* tail_base = nullptr;
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -432,14 +438,18 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         for (int p = 0; p < kPerThread; ++p) acc[h][p] = 0.f;
     }
     __syncthreads();
-    const int64_t kv_base = ((int64_t)b * a.heads + g) * a.tail_cap;
+    // element offset of tail token i of (entry b, KV head g)
+    const int64_t row0 = a.tail_base ? (int64_t)a.tail_base[b] : 0;
+    auto tail_off = [&](int i) -> int64_t {
+        return a.tail_base ? ((row0 + i) * a.heads + g) * D : (((int64_t)b * a.heads + g) * a.tail_cap + i) * D;
+    };
     for (int tt = 0; tt < tl; tt += kTile) {
         const int n_tok = min(kTile, tl - tt);
         for (int e = tid; e < G * kTile; e += blockDim.x) pr[e] = -INFINITY;
         __syncthreads();
         for (int e = tid; e < n_tok * G; e += blockDim.x) {
             const int t = e / G, h = e % G;
-            const uint16_t* krow = a.tail_k + (kv_base + tt + t) * D;
+            const uint16_t* krow = a.tail_k + tail_off(tt + t);
             float s = 0.f;
             for (int i = 0; i < D; ++i) s = fmaf(qs[h * D + i], bf16_bits_to_float(krow[i]), s);
             pr[h * kTile + t] = s;
@@ -475,7 +485,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
             for (int p = 0; p < kPerThread; ++p) {
                 const int i = tid + 128 * p;
                 for (int t = 0; t < n_tok; ++t) {
-                    const float v = bf16_bits_to_float(a.tail_v[(kv_base + tt + t) * D + i]);
+                    const float v = bf16_bits_to_float(a.tail_v[tail_off(tt + t) + i]);
                     for (int h = 0; h < G; ++h) acc[h][p] = fmaf(pr[h * kTile + t], v, acc[h][p]);
                 }
             }
@@ -640,7 +650,7 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
         }
     }
 
-    const int32_t* btab = a.block_table + (int64_t)b * a.max_blocks + t0 / kBlock;
+    const int32_t* btab = a.block_table + (int64_t)(a.row_of ? a.row_of[b] : b) * a.max_blocks + t0 / kBlock;
     if (tid == 0) {
         for (int i = 0; i < S + 2; ++i) mbar_init(smem_u32(&bars[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

@@ -412,7 +412,10 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             if (e < nk * SB) {
                 const WsItem& it = items[e / SB];
                 const int pg = e % SB;
-                if (pg < it.n_pages) v[u] = a.block_table[(int64_t)it.b * a.max_blocks + it.t0 / kBlock + pg];
+                if (pg < it.n_pages) {
+                    const int row = a.row_of ? a.row_of[it.b] : it.b;
+                    v[u] = a.block_table[(int64_t)row * a.max_blocks + it.t0 / kBlock + pg];
+                }
             }
         }
 #pragma unroll

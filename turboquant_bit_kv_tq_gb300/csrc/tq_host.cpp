@@ -135,6 +135,8 @@ WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     off = up256(off + bh * s.n_splits * d * 4);
     w.ml = off;
     off = up256(off + bh * s.n_splits * 2 * 4);
+    w.ext = off;
+    off = up256(off + size_t(c.max_batch) * 4 * 4);
     w.total = off;
     return w;
 }
@@ -531,6 +533,7 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     h->ws_cst = (float*)(ws + wl.cst);
     h->ws_acc = (float*)(ws + wl.acc);
     h->ws_ml = (float*)(ws + wl.ml);
+    h->ws_ext = (int32_t*)(ws + wl.ext);
     *out = h;
     return TQ_OK;
 }

@@ -77,8 +77,9 @@ DecodeGeom decode_geom(const tq_cache_config& c);
 
 struct WorkspaceLayout {
     // q: [B][Hq][3][d] fp32; bimg: [B][Hkv][nhg][bimg_bytes] (score operands);
-    // cst: [B][Hq][4] fp32; acc: [B][Hq][S][d]; ml: [B][Hq][S][2]
-    size_t q, bimg, cst, acc, ml, total;
+    // cst: [B][Hq][4] fp32; acc: [B][Hq][S][d]; ml: [B][Hq][S][2];
+    // ext: 4 x [B] int32 (extend attention's per-token lengths and rows)
+    size_t q, bimg, cst, acc, ml, ext, total;
 };
 
 // TQ_OK for cudaSuccess; otherwise records the runtime's message for
@@ -105,6 +106,7 @@ struct tq_cache {
     float* ws_cst;
     float* ws_acc;
     float* ws_ml;
+    int32_t* ws_ext;
     // profiling events (cudaEvent_t) around the store / decode-split kernels
     void* prof_start[2] = {nullptr, nullptr};
     void* prof_stop[2] = {nullptr, nullptr};
