@@ -249,7 +249,8 @@ tq_status tq_store(const tq_cache* cache, const void* k, const void* v, int in_d
  *   cache_buf   device, as written by tq_store
  *   block_table device int32 [batch][max_blocks_per_seq]
  *   seq_lens    device int32 [batch], compressed tokens, 0..16*max_blocks_per_seq
- *   tail_k/v    device bf16 [batch][H_kv][tail_cap][d] or NULL (no tail)
+ *   tail_k/v    device bf16 [batch][H_kv][tail_cap][d] or NULL (no tail);
+ *               16-byte aligned (else TQ_ERR_MISALIGNED)
  *   tail_lens   device int32 [batch] or NULL (no tail)
  *   scale       softmax scale; <= 0 means 1/sqrt(d)
  *   out         device [batch][H_q][d], out_dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16,
@@ -280,7 +281,7 @@ tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype,
  *                cu_q[batch] = n_tokens.  A row of q that no chunk holds gets
  *                out = 0 and sets TQ_DEVERR_CHUNK; every row a chunk names
  *                lies in [0, n_tokens).
- *   new_k/new_v  device bf16 [n_tokens][H_kv][d]
+ *   new_k/new_v  device bf16 [n_tokens][H_kv][d], 16-byte aligned
  *   scale, out_dtype as for tq_decode_attention; out device [n_tokens][H_q][d]
  * Each token is one entry of the decode grid: n_tokens <= max_batch, and a
  * chunk may hold at most tail_cap tokens (tail_cap >= 1; a longer chunk is

@@ -109,6 +109,7 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     if (out_rot && c->cfg.v_mode != TQ_V_MSE) return TQ_ERR_INVALID_ARG;
     const bool has_tail = tail_k != nullptr || tail_v != nullptr || tail_lens != nullptr;
     if (has_tail && (!tail_k || !tail_v || !tail_lens || c->cfg.tail_cap == 0)) return TQ_ERR_INVALID_ARG;
+    if (((uintptr_t)tail_k | (uintptr_t)tail_v) & 15) return TQ_ERR_MISALIGNED;
     if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
     DecodeArgs a;
     a.q = q;
@@ -196,7 +197,7 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
     out_dtype &= ~TQ_OUT_ROTATED;
     if (out_dtype != TQ_DTYPE_F32 && out_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
     if (out_rot && c->cfg.v_mode != TQ_V_MSE) return TQ_ERR_INVALID_ARG;
-    if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
+    if (((uintptr_t)cache_buf | (uintptr_t)new_k | (uintptr_t)new_v) & 15) return TQ_ERR_MISALIGNED;
     if (n_tokens == 0) return TQ_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const int B = c->cfg.max_batch;

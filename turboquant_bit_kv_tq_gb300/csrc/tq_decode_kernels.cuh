@@ -447,12 +447,34 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         const int n_tok = min(kTile, tl - tt);
         for (int e = tid; e < G * kTile; e += blockDim.x) pr[e] = -INFINITY;
         __syncthreads();
-        for (int e = tid; e < n_tok * G; e += blockDim.x) {
-            const int t = e / G, h = e % G;
-            const uint16_t* krow = a.tail_k + tail_off(tt + t);
-            float s = 0.f;
-            for (int i = 0; i < D; ++i) s = fmaf(qs[h * D + i], bf16_bits_to_float(krow[i]), s);
-            pr[h * kTile + t] = s;
+        // a thread per token: one pass over its key row (16-byte loads) for
+        // every head of the group
+        for (int t = tid; t < n_tok; t += blockDim.x) {
+            const uint4* krow = reinterpret_cast<const uint4*>(a.tail_k + tail_off(tt + t));
+            float s[kMaxG];
+#pragma unroll
+            for (int h = 0; h < kMaxG; ++h) s[h] = 0.f;
+            for (int i8 = 0; i8 < D / 8; ++i8) {
+                const uint4 u = __ldg(krow + i8);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float kf[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kf[2 * e] = __uint_as_float(w[e] << 16);
+                    kf[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int h = 0; h < kMaxG; ++h) {
+                    if (h < G) {
+                        const float* qh = qs + h * D + 8 * i8;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s[h] = fmaf(qh[e], kf[e], s[h]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < kMaxG; ++h)
+                if (h < G) pr[h * kTile + t] = s[h];
         }
         __syncthreads();
         {
@@ -470,7 +492,11 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
             pr[e] = sv == -INFINITY ? 0.f : exp2f(sv - sm_m[e / kTile]);
         }
         __syncthreads();
-        for (int h = 0; h < G; ++h) {
+        // (head loops unrolled to kMaxG with a guard keep the running
+        // state in registers)
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+            if (h >= G) continue;
             const float m_new = sm_m[h];
             const float alpha = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
             float psum = 0.f;
@@ -486,7 +512,9 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
                 const int i = tid + 128 * p;
                 for (int t = 0; t < n_tok; ++t) {
                     const float v = bf16_bits_to_float(a.tail_v[tail_off(tt + t) + i]);
-                    for (int h = 0; h < G; ++h) acc[h][p] = fmaf(pr[h * kTile + t], v, acc[h][p]);
+#pragma unroll
+                    for (int h = 0; h < kMaxG; ++h)
+                        if (h < G) acc[h][p] = fmaf(pr[h * kTile + t], v, acc[h][p]);
                 }
             }
         }
@@ -497,22 +525,29 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         float* buf = qs;
         __syncthreads();
         if (tid < 128)
-            for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int p = 0; p < kPerThread; ++p) buf[h * D + tid + 128 * p] = acc[h][p] * a.dp.signs[tid + 128 * p];
+            for (int h = 0; h < kMaxG; ++h)
+                if (h < G)
+#pragma unroll
+                    for (int p = 0; p < kPerThread; ++p)
+                        buf[h * D + tid + 128 * p] = acc[h][p] * a.dp.signs[tid + 128 * p];
         __syncthreads();
         if (tid < 128)
-            for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int p = 0; p < kPerThread; ++p) {
-                    const int i = tid + 128 * p;
-                    float s = 0.f;
-                    for (int j = 0; j < D; ++j) s += (__popc(i & j) & 1) ? -buf[h * D + j] : buf[h * D + j];
-                    acc[h][p] = s * rsqrtf((float)D);
-                }
+            for (int h = 0; h < kMaxG; ++h)
+                if (h < G)
+#pragma unroll
+                    for (int p = 0; p < kPerThread; ++p) {
+                        const int i = tid + 128 * p;
+                        float s = 0.f;
+                        for (int j = 0; j < D; ++j) s += (__popc(i & j) & 1) ? -buf[h * D + j] : buf[h * D + j];
+                        acc[h][p] = s * rsqrtf((float)D);
+                    }
     }
     if (tid < 128)
-        for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+            if (h >= G) continue;
             const int64_t idx = ((int64_t)b * a.q_heads + g * G + h) * a.sp.n_splits + chunk;
 #pragma unroll
             for (int p = 0; p < kPerThread; ++p) a.ws_acc[idx * D + tid + 128 * p] = acc[h][p];

@@ -53,6 +53,7 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache* c, const void* 
     if (out_rot && c->cfg.v_mode != TQ_V_MSE) return TQ_ERR_INVALID_ARG;
     const bool has_tail = tail_k != nullptr || tail_v != nullptr || tail_lens != nullptr;
     if (has_tail && (!tail_k || !tail_v || !tail_lens || c->cfg.tail_cap == 0)) return TQ_ERR_INVALID_ARG;
+    if (((uintptr_t)tail_k | (uintptr_t)tail_v) & 15) return TQ_ERR_MISALIGNED;
     if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
     const WorkspaceLayout wl = workspace_layout(c->cfg);
     if (wl.total > kNoAllocScratch) return TQ_ERR_BUFFER_TOO_SMALL;
