@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,17 +76,27 @@ def _kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+_TRAFFIC_RE = re.compile(r"traffic record: kernel=(\S+) workload=(\S+) source_hash=([0-9a-f]+) "
+                         r"dram_bytes_per_launch=(\d+)")
+
+
 def _ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    """DRAM bytes (read + write) per launch from a committed ncu summary under
+    profiles/ (its "traffic record" line), if that capture was taken on the
+    current kernel sources; else None."""
+    want = _kernel_source_hash()
+    pdir = os.path.join(ROOT, "profiles")
     try:
-        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            rec = json.load(f)
-        e = rec.get(f"{kernel}:{workload}")
-        if e and e.get("source_hash") == _kernel_source_hash():
-            return e.get("dram_bytes_per_launch_scaled", e.get("dram_bytes_per_launch"))
-    except Exception:
-        pass
+        names = sorted(os.listdir(pdir))
+    except OSError:
+        return None
+    for name in names:
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for m in _TRAFFIC_RE.finditer(f.read()):
+                if m.group(1) == kernel and m.group(2) == workload and m.group(3) == want:
+                    return int(m.group(4))
     return None
 
 
@@ -162,6 +173,12 @@ def max_over_ranks(x, device):
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def traffic_key(w):
+    """Workload key of a traffic record: the workload name plus the key
+    format (bits, codebook initial, q when the QJL plane is kept)."""
+    return f"{w.name}:k{w.k_bits}{w.k_codebook[0]}{'q' if w.k_qjl else ''}"
 
 
 def job_value(world_size, units_per_rank, ms):
@@ -539,7 +556,7 @@ def run_ours(args):
                                  "load up to 0.6 s",
                        "step": "tq_store of each sequence's new token + tq_decode_attention"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _ncu_traffic("split_kernel", w.name),
+                         "frac": achieved / peak, "traffic": _ncu_traffic(split_kernel_name, traffic_key(w)),
                          "kernel": split_kernel_name, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": split_bytes, "bytes_per_token_head": per_token_head,
                          "units_per_launch": token_heads, "avg_launch_ms": split_avg,

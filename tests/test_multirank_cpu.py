@@ -1,7 +1,10 @@
-"""The benchmark's multi-replica path on CPU: two gloo ranks on 127.0.0.1
-reduce their step times to the slowest one, and the job value counts every
-replica's units (weak scaling).  The decode path does not shard across GPUs
-(replicas only), so this reduction is its whole multi-rank logic."""
+"""Host-side logic of the benchmark, on CPU.
+
+The multi-replica path: two gloo ranks on 127.0.0.1 reduce their step times to
+the slowest one, and the job value counts every replica's units (weak
+scaling).  The decode path does not shard across GPUs (replicas only), so this
+reduction is its whole multi-rank logic.  Also the lookup of committed ncu
+traffic figures."""
 
 import os
 import socket
@@ -53,3 +56,18 @@ def test_two_gloo_ranks_reduce_to_the_slowest_replica():
 def test_single_process_keeps_its_own_time():
     assert bench.max_over_ranks(3.0, torch.device("cpu")) == 3.0
     assert bench.job_value(1, 1000, 2.0) == pytest.approx(5e5)
+
+
+def test_traffic_record_is_read_only_for_the_current_sources(tmp_path, monkeypatch):
+    # the bench reports ncu DRAM bytes only from a summary taken on the kernel
+    # sources it runs
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "k.md").write_text("text\ntraffic record: kernel=tq::split_ws_kernel workload=w:k3lq "
+                               "source_hash=00aa11bb22cc33dd dram_bytes_per_launch=163030000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "00aa11bb22cc33dd")
+    assert bench._ncu_traffic("tq::split_ws_kernel", "w:k3lq") == 163030000
+    assert bench._ncu_traffic("tq::split_ws_kernel", "w:k4uq") is None
+    monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "ffffffffffffffff")
+    assert bench._ncu_traffic("tq::split_ws_kernel", "w:k3lq") is None
