@@ -405,7 +405,7 @@ def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak):
             "launches": steps}
 
 
-def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4):
+def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4, split_blocks=128):
     """Extend (prefill) attention on the 8B shape (context line): batch
     sequences, each with `prefix` compressed tokens and `chunk` new exact
     tokens that attend causally among themselves."""
@@ -415,7 +415,8 @@ def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, c
     table, num_blocks = wl.block_table(w)
     T = batch * chunk
     c = tq.TQCache(device=device, **{**wl.cache_config_kwargs(w, num_blocks=num_blocks, max_blocks=table.shape[1],
-                                                               max_batch=T, split_blocks=32), "tail_cap": chunk})
+                                                               max_batch=T, split_blocks=split_blocks),
+                         "tail_cap": chunk})
     gen = torch.Generator(device=device)
     gen.manual_seed(w.seed)
     for b in range(batch):
@@ -445,7 +446,7 @@ def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, c
     attended = T * prefix + batch * chunk * (chunk + 1) // 2
     return {"workload": f"llama8b_gqa4 extend: {batch} seqs x {prefix}-token compressed prefix + {chunk} new tokens",
             "new_tokens_per_s": T / (ms * 1e-3), "attended_kv_tokens_per_s": attended / (ms * 1e-3), "ms": ms,
-            "calls": steps}
+            "split_blocks": split_blocks, "calls": steps}
 
 
 def run_ours(args):

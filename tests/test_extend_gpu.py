@@ -89,6 +89,9 @@ CASES = [
      [64, 500], [12, 2], 8),
     ("f32_single_head", "single_head_d128_1k", {}, [1024], [8], 8),
     ("prefill_only", "llama8b_gqa4_b16_8k", {}, [0, 0], [16, 3], 4),
+    ("prefill_long_chunks", "llama8b_gqa4_b16_8k", {}, [0, 5], [150, 77], 4),
+    ("k4_lloyd_fallback_kernel", "llama8b_gqa4_b16_8k", dict(k_bits=4), [100, 7], [9, 4], 4),
+    ("mse_values_chunk", "llama8b_gqa4_b16_8k", dict(v_mode="mse", v_bits=3), [64, 0], [20, 11], 4),
 ]
 
 

@@ -60,6 +60,19 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         const tq_status cfg = split_config<D>(a, &a.stages, &smem);
         if (cfg != TQ_OK) return cfg;
     }
+    if constexpr (D == 128) {
+        // extend: the exact causal part of every new token in one pass over
+        // the new-token tiles (the tail split of each entry), in stream order
+        // before the query prep
+        if (a.tail_base != nullptr && a.tail_cap > 0) {
+            a.chunk_attn = true;
+            const int warps = std::min(a.group, kChunkMaxWarps);
+            chunk_attn_kernel<D><<<dim3((a.batch + kChunkRows - 1) / kChunkRows, a.heads), 32 * warps,
+                                   chunk_smem_bytes(), s>>>(a);
+            const tq_status st = cuda_status(cudaGetLastError());
+            if (st != TQ_OK) return st;
+        }
+    }
     {
         // the split (and tail) and combine kernels launch programmatically
         // (each one's prologue overlaps the previous kernel's tail) unless
@@ -70,7 +83,7 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         const cudaError_t e = launch_pdl(false, prep_kernel<D>, dim3(a.heads, a.batch), dim3(256), prep_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    if (grid > 0 && a.tail_cap > 0) {
+    if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {
         const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
         const cudaError_t e = launch_pdl(a.pdl, tail_kernel<D>, dim3(a.heads, a.batch), dim3(128), tail_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);

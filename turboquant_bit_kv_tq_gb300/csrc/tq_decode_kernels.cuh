@@ -67,6 +67,7 @@ struct DecodeArgs {
     // for decode (row b; tail [B][H_kv][tail_cap][d]).
     const int32_t* row_of = nullptr;
     const int32_t* tail_base = nullptr;
+    bool chunk_attn = false;  // the tail partials come from chunk_attn_kernel
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -257,6 +258,9 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     pdl_launch_dependents();  // the split kernel's prologue may start
     const int g = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
+    // an extend entry with no compressed prefix uses none of this (its exact
+    // part reads the raw queries)
+    if (a.chunk_attn && a.seq_lens[b] <= 0) return;
     const int G = a.group, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t* st = reinterpret_cast<uint16_t*>(smem);           // S^T bf16 [D][D]
@@ -407,6 +411,289 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
             if (n < gm.n_cols)
                 *reinterpret_cast<uint32_t*>(img + (n & 7) * 16 + (n >> 3) * sbo + (kk0 >> 4) * 128 + (kk0 & 15)) =
                     word[k];
+        }
+    }
+}
+
+// ------------------------------------------------- extend: exact chunk part
+// Extend attention's exact causal part at d = 128, written as the tail split
+// partial of every new token.  A CTA takes 16 consecutive token rows t0.. of
+// one KV head; warp w takes query head w (then w + warps, ...).  Token t's
+// keys are rows tail_base[t] .. tail_base[t] + min(tail_len[t], tail_cap) - 1
+// of the token-major new-token buffers.  Those key tiles (64 rows) are staged
+// in shared memory once for all 16 rows and all heads:
+//   S = Q K^T    bf16 tensor-core products, fp32 accumulation (an fp32 query
+//                is split into bf16 high and low parts, two products)
+//   P V          probabilities as fp16 high and low parts times the values
+//                converted to fp16 (exact for bf16 values of normal
+//                magnitude), fp32 accumulation
+// with an online exp2 softmax per row.  MSE values leave in the rotated space
+// (R acc = H D acc / sqrt(d), butterflies across the quad's lanes and the
+// thread's registers), as the combine expects of every split.
+constexpr int kChunkRows = 16;
+constexpr int kChunkKeys = 64;
+constexpr int kChunkMaxWarps = 8;
+
+__device__ __forceinline__ void mma_bf16f32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (x, y) as fp16 high parts and fp16 roundings of the remainders
+__device__ __forceinline__ void split_f16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_f16x2(x - hf.x, y - hf.y);
+}
+
+// bf16 pair (element c, c+1) of query row t, head hq: the high parts and,
+// for an fp32 query, the low parts
+__device__ __forceinline__ void chunk_q_pair(const DecodeArgs& a, int t, int hq, int c, uint32_t& hi, uint32_t& lo) {
+    hi = lo = 0u;
+    if (t >= a.batch) return;
+    const int64_t off = ((int64_t)t * a.q_heads + hq) * 128 + c;
+    if (a.q_dtype == TQ_DTYPE_BF16) {
+        hi = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(a.q) + off);
+    } else {
+        const float2 x = *reinterpret_cast<const float2*>(static_cast<const float*>(a.q) + off);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x.x - hf.x, x.y - hf.y);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+    }
+}
+
+__host__ __device__ constexpr size_t chunk_smem_bytes() {
+    return (size_t)2 * kChunkKeys * (128 * 2 + 16) + 2 * kChunkRows * 4 + 16;
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kChunkMaxWarps) chunk_attn_kernel(DecodeArgs a) {
+    static_assert(D == 128, "the chunk kernel holds a 128-wide output row in registers");
+    constexpr int KP = D * 2 + 16;  // staged row pitch (bytes): conflict-free fragment loads
+    constexpr int NKS = D / 16, NSB = kChunkKeys / 8, NOB = D / 8;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* ks = smem;                    // [kChunkKeys][KP] keys, bf16
+    uint8_t* vs = smem + kChunkKeys * KP;  // [kChunkKeys][KP] values, fp16
+    int* rlo = reinterpret_cast<int*>(vs + kChunkKeys * KP);
+    int* rhi = rlo + kChunkRows;
+    __shared__ int s_range[2];
+    const int g = blockIdx.y, t0 = blockIdx.x * kChunkRows;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    const int G = a.group, gr = lane >> 2, q4 = lane & 3;
+    if (tid < kChunkRows) {
+        const int t = t0 + tid;
+        int lo = 0x7fffffff, hi = -1;
+        if (t < a.batch) {
+            int tl = a.tail_lens[t];
+            if (tl > a.tail_cap) {
+                if (g == 0) set_error(a.dp.err, TQ_DEVERR_TAIL);
+                tl = a.tail_cap;
+            }
+            if (tl > 0) {
+                lo = a.tail_base[t];
+                hi = lo + tl - 1;
+            }
+        }
+        rlo[tid] = lo;
+        rhi[tid] = hi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int lo = 0x7fffffff, hi = -1;
+        for (int r = 0; r < kChunkRows; ++r) {
+            lo = min(lo, rlo[r]);
+            hi = max(hi, rhi[r]);
+        }
+        s_range[0] = lo;
+        s_range[1] = hi;
+    }
+    __syncthreads();
+    const int kmin = s_range[0], kmax = s_range[1];
+    const float f = a.scale_log2e;
+    const bool qf32 = a.q_dtype != TQ_DTYPE_BF16;
+    const int lo0 = rlo[gr], hi0 = rhi[gr], lo1 = rlo[gr + 8], hi1 = rhi[gr + 8];
+    for (int hb = 0; hb < G; hb += nwarps) {
+        const int h = hb + warp;
+        const bool active = h < G;
+        const int hq = g * G + (active ? h : 0);
+        uint32_t qh[NKS][4], ql[NKS][4];
+#pragma unroll
+        for (int k = 0; k < NKS; ++k) {
+            const int c = 16 * k + 2 * q4;
+            chunk_q_pair(a, active ? t0 + gr : a.batch, hq, c, qh[k][0], ql[k][0]);
+            chunk_q_pair(a, active ? t0 + gr + 8 : a.batch, hq, c, qh[k][1], ql[k][1]);
+            chunk_q_pair(a, active ? t0 + gr : a.batch, hq, c + 8, qh[k][2], ql[k][2]);
+            chunk_q_pair(a, active ? t0 + gr + 8 : a.batch, hq, c + 8, qh[k][3], ql[k][3]);
+        }
+        float o[NOB][4];
+#pragma unroll
+        for (int n = 0; n < NOB; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        for (int k0 = kmin; k0 <= kmax; k0 += kChunkKeys) {
+            __syncthreads();  // the previous tile is consumed
+            for (int e = tid; e < kChunkKeys * (D / 8); e += blockDim.x) {
+                const int row = e / (D / 8), c8 = e % (D / 8), k = k0 + row;
+                uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+                if (k <= kmax) {
+                    const int64_t off = ((int64_t)k * a.heads + g) * D + 8 * c8;
+                    kv = __ldg(reinterpret_cast<const uint4*>(a.tail_k + off));
+                    const uint4 vb = __ldg(reinterpret_cast<const uint4*>(a.tail_v + off));
+                    const uint32_t w[4] = {vb.x, vb.y, vb.z, vb.w};
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        hw[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+                    vv = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+                *reinterpret_cast<uint4*>(ks + row * KP + 16 * c8) = kv;
+                *reinterpret_cast<uint4*>(vs + row * KP + 16 * c8) = vv;
+            }
+            __syncthreads();
+            if (!active) continue;
+            float sc[NSB][4];
+#pragma unroll
+            for (int n = 0; n < NSB; ++n) {
+                sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                const uint8_t* krow = ks + (8 * n + gr) * KP + 4 * q4;
+#pragma unroll
+                for (int k = 0; k < NKS; ++k) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 32 * k);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 32 * k + 16);
+                    mma_bf16f32(sc[n], qh[k], b0, b1);
+                    if (qf32) mma_bf16f32(sc[n], ql[k], b0, b1);
+                }
+            }
+            // scale, causal mask, running maxima of the two rows
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < NSB; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = k0 + 8 * n + 2 * q4 + (e & 1);
+                    const bool ok = e < 2 ? (key >= lo0 && key <= hi0) : (key >= lo1 && key <= hi1);
+                    const float v = ok ? sc[n][e] * f : -INFINITY;
+                    sc[n][e] = v;
+                    if (e < 2) mx0 = fmaxf(mx0, v);
+                    else mx1 = fmaxf(mx1, v);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float al0 = m0 == -INFINITY ? 0.f : exp2f(m0 - n0);
+            const float al1 = m1 == -INFINITY ? 0.f : exp2f(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int n = 0; n < NOB; ++n) {
+                o[n][0] *= al0;
+                o[n][1] *= al0;
+                o[n][2] *= al1;
+                o[n][3] *= al1;
+            }
+#pragma unroll
+            for (int n = 0; n < NSB; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float mr = e < 2 ? n0 : n1;
+                    const float p = sc[n][e] == -INFINITY ? 0.f : exp2f(sc[n][e] - mr);
+                    sc[n][e] = p;
+                    if (e < 2) l0 += p;
+                    else l1 += p;
+                }
+            // O += P V: the score fragments of key blocks 2j, 2j+1 are the
+            // A fragment of the j-th 16-key step; P goes in as an fp16 high
+            // part and the fp16 rounding of its remainder (two products)
+#pragma unroll
+            for (int j = 0; j < kChunkKeys / 16; ++j) {
+                uint32_t pa[4], pl[4];
+                split_f16x2(sc[2 * j][0], sc[2 * j][1], pa[0], pl[0]);
+                split_f16x2(sc[2 * j][2], sc[2 * j][3], pa[1], pl[1]);
+                split_f16x2(sc[2 * j + 1][0], sc[2 * j + 1][1], pa[2], pl[2]);
+                split_f16x2(sc[2 * j + 1][2], sc[2 * j + 1][3], pa[3], pl[3]);
+                const uint8_t* v0 = vs + (16 * j + 2 * q4) * KP + 2 * gr;
+#pragma unroll
+                for (int n = 0; n < NOB; ++n) {
+                    const uint8_t* vp = v0 + 16 * n;
+                    const uint32_t b0 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp) |
+                                        ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + KP) << 16);
+                    const uint32_t b1 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp + 8 * KP) |
+                                        ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + 9 * KP) << 16);
+                    mma_f16(o[n], pa[0], pa[1], pa[2], pa[3], b0, b1);
+                    mma_f16(o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+                }
+            }
+        }
+        if (!active) continue;
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (a.lay.v_mode == TQ_V_MSE) {
+            // R o = H D o / sqrt(d) on each row; column c = 8n + 2*q4 + (e & 1)
+#pragma unroll
+            for (int n = 0; n < NOB; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] *= a.dp.signs[8 * n + 2 * q4 + (e & 1)];
+#pragma unroll
+            for (int n = 0; n < NOB; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float x = o[n][e], y = o[n][e + 1];
+                    o[n][e] = x + y;
+                    o[n][e + 1] = x - y;
+                }
+#pragma unroll
+            for (int bit = 1; bit <= 2; bit <<= 1)
+#pragma unroll
+                for (int n = 0; n < NOB; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x = o[n][e], other = __shfl_xor_sync(0xffffffffu, x, bit);
+                        o[n][e] = (q4 & bit) ? other - x : x + other;
+                    }
+#pragma unroll
+            for (int hbit = 1; hbit < NOB; hbit <<= 1)
+#pragma unroll
+                for (int n = 0; n < NOB; ++n)
+                    if (!(n & hbit))
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x = o[n][e], y = o[n + hbit][e];
+                            o[n][e] = x + y;
+                            o[n + hbit][e] = x - y;
+                        }
+            const float inv = rsqrtf((float)D);
+#pragma unroll
+            for (int n = 0; n < NOB; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] *= inv;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int t = t0 + gr + 8 * rr;
+            if (t >= a.batch) continue;
+            const int64_t idx = ((int64_t)t * a.q_heads + hq) * a.sp.n_splits + a.sp.n_chunks;
+#pragma unroll
+            for (int n = 0; n < NOB; ++n)
+                *reinterpret_cast<float2*>(a.ws_acc + idx * D + 8 * n + 2 * q4) =
+                    make_float2(o[n][2 * rr], o[n][2 * rr + 1]);
+            if (q4 == 0) {
+                a.ws_ml[idx * 2] = rr ? m1 : m0;
+                a.ws_ml[idx * 2 + 1] = rr ? l1 : l0;
+            }
         }
     }
 }
@@ -639,7 +926,9 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
     if (b >= a.batch) return;
     extern __shared__ __align__(16) uint8_t smem[];
     if (a.tail_cap > 0 && chunk == a.sp.n_chunks) {
-        if (hgi == 0) tail_split<D>(a, g, b, smem);  // all G heads of the tail in one CTA
+        // all G heads of the tail in one CTA (extend's chunk kernel may have
+        // written it already)
+        if (hgi == 0 && !a.chunk_attn) tail_split<D>(a, g, b, smem);
         return;
     }
     const Layout& L = a.lay;
