@@ -124,3 +124,21 @@ def test_bad_configs_are_rejected_on_the_host():
         with pytest.raises(tq.TQError) as e:
             tq.tq_cache_sizes(tq.tq_cache_config(**{**ok, **bad}))
         assert e.value.status == status, bad
+
+
+def test_extend_binding_checks_shapes_before_any_call():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((5, 4, 128))
+    table = torch.zeros((2, 3), dtype=torch.int32)
+    pl = torch.zeros(2, dtype=torch.int32)
+    cu = torch.tensor([0, 2, 5], dtype=torch.int32)
+    kv = torch.zeros((5, 1, 128), dtype=torch.bfloat16)
+    out = torch.zeros((5, 4, 128))
+    with pytest.raises(ValueError):
+        tq.tq_extend_attention(None, q, None, table, pl, cu, kv[:4], kv, out)
+    with pytest.raises(ValueError):
+        tq.tq_extend_attention(None, q, None, table, pl, cu[:2], kv, kv, out)
+    with pytest.raises(ValueError):
+        tq.tq_extend_attention(None, q, None, table[:1], pl, cu, kv, kv, out)
+    with pytest.raises(ValueError):  # CPU tensors never reach the library
+        tq.tq_extend_attention(None, q, torch.zeros(16, dtype=torch.uint8), table, pl, cu, kv, kv, out)
