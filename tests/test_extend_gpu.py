@@ -146,3 +146,59 @@ def test_extend_bf16_output():
     got = e.run(c, out_dtype=torch.bfloat16)
     ref = e.oracle()
     assert np.max(np.abs(got - ref)) <= 8e-3 * max(1.0, np.abs(ref).max())
+
+
+def test_extend_full_size_sampled():
+    """The bench's extend context line (8B shape, 4 sequences x 4096-token
+    prefix + 256 new tokens, 128-block splits) in its launch configuration:
+    every prefix is filled by the GPU store (not compared); the pages of two
+    sampled (sequence, KV head) pairs are then overwritten with the oracle's
+    encoding, and sampled new tokens of those pairs are compared."""
+    prefix, chunk, batch = 4096, 256, 4
+    w = wl.scaled(wl.config("llama8b_gqa4_b16_8k"), batch=batch, seq_lens=[prefix] * batch)
+    P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook,
+                          w.v_codebook)
+    table, num_blocks = wl.block_table(w)
+    T = batch * chunk
+    kw = wl.cache_config_kwargs(w, num_blocks=num_blocks, max_blocks=table.shape[1], max_batch=T, split_blocks=128)
+    kw["tail_cap"] = chunk
+    c = tq.TQCache(**kw)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    t = np.arange(prefix)
+    for b in range(batch):
+        K, V = wl.kv_tokens_device(w, prefix, gen)
+        c.store(K, V, torch.from_numpy(table[b, t // 16].astype(np.int64) * 16 + t % 16).cuda())
+    torch.cuda.synchronize()
+    assert c.device_error() == 0
+    pages = c.pages()
+    picks = [(1, 3), (3, 6)]
+    ones = {}
+    for b, g in picks:
+        one = np.zeros((num_blocks, 1, P.layout.page_bytes), np.uint8)
+        K, V = wl.kv_tokens(w, b, 0, prefix, heads=[g])
+        paged.store(one, P, K, V, table[b, t // 16].astype(np.int64) * 16 + t % 16)
+        used = torch.from_numpy(np.unique(table[b]).astype(np.int64)).cuda()
+        pages[used, g] = torch.from_numpy(one[:, 0]).cuda()[used]
+        ones[(b, g)] = one
+    ck = np.concatenate([wl.round_bf16(wl.kv_tokens(w, b, prefix, chunk)[0]) for b in range(batch)])
+    cv = np.concatenate([wl.round_bf16(wl.kv_tokens(w, b, prefix, chunk)[1]) for b in range(batch)])
+    Q = wl.queries(w, T)
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda", torch.bfloat16)  # noqa: E731
+    cu = np.arange(0, T + 1, chunk, dtype=np.int32)
+    out = c.extend(bf(Q), torch.from_numpy(table).cuda(), torch.full((batch,), prefix, dtype=torch.int32,
+                                                                     device="cuda"),
+                   torch.from_numpy(cu).cuda(), bf(ck), bf(cv))
+    torch.cuda.synchronize()
+    assert c.device_error() == 0
+    got = out.cpu().numpy()
+    G = w.group
+    for (b, g), one in ones.items():
+        for j in (0, 100, chunk - 1):
+            row = b * chunk + j
+            lo = b * chunk
+            ref = paged.decode_attention(one, P, Q[row:row + 1, g * G:(g + 1) * G].astype(np.float64), table[b:b + 1],
+                                         [prefix], tail_k=ck[None, lo:row + 1, g:g + 1].transpose(0, 2, 1, 3),
+                                         tail_v=cv[None, lo:row + 1, g:g + 1].transpose(0, 2, 1, 3),
+                                         tail_lens=[j + 1])
+            _assert_close(got[row, g * G:(g + 1) * G], ref[0])
