@@ -219,6 +219,21 @@ def test_uniform_sphere_quantiser_tends_to_gaussian_table():
         assert abs(np.sqrt(8192) * step - rows[2**bits]) < 2e-3
 
 
+@pytest.mark.parametrize("bits", [3, 4])
+def test_uniform_codebook_mse_monte_carlo(bits):
+    # random unit vectors through the rotation and the uniform codebook: the
+    # mean squared error matches d * E[(t - Q(t))^2] within 3 standard errors
+    d = 128
+    c, b = codebook.sphere_uniform_codebook(d, bits)
+    R = rotation.rotation_matrix(prng.rotation_signs(d, 2))
+    X = np.random.default_rng(12).standard_normal((20000, d))
+    n16, idx, _ = quant.mse_quantise(X, R, b)
+    Xn = X / np.linalg.norm(X, axis=1, keepdims=True)
+    err = np.sum((Xn - c[idx] @ R) ** 2, axis=1)
+    D = d * codebook.nearest_neighbour_mse(codebook.SphereCoordinate(d), 1.0 / d, c)
+    assert abs(err.mean() - D) < 3 * err.std() / np.sqrt(len(err))
+
+
 def test_uniform_costs_little_distortion_at_four_bits():
     # [Roadmap] §4.3: at 4 bits the uniform grid costs almost nothing in
     # accuracy against the Lloyd codebook; in distortion it is above Lloyd-Max
