@@ -92,6 +92,7 @@ CASES = [
     ("prefill_long_chunks", "llama8b_gqa4_b16_8k", {}, [0, 5], [150, 77], 4),
     ("k4_lloyd_fallback_kernel", "llama8b_gqa4_b16_8k", dict(k_bits=4), [100, 7], [9, 4], 4),
     ("mse_values_chunk", "llama8b_gqa4_b16_8k", dict(v_mode="mse", v_bits=3), [64, 0], [20, 11], 4),
+    ("empty_chunk_first", "llama8b_gqa4_b16_8k", {}, [50, 30, 9], [0, 5, 2], 4),
 ]
 
 
