@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 
 
 def _params(w):
-    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
+    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl,
+                             w.k_codebook, w.v_codebook)
 
 
 def _dev(x, dtype):

@@ -18,7 +18,8 @@ def _cache_for(w, num_blocks):
 
 
 def _oracle_params(w):
-    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
+    return paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl,
+                             w.k_codebook, w.v_codebook)
 
 
 def _to_dev(x, dtype):

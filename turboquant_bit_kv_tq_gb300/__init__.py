@@ -17,7 +17,8 @@ __all__ = [
     "TQError", "tq_cache_config", "TQ_DTYPE_F32", "TQ_DTYPE_BF16", "TQ_OUT_ROTATED", "TQ_V_MSE", "TQ_V_G32",
     "TQ_CODEBOOK_LLOYD", "TQ_CODEBOOK_UNIFORM", "tq_make_uniform_codebook",
     "TQ_DEVERR_SLOT", "TQ_DEVERR_BLOCK", "TQ_DEVERR_SEQLEN", "TQ_DEVERR_TAIL", "TQ_DEVERR_TIMEOUT", "EXPORTED",
-    "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook", "tq_make_rotation_signs",
+    "library_path", "load_library", "tq_status_string", "tq_last_cuda_error", "tq_make_codebook",
+    "tq_make_rotation_signs",
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
     "tq_get_device_error", "tq_set_store_small_max", "tq_extend_attention", "TQ_DEVERR_CHUNK", "TQCache",
@@ -28,7 +29,8 @@ TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
 TQ_OUT_ROTATED = 0x100
 TQ_V_MSE, TQ_V_G32 = 0, 1
 TQ_CODEBOOK_LLOYD, TQ_CODEBOOK_UNIFORM = 0, 1
-TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL, TQ_DEVERR_TIMEOUT, TQ_DEVERR_CHUNK = 1, 2, 4, 8, 16, 32
+TQ_DEVERR_SLOT, TQ_DEVERR_BLOCK, TQ_DEVERR_SEQLEN, TQ_DEVERR_TAIL = 1, 2, 4, 8
+TQ_DEVERR_TIMEOUT, TQ_DEVERR_CHUNK = 16, 32
 
 # every function include/tq_kv.h declares
 EXPORTED = [
