@@ -571,7 +571,9 @@ def run_ours(args):
             "no_profiling_events": {"ms_per_step": free_ms_max,
                                     "value": job_value(ws, attended, free_ms_max),
                                     "unit": UNIT, "steps": len(free_ms)},
-            "gpu_launches": 4 * args.steps,
+            # per step: store, prep, split, combine, and the exact-tail kernel
+            # beside the warp-specialized split when the workload has a tail
+            "gpu_launches": (4 + (1 if (w.tail and ws_path) else 0)) * args.steps,
             "store_workload": store_line,
             "extend_workload": extend_line,
         }
