@@ -4,7 +4,7 @@ The multi-replica path: two gloo ranks on 127.0.0.1 reduce their step times to
 the slowest one, and the job value counts every replica's units (weak
 scaling).  The decode path does not shard across GPUs (replicas only), so this
 reduction is its whole multi-rank logic.  Also the lookup of committed ncu
-traffic figures."""
+traffic figures and the reference arm's JSON line."""
 
 import os
 import socket
@@ -71,3 +71,20 @@ def test_traffic_record_is_read_only_for_the_current_sources(tmp_path, monkeypat
     assert bench._ncu_traffic("tq::split_ws_kernel", "w:k4uq") is None
     monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "ffffffffffffffff")
     assert bench._ncu_traffic("tq::split_ws_kernel", "w:k3lq") is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm times the oracle on the host cores and prints one JSON
+    # line with the contract's keys
+    import json
+    import subprocess
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "KV tokens/s"
+    assert line["n_gpus"] == 1 and line["steps"] == 1 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "llama8b_gqa4_b16_8k"
