@@ -521,8 +521,9 @@ def run_ours(args):
                   w.batch * w.kv_heads * w.d * 2 * 2 + w.batch * w.kv_heads * per_token_head)
 
     # the warp-specialized split kernel serves every configuration whose score
-    # planes fit its tensor-memory plan (d=128 with 2- or 3-bit keys, d=256
-    # with 2-bit keys); the one-warpgroup kernel the rest
+    # planes fit its tensor-memory plan (d=128 with 2- or 3-bit keys or any
+    # uniform-codebook keys, d=256 with 2-bit keys); the one-warpgroup kernel
+    # the rest
     ws_path = (w.d == 128 and (w.k_bits <= 3 or w.k_codebook == "uniform")) or (w.d == 256 and w.k_bits == 2)
     split_kernel_name = "tq::split_ws_kernel" if ws_path else "tq::split_kernel"
     e2e_ms, h2d, d2h = _e2e(torch, c, st, w, stream, args.steps, max(3, args.warmup), flush)
