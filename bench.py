@@ -12,8 +12,13 @@ Llama-3.1-8B-shaped decode layer (32 query / 8 KV heads, d=128, batch 16,
 
 Prints one JSON line (rank 0).  `value` is KV tokens attended per second over
 the whole job (sum of context lengths / step time, summed over ranks; every
-rank runs its own replica: weak scaling).  The reference arm (--impl
-reference) times the CPU oracle on a bounded sample of the same workload.
+rank runs its own replica: weak scaling).  Beside the headline, the same line
+carries the d=256 GQA-8 decode and the 70B-shaped ragged 131K hybrid decode
+(`decode_workloads`, each with its split kernel's roofline), the store and
+extend workloads, the oracle's CPU timing (one thread and all host cores) and
+the counted boundary cases of a re-encoded store sample.  The reference arm
+(--impl reference) times the CPU oracle on a bounded sample of the same
+workload, on all host cores.
 """
 
 import argparse
@@ -52,8 +57,20 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-store-workload", action="store_true")
     p.add_argument("--no-extend-workload", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-decode-workloads", action="store_true",
+                   help="skip the d=256 and 70B-shaped hybrid decode lines")
+    p.add_argument("--no-boundary-cases", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
+
+
+# the decode workloads timed beside the headline, each with its own roofline
+EXTRA_DECODES = ["d256_gqa8_b8_32k", "llama70b_gqa8_b4_ragged131k_hybrid"]
+# arithmetic of the timed path: scores as four e4m3 pieces of the query
+# operand against exact e4m3 bit-plane operands, probabilities x values as fp16
+# high/low pieces against exact fp16 code operands, fp32 accumulation and
+# softmax; the store in fp32 with bf16-split tensor-core projections
+DTYPE = "e4m3x4 score pieces, f16 hi/lo P.V, f32 accumulate"
 
 
 # ------------------------------------------------------------------ helpers
@@ -188,54 +205,92 @@ def job_value(world_size, units_per_rank, ms):
 
 
 # ------------------------------------------------------------ CPU baseline
+def host_cores():
+    """Cores this process may run on (its CPU affinity set)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_sequence_worker(task):
+    """One oracle run (numpy fp64, one thread): sequence b of the workload, its
+    first `cap` compressed tokens and its exact tail, all heads; repeats the
+    step -- the oracle's store of the step's new token, then its decode
+    attention -- for `seconds` or `max_steps` steps.  Runs in a spawned worker
+    process (or inline); returns tokens attended, steps and seconds."""
+    name, b, cap, seconds, max_steps = task
+    import numpy as np
+
+    from oracle import paged
+    from turboquant_bit_kv_tq_gb300 import workloads as wl
+
+    w = wl.config(name)
+    P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook,
+                          w.v_codebook)
+    b = b % w.batch
+    n = min(w.compressed_lens()[b], cap)
+    nb = max(1, (n + 15) // 16)
+    cache = np.zeros((nb, w.kv_heads, P.layout.page_bytes), np.uint8)
+    K, V = wl.kv_tokens(w, b, 0, n)
+    t = np.arange(n)
+    if n > 1:
+        paged.store(cache, P, K[:-1], V[:-1], t[:-1])
+    Q = wl.queries(w)[b:b + 1].astype(np.float64)
+    tail = w.tail_lens()[b] if w.tail else 0
+    kw = {}
+    if tail:
+        tk, tv = wl.kv_tokens(w, b, w.compressed_lens()[b], tail)
+        kw = dict(tail_k=tk.transpose(1, 0, 2)[None], tail_v=tv.transpose(1, 0, 2)[None], tail_lens=[tail])
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        if n:
+            paged.store(cache, P, K[-1:], V[-1:], t[-1:])  # the step's new token
+        paged.decode_attention(cache, P, Q, np.arange(nb)[None], [n], **kw)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or steps >= max_steps:
+            break
+    return dict(tokens=(n + tail) * steps, steps=steps, seconds=el, seq_tokens=n + tail)
+
+
 _CPU_SNIPPET = r"""
-import json, os, sys, time
+import json, multiprocessing as mp, os, sys
 sys.path.insert(0, {root!r})
-import numpy as np
-from oracle import paged
-from turboquant_bit_kv_tq_gb300 import workloads as wl
-w = wl.config({name!r})
-cap = {cap}
-P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook, w.v_codebook)
-n = min(w.compressed_lens()[0], cap)
-nb = (n + 15) // 16
-cache = np.zeros((nb, w.kv_heads, P.layout.page_bytes), np.uint8)
-K, V = wl.kv_tokens(w, 0, 0, n)
-t = np.arange(n)
-paged.store(cache, P, K[:-1], V[:-1], t[:-1])
-Q = wl.queries(w, 1).astype(np.float64)
-tail = min(w.tail, w.seq_lens[0]) if w.tail else 0
-kw = {{}}
-if tail:
-    tk, tv = wl.kv_tokens(w, 0, w.compressed_lens()[0], tail)
-    kw = dict(tail_k=tk.transpose(1, 0, 2)[None], tail_v=tv.transpose(1, 0, 2)[None], tail_lens=[tail])
-steps, t0 = 0, time.perf_counter()
-while True:
-    paged.store(cache, P, K[-1:], V[-1:], t[-1:])           # the step's new token
-    paged.decode_attention(cache, P, Q, np.arange(nb)[None], [n], **kw)
-    steps += 1
-    el = time.perf_counter() - t0
-    if el >= {seconds} or steps >= {max_steps}:
-        break
-print(json.dumps(dict(steps=steps, seconds=el, tokens=(n + tail) * steps, seq_tokens=n + tail)))
+import bench
+cores = {cores}
+tasks = [({name!r}, i, {cap}, {seconds}, {max_steps}) for i in range(cores)]
+if cores == 1:
+    res = [bench._oracle_sequence_worker(tasks[0])]
+else:
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(bench._oracle_sequence_worker, tasks)
+el = max(r["seconds"] for r in res)
+print(json.dumps(dict(tokens=sum(r["tokens"] for r in res), seconds=el, steps=min(r["steps"] for r in res),
+                      seq_tokens=res[0]["seq_tokens"], workers=len(res))))
 """
 
 
-def cpu_oracle_run(name, seconds, max_steps=10**6, cap=8192):
-    """Time the oracle (single thread, spawned process) on one sequence of the
-    workload (its first `cap` compressed tokens + tail, all heads)."""
+def cpu_oracle_run(name, seconds, max_steps=10**6, cap=8192, cores=1):
+    """Time the oracle on the host, in a spawned process (so that no worker is
+    forked from a process holding a CUDA context): `cores` single-threaded
+    workers at once, worker i on sequence i of the workload (its first `cap`
+    compressed tokens + tail, all heads).  value = tokens attended by all
+    workers / the slowest worker's time."""
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = _CPU_SNIPPET.format(root=ROOT, name=name, cap=cap, seconds=seconds, max_steps=max_steps)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    code = _CPU_SNIPPET.format(root=ROOT, name=name, cap=cap, seconds=seconds, max_steps=max_steps, cores=cores)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     res = json.loads(r.stdout.strip().splitlines()[-1])
     res["value"] = res["tokens"] / res["seconds"]
-    res["cores"] = 1
-    res["sample"] = (f"oracle (numpy fp64, 1 thread) on sequence 0 of {name}: first {res['seq_tokens']} tokens "
-                     f"(compressed + tail), all {wl_heads(name)} query heads, store of the step's new token + "
-                     f"decode, {res['steps']} steps in {res['seconds']:.1f} s")
+    res["cores"] = res["workers"]
+    seqs = "sequence 0" if cores == 1 else f"sequences 0..{cores - 1} (mod the batch), one per worker process"
+    res["sample"] = (f"oracle (numpy fp64, {cores} single-threaded process{'es' if cores > 1 else ''}) on {seqs} "
+                     f"of {name}: first {res['seq_tokens']} tokens (compressed + tail), all {wl_heads(name)} query "
+                     f"heads, store of the step's new token + decode, {res['steps']}+ steps each in "
+                     f"{res['seconds']:.1f} s")
     return res
 
 
@@ -243,6 +298,46 @@ def wl_heads(name):
     from turboquant_bit_kv_tq_gb300 import workloads as wl
 
     return wl.config(name).q_heads
+
+
+def cpu_baseline(name, seconds):
+    """The oracle's throughput on the host: all cores (the reported value) and
+    one thread; cores = the worker processes used, host_cores = the affinity
+    set's size."""
+    cores = host_cores()
+    allc = cpu_oracle_run(name, seconds, cores=cores)
+    one = cpu_oracle_run(name, seconds) if cores > 1 else allc
+    return {"value": allc["value"], "unit": UNIT, "cores": allc["cores"], "kind": "oracle", "sample": allc["sample"],
+            "host_cores": cores, "single_thread": {"value": one["value"], "cores": 1, "sample": one["sample"]}}
+
+
+def boundary_cases(torch, pages, K, V, slots, w, count=1024):
+    """Re-encode `count` random tokens of a store the GPU made with the oracle
+    and compare the bytes (after the timed region; tests/parity.py's bar):
+    the counted boundary cases of each class beside the count the density
+    predicts, and the bytes that differed."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+    from oracle import paged
+
+    P = paged.CacheParams(w.d, w.k_bits, w.k_qjl, w.v_mode, w.v_bits, w.seed_rot, w.seed_qjl, w.k_codebook,
+                          w.v_codebook)
+    rng = np.random.default_rng(0)
+    pick = np.sort(rng.choice(len(slots), min(count, len(slots)), replace=False))
+    blocks = np.unique(slots[pick] // 16)
+    sub = pages[torch.from_numpy(blocks).to(pages.device)].cpu().numpy()
+    remap = {int(b): i for i, b in enumerate(blocks)}
+    sub_slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 for s in slots[pick]], np.int64)
+    Kh = K[torch.from_numpy(pick).to(K.device)].float().cpu().numpy()
+    Vh = V[torch.from_numpy(pick).to(V.device)].float().cpu().numpy()
+    r = parity.compare_store(sub, P, Kh, Vh, sub_slots, w.kv_heads)
+    return {"workload": w.name, "tokens": int(len(pick)), "vectors": r["vectors"], "checked_bytes": r["checked_bytes"],
+            "mismatched_bytes": r["mismatched_bytes"], "unexplained_bytes": len(r["unexplained"]),
+            "counted": r["counts"], "expected_from_density": {k: round(v, 3) for k, v in r["expected"].items()},
+            "bar": "codes within 1e-6 of a boundary, |S r|/||k|| < 1e-6, fp16 values within 1e-6 of a "
+                   "midpoint, group-32 half-integers: counted and excused; every other byte bit-exact"}
 
 
 # ---------------------------------------------------------- reference arm
@@ -253,9 +348,10 @@ def run_reference(args):
     from turboquant_bit_kv_tq_gb300 import workloads as wl
 
     w = wl.config(args.workload)
+    cores = host_cores()
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    cpu_oracle_run(args.workload, per_step, max_steps=max(1, args.warmup))  # warm-up steps
-    res = cpu_oracle_run(args.workload, per_step * args.steps, max_steps=args.steps)
+    cpu_oracle_run(args.workload, per_step, max_steps=max(1, args.warmup), cores=cores)  # warm-up steps
+    res = cpu_oracle_run(args.workload, per_step * args.steps, max_steps=args.steps, cores=cores)
     ms = 1e3 * res["seconds"] / res["steps"]
     line = {
         "impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": args.gpus,
@@ -263,13 +359,20 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": res["sample"]},
         "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
-                         "sample": res["sample"]},
+                         "sample": res["sample"], "host_cores": cores},
         "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------- our arm
+def _split_blocks(w, override=0):
+    """Blocks per decode split: longer splits for long contexts; a short one
+    (a few work items in all) needs short splits to spread over the SMs."""
+    longest = max(w.seq_lens)
+    return override or (64 if longest > 16384 else 32 if longest > 2048 else 8)
+
+
 def _setup_decode(w, split_blocks, torch, tq, wl, device):
     import numpy as np
 
@@ -304,11 +407,17 @@ def _setup_decode(w, split_blocks, torch, tq, wl, device):
     K, V = wl.kv_tokens_device(w, w.batch, gen, device)
     st["new_k"], st["new_v"] = K, V
     if w.tail:
+        # the newest tokens of each sequence, exact bf16, from the workload's
+        # own generator (positions compressed_len .. seq_len - 1)
         tl = w.tail_lens()
-        st["tail_k"] = (torch.randn((w.batch, w.kv_heads, w.tail, w.d), generator=gen, device=device)).to(
-            torch.bfloat16)
-        st["tail_v"] = (torch.randn((w.batch, w.kv_heads, w.tail, w.d), generator=gen, device=device)).to(
-            torch.bfloat16)
+        tk = np.zeros((w.batch, w.kv_heads, w.tail, w.d), np.float32)
+        tv = np.zeros_like(tk)
+        for b in range(w.batch):
+            kb, vb = wl.kv_tokens(w, b, comp[b], tl[b])
+            tk[b, :, :tl[b]] = kb.transpose(1, 0, 2)
+            tv[b, :, :tl[b]] = vb.transpose(1, 0, 2)
+        st["tail_k"] = torch.from_numpy(tk).to(device, torch.bfloat16)
+        st["tail_v"] = torch.from_numpy(tv).to(device, torch.bfloat16)
         st["tail_lens"] = torch.tensor(tl, dtype=torch.int32, device=device)
     return c, st, table
 
@@ -377,8 +486,68 @@ def _e2e(torch, c, st, w, stream, steps, warmup, flush):
     return ms, h2d, d2h
 
 
-def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak):
-    """Store throughput on the 65,536-token scattered append (context line)."""
+def _ws_path(w):
+    """Whether the decode runs the warp-specialized split kernel: every
+    configuration whose score planes fit its tensor-memory plan (d=128 with 2-
+    or 3-bit keys or any uniform-codebook keys, d=256 with 2-bit keys); the
+    one-warpgroup split kernel the rest.  With the warp-specialized kernel an
+    exact tail runs as its own kernel before it."""
+    return (w.d == 128 and (w.k_bits <= 3 or w.k_codebook == "uniform")) or (w.d == 256 and w.k_bits == 2)
+
+
+def _split_roofline(w, page_bytes, split_ms, peak, peak_kind):
+    """Roofline of the split-KV kernel: ALGORITHMIC bytes per launch (the
+    compressed page bytes of every attended token-head plus the block-table
+    entries; the exact tail K/V too when the split kernel reads it itself)
+    over its average event-timed duration."""
+    per_token_head = page_bytes // 16
+    token_heads = sum(w.compressed_lens()) * w.kv_heads
+    blocks = sum((n + 15) // 16 for n in w.compressed_lens())
+    tail_bytes = sum(w.tail_lens()) * w.kv_heads * w.d * 2 * 2
+    ws = _ws_path(w)
+    split_bytes = token_heads * per_token_head + blocks * 4 + (0 if ws else tail_bytes)
+    avg = statistics.mean(split_ms)
+    achieved = split_bytes / (avg * 1e-3) / 1e9
+    kernel = "tq::split_ws_kernel" if ws else "tq::split_kernel"
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": _ncu_traffic(kernel, traffic_key(w)), "kernel": kernel, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": split_bytes, "bytes_per_token_head": per_token_head,
+            "units_per_launch": token_heads, "unit_of_work": "token-head", "avg_launch_ms": avg,
+            "launches": len(split_ms)}
+
+
+def _decode_workload(torch, tq, wl, w, device, steps, warmup, flush, peak, peak_kind, split_blocks=0):
+    """One decode workload beside the headline: the same step (store of each
+    sequence's new token + decode), timed with L2 flushed between steps; its
+    split kernel's roofline; the step without profiling events."""
+    sb = _split_blocks(w, split_blocks)
+    c, st, _ = _setup_decode(w, sb, torch, tq, wl, device)
+    stream = torch.cuda.Stream(device=device)
+    _time_steps(torch, tq, c, st, stream, warmup, flush, split_events=False)
+    step_ms, split_ms = _time_steps(torch, tq, c, st, stream, steps, flush)
+    free_ms = _time_steps(torch, tq, c, st, stream, steps, flush, split_events=False)[0]
+    if c.device_error():
+        raise RuntimeError(f"device error during the {w.name} steps")
+    attended = sum(w.compressed_lens()) + sum(w.tail_lens())
+    ms = statistics.mean(step_ms)
+    line = {"workload": w.name, "value": attended / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "kv_tokens_per_step": attended, "compressed_tokens": sum(w.compressed_lens()),
+            "tail_tokens": sum(w.tail_lens()), "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
+            "head_dim": w.d, "k_bits": w.k_bits, "v_mode": w.v_mode, "v_bits": w.v_bits, "split_blocks": sb,
+            "steps": steps, "roofline": _split_roofline(w, c.page_bytes, split_ms, peak, peak_kind),
+            "no_profiling_events": {"ms_per_step": statistics.mean(free_ms),
+                                    "value": attended / (statistics.mean(free_ms) * 1e-3)},
+            "gpu_launches_per_step": 4 + (1 if (w.tail and _ws_path(w)) else 0)}
+    c.close()
+    del c, st
+    torch.cuda.empty_cache()
+    return line
+
+
+def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak, with_boundary_cases=True):
+    """Store throughput on the 65,536-token scattered append (context line);
+    then, outside the timed region, the oracle's re-encoding of a 1,024-token
+    sample of what the last timed store wrote."""
     w = wl.config("store_64seq_65536tok")
     lens, prior, table, slots = wl.store_layout(w)
     c = tq.TQCache(device=device, **wl.cache_config_kwargs(w, num_blocks=w.pool_blocks, max_blocks=4, max_batch=1))
@@ -396,13 +565,18 @@ def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak):
         c.store(K, V, s)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    if c.device_error():
+        raise RuntimeError("device error during the store workload")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     read = K.numel() * 2 * 2 + s.numel() * 8
     written = w.store_tokens * w.kv_heads * c.page_bytes // 16
     gbs = (read + written) / (ms * 1e-3) / 1e9
-    return {"workload": w.name, "tokens_per_s": w.store_tokens / (ms * 1e-3), "ms": ms,
+    line = {"workload": w.name, "tokens_per_s": w.store_tokens / (ms * 1e-3), "ms": ms,
             "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "algorithmic_bytes": read + written,
-            "launches": steps}
+            "bytes_per_token_head": 2 * w.d * 2 + c.page_bytes // 16 + 8 / w.kv_heads, "launches": steps}
+    cases = boundary_cases(torch, c.pages(), K, V, slots, w) if with_boundary_cases else None
+    c.close()
+    return line, cases
 
 
 def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4, split_blocks=128):
@@ -472,10 +646,7 @@ def run_ours(args):
         w = wl.scaled(w, k_bits=args.k_bits)
     if args.codebook != "lloyd":
         w = wl.scaled(w, k_codebook=args.codebook, v_codebook=args.codebook if w.v_mode == "mse" else "lloyd")
-    # blocks per decode split: longer splits for long contexts; a short one
-    # (a few work items in all) needs short splits to spread over the SMs
-    longest = max(w.seq_lens)
-    split_blocks = args.split_blocks or (64 if longest > 16384 else 32 if longest > 2048 else 8)
+    split_blocks = _split_blocks(w, args.split_blocks)
     c, st, table = _setup_decode(w, split_blocks, torch, tq, wl, device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
@@ -506,33 +677,29 @@ def run_ours(args):
 
     attended = sum(w.compressed_lens()) + sum(w.tail_lens())
     value = job_value(ws, attended, ms)
-    # algorithmic bytes of the split-KV kernel: the compressed bytes of every
-    # attended token-head, the block-table entries and the exact tail K/V
+    roof = _split_roofline(w, c.page_bytes, split_ms, peak, peak_kind)
+    # whole-step algorithmic bytes: the split kernel's bytes + the exact tail
+    # + q read + out written + the store's bf16 read and packed write
     per_token_head = c.page_bytes // 16
-    token_heads = sum(w.compressed_lens()) * w.kv_heads
-    blocks = sum((n + 15) // 16 for n in w.compressed_lens())
     tail_bytes = sum(w.tail_lens()) * w.kv_heads * w.d * 2 * 2
-    split_bytes = token_heads * per_token_head + blocks * 4 + tail_bytes
-    split_avg = statistics.mean(split_ms)
-    achieved = split_bytes / (split_avg * 1e-3) / 1e9
-    # whole-step algorithmic bytes: decode's bytes + q read + out written +
-    # the store's bf16 read and packed write
-    step_bytes = (split_bytes + w.batch * w.q_heads * w.d * (2 + 2) +
-                  w.batch * w.kv_heads * w.d * 2 * 2 + w.batch * w.kv_heads * per_token_head)
-
-    # the warp-specialized split kernel serves every configuration whose score
-    # planes fit its tensor-memory plan (d=128 with 2- or 3-bit keys or any
-    # uniform-codebook keys, d=256 with 2-bit keys); the one-warpgroup kernel
-    # the rest
-    ws_path = (w.d == 128 and (w.k_bits <= 3 or w.k_codebook == "uniform")) or (w.d == 256 and w.k_bits == 2)
-    split_kernel_name = "tq::split_ws_kernel" if ws_path else "tq::split_kernel"
+    step_bytes = (roof["algorithmic_bytes_per_launch"] + (tail_bytes if _ws_path(w) else 0) +
+                  w.batch * w.q_heads * w.d * (2 + 2) + w.batch * w.kv_heads * w.d * 2 * 2 +
+                  w.batch * w.kv_heads * per_token_head)
+    roof["step_achieved_gbs"] = step_bytes / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = _e2e(torch, c, st, w, stream, args.steps, max(3, args.warmup), flush)
     e2e_ms_max = max_over_ranks(e2e_ms, device)
     free_ms_max = max_over_ranks(statistics.mean(free_ms), device)
+    c.close()
+    del c, st
+    torch.cuda.empty_cache()
 
-    store_line = extend_line = None
+    extra = store_line = cases = extend_line = None
+    if rank == 0 and not args.no_decode_workloads and args.workload == DEFAULT_WORKLOAD:
+        extra = [_decode_workload(torch, tq, wl, wl.config(name), device, max(5, min(args.steps, 20)),
+                                  max(3, args.warmup), flush, peak, peak_kind) for name in EXTRA_DECODES]
     if not args.no_store_workload and rank == 0:
-        store_line = _store_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush, peak)
+        store_line, cases = _store_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush, peak,
+                                            with_boundary_cases=not args.no_boundary_cases)
     if not args.no_extend_workload and rank == 0:
         extend_line = _extend_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush)
 
@@ -540,14 +707,13 @@ def run_ours(args):
         cpu = None
         if not args.no_cpu_baseline and ws == 1:
             try:
-                r = cpu_oracle_run(args.workload, args.cpu_seconds)
-                cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+                cpu = cpu_baseline(args.workload, args.cpu_seconds)
             except Exception as e:  # reported, not fatal
                 cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"[:300]}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
                        "head_dim": w.d, "context_lens": sorted(set(w.seq_lens)), "tail": w.tail,
                        "k_bits": w.k_bits, "k_qjl": w.k_qjl, "v_mode": w.v_mode, "v_bits": w.v_bits,
@@ -557,12 +723,7 @@ def run_ours(args):
                        "clocks": "sampled every 50 ms over the timed steps plus untimed steps of the same "
                                  "load up to 0.6 s",
                        "step": "tq_store of each sequence's new token + tq_decode_attention"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _ncu_traffic(split_kernel_name, traffic_key(w)),
-                         "kernel": split_kernel_name, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": split_bytes, "bytes_per_token_head": per_token_head,
-                         "units_per_launch": token_heads, "avg_launch_ms": split_avg,
-                         "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9},
+            "roofline": roof,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
             "e2e": {"value": job_value(ws, attended, e2e_ms_max), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -574,8 +735,10 @@ def run_ours(args):
                                     "unit": UNIT, "steps": len(free_ms)},
             # per step: store, prep, split, combine, and the exact-tail kernel
             # beside the warp-specialized split when the workload has a tail
-            "gpu_launches": (4 + (1 if (w.tail and ws_path) else 0)) * args.steps,
+            "gpu_launches": (4 + (1 if (w.tail and _ws_path(w)) else 0)) * args.steps,
+            "decode_workloads": extra,
             "store_workload": store_line,
+            "boundary_cases": cases,
             "extend_workload": extend_line,
         }
         print(json.dumps(line), flush=True)

@@ -27,6 +27,11 @@
  *     configuration (CUDA-graph capturable), and do not synchronise the host.
  *     Calls on distinct streams may run concurrently only if they use distinct
  *     workspaces (one cache handle = one workspace).
+ *   - Any host thread may call any entry point, on any device (the one current
+ *     on the calling thread).  The first tq_store / tq_decode_attention /
+ *     tq_extend_attention call on a device does that device's launch set-up
+ *     (its SM count, the kernels' shared-memory limits) under a lock, once per
+ *     device; make it before capturing a stream on that device.
  *   - Bad arguments found on the host return TQ_ERR_INVALID_ARG and launch
  *     nothing.  Bad indices found on the device (a slot or block id outside
  *     the cache, a sequence longer than its block-table row) skip the item and
@@ -103,7 +108,7 @@ enum {
     TQ_DEVERR_BLOCK = 1u << 1,     /* decode: block id outside [0, num_blocks); block skipped */
     TQ_DEVERR_SEQLEN = 1u << 2,    /* decode: seq_len < 0 or > 16*max_blocks_per_seq; clamped */
     TQ_DEVERR_TAIL = 1u << 3,      /* decode: tail_len < 0 or > tail_cap; clamped */
-    TQ_DEVERR_TIMEOUT = 1u << 4,   /* decode: a bounded wait for a staged page gave up; split abandoned */
+    TQ_DEVERR_TIMEOUT = 1u << 4,   /* decode: a bounded wait (2 s) for a staged page gave up; split abandoned */
     TQ_DEVERR_CHUNK = 1u << 5      /* extend: a token row outside every sequence's chunk (cu_q); its output is 0 */
 };
 
@@ -318,6 +323,21 @@ tq_status tq_set_store_small_max(int64_t max_vectors);
  * `stream`; the only synchronising call besides tq_cache_create.
  */
 tq_status tq_get_device_error(const tq_cache* cache, uint32_t* flags, void* stream);
+
+/*
+ * Diagnostic; the pages have no counterpart.  Every wait of the decode kernels
+ * on an mbarrier (a staged page, a tensor-core result) is bounded: after 2 s of
+ * the device's global timer (or 2^26 polls) it gives up, sets
+ * TQ_DEVERR_TIMEOUT, drains its copies in flight and returns, so a stalled
+ * copy becomes an error status instead of a hung GPU.  This call launches one
+ * thread that makes that same wait on an mbarrier nothing ever completes, with
+ * the limit set to limit_us microseconds (1 .. 10^7), and OR-s
+ * TQ_DEVERR_TIMEOUT into *err_word (caller-owned device uint32, 4-byte
+ * aligned) when it gives up.  Asynchronous on `stream`; lets a test check that
+ * a wait that runs out ends its kernel with the error bit set and leaves the
+ * context usable.
+ */
+tq_status tq_check_wait_timeout(uint32_t* err_word, uint32_t limit_us, void* stream);
 
 /*
  * Decode attention that allocates nothing and takes no workspace buffer.

@@ -275,6 +275,21 @@ def test_pack_golden_examples():
         assert list(got) == expect
 
 
+def test_bit_plane_golden_examples():
+    # the bit-sliced layout of key codes and MSE value codes, worked by hand
+    with open(os.path.join(GOLDEN, "bit_plane_examples.txt")) as f:
+        rows = [line.split("|") for line in f if line.strip() and not line.startswith("#")]
+    for bits_s, codes_s, planes_s in rows:
+        bits = int(bits_s)
+        codes = np.array([int(x) for x in codes_s.split()])[None]
+        expect = [bytes.fromhex(p.replace(" ", "")) for p in planes_s.split("/")]
+        got = paged.pack_bit_planes(codes, bits)
+        assert [bytes(p[0]) for p in got] == expect
+        # same bytes per row as the page's stated density (b bits per code)
+        assert sum(len(e) for e in expect) == codes.shape[1] * bits // 8
+        assert np.array_equal(paged.unpack_bit_planes(got, codes.shape[1]), codes)
+
+
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_pack_unpack_round_trip(bits):
     rng = np.random.default_rng(bits)

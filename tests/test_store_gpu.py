@@ -36,12 +36,12 @@ def _run(w, K, V, slots, num_blocks):
     return pages, err
 
 
-def _check(w, K, V, slots, num_blocks, expect_err=0):
+def _check(w, K, V, slots, num_blocks, case, expect_err=0, density_bound=True):
     pages, err = _run(w, K, V, slots, num_blocks)
     assert err == expect_err
     P = _oracle_params(w)
     r = parity.compare_store(pages, P, K, V, slots, w.kv_heads)
-    assert not r["unexplained"], r["unexplained"][:10]
+    parity.check_store(r, case, density_bound)
     # untouched rows stay zero: rebuild the set of written (block,row) pairs
     written = np.zeros((num_blocks, 16), bool)
     s = slots[slots >= 0]
@@ -88,7 +88,7 @@ def test_store_parity_small(case, store_path):
     rng = np.random.default_rng(5)
     slots = rng.permutation(num_blocks * 16)[:T].astype(np.int64)
     slots[rng.choice(T, 7, replace=False)] = -1
-    r = _check(w, K, V, slots, num_blocks)
+    r = _check(w, K, V, slots, num_blocks, f"{name}/{store_path}")
     assert r["checked_bytes"] > 0
 
 
@@ -105,7 +105,7 @@ def test_store_edge_vectors(store_path):
     V[4, :, 7] *= 1e3
     K, V = wl.round_bf16(K), wl.round_bf16(V)
     slots = np.arange(3, 43, dtype=np.int64)  # starts mid-block, ends mid-block
-    _check(w, K, V, slots, 4)
+    _check(w, K, V, slots, 4, f"edge_vectors/{store_path}", density_bound=False)
 
 
 def test_store_skip_and_bad_slot_sets_device_error(store_path):
@@ -121,7 +121,7 @@ def test_store_skip_and_bad_slot_sets_device_error(store_path):
     ok[[5, 6]] = -1
     P = _oracle_params(w)
     r = parity.compare_store(pages, P, K, V, ok, w.kv_heads)
-    assert not r["unexplained"]
+    parity.check_store(r, f"bad_slot/{store_path}")
 
 
 def test_store_zero_tokens_is_noop():
@@ -154,5 +154,5 @@ def test_store_full_size_sampled():
     remap = {int(b): i for i, b in enumerate(blocks.cpu().numpy())}
     sub_slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 for s in slots[pick]], np.int64)
     r = parity.compare_store(sub, P, K[pick], V[pick], sub_slots, w.kv_heads)
-    assert not r["unexplained"], r["unexplained"][:10]
+    parity.check_store(r, "store_64seq_65536tok/sampled1024")
     assert r["checked_bytes"] == 1024 * 8 * (L.page_bytes // 16)

@@ -3,9 +3,12 @@
 It exists for callers that cannot allocate device memory themselves -- an
 engine whose memory manager owns the whole GPU, or code that must not cause the
 synchronisation a cudaMalloc can bring -- and keeps its split-KV scratch in the
-library's static device array instead of a caller workspace.  Its results must
-equal those of tq_decode_attention, call after call, although the array keeps
-whatever the previous call left in it.  This file is collected last on purpose.
+library's static device array instead of a caller workspace.  It runs the same
+kernels on the same inputs as tq_decode_attention, whose work is dealt out and
+reduced in a fixed order, so its outputs must equal that entry point's bit for
+bit, call after call, although the array keeps whatever the previous call left
+in it (a stale scratch read would show up as a difference of any size).  This
+file is collected last on purpose.
 """
 
 import numpy as np
@@ -56,8 +59,9 @@ def _both(c, q, table, lens, tail=None):
 
 
 def _close(got, ref):
-    max_abs, rel = parity.output_errors(got, ref)
-    assert max_abs <= parity.MAX_ABS and rel <= parity.REL_L2, (max_abs, rel)
+    if not np.array_equal(got, ref):
+        max_abs, rel = parity.output_errors(got, ref)
+        raise AssertionError(f"outputs differ: {np.count_nonzero(got != ref)} elements, max-abs {max_abs:.3e}")
 
 
 def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():

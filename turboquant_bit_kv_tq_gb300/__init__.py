@@ -22,7 +22,7 @@ __all__ = [
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
     "tq_get_device_error", "tq_set_store_small_max", "tq_extend_attention", "TQ_DEVERR_CHUNK", "TQCache",
-    "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT",
+    "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT", "tq_check_wait_timeout",
 ]
 
 TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
@@ -37,7 +37,7 @@ EXPORTED = [
     "tq_status_string", "tq_make_codebook", "tq_make_rotation_signs", "tq_make_qjl_matrix", "tq_cache_sizes",
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
     "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
-    "tq_set_store_small_max", "tq_make_uniform_codebook", "tq_extend_attention",
+    "tq_set_store_small_max", "tq_make_uniform_codebook", "tq_extend_attention", "tq_check_wait_timeout",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -117,6 +117,7 @@ def load_library():
                 i32, [_P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
             "tq_get_device_error": (i32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
             "tq_set_store_small_max": (i32, [i64]),
+            "tq_check_wait_timeout": (i32, [_P, ctypes.c_uint32, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -309,6 +310,17 @@ def tq_set_profile_events(handle, kernel, start=None, stop=None):
     split-KV (kernel=1) launch of later calls; None switches it off."""
     ev = lambda e: _P(e.cuda_event) if e is not None else _P()  # noqa: E731
     _check(load_library().tq_set_profile_events(handle, kernel, ev(start), ev(stop)), "tq_set_profile_events")
+
+
+def tq_check_wait_timeout(err_word, limit_us, stream=None):
+    """Make the decode kernels' bounded mbarrier wait run out (nothing ever
+    completes the phase) with a limit of limit_us microseconds; the kernel ORs
+    TQ_DEVERR_TIMEOUT into err_word (a CUDA uint32/int32 tensor of one
+    element) and returns."""
+    if err_word.numel() < 1 or err_word.element_size() != 4:
+        raise ValueError("err_word must hold one 4-byte element")
+    _check(load_library().tq_check_wait_timeout(_dev(err_word, "err_word"), int(limit_us), _stream_ptr(stream)),
+           "tq_check_wait_timeout")
 
 
 def tq_get_device_error(handle, stream=None):

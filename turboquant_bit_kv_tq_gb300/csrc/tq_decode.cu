@@ -10,16 +10,15 @@ namespace tq {
 template <int D>
 static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) {
     const size_t prep_smem = prep_smem_bytes<D>(a.group);
-    static bool prep_attr = false;  // once per head dim, before any capture
     constexpr size_t kPrepMax = prep_smem_bytes<D>(kMaxG);  // the largest head group's need
-    if (!prep_attr) {
-        const tq_status fs = cuda_status_detail(
-            cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepMax),
-            "prep_kernel dynamic shared memory %zu", kPrepMax);
-        if (fs != TQ_OK) return fs;
-        prep_attr = true;
-    }
     if (prep_smem > kPrepMax) return TQ_ERR_UNSUPPORTED;
+    // per-device set-up (the first call on a device does it; before any capture)
+    int sms = 0;
+    {
+        tq_status fs = device_sms(&sms);
+        if (fs == TQ_OK) fs = ensure_dynamic_smem((const void*)prep_kernel<D>, (int)kPrepMax, "prep_kernel");
+        if (fs != TQ_OK) return fs;
+    }
     size_t smem = 0;
     int grid = 0;
     // a uniform key codebook expands over its k_bits single-bit planes only
@@ -34,13 +33,6 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel
-        static int sms = 0;
-        if (sms == 0) {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-                return TQ_ERR_CUDA;
-        }
         const int n_items = a.batch * a.heads * a.gm.nhg * a.sp.n_chunks;
         const int kitems = ws_items_per_cta(n_items, std::min(n_items, kWsCtasPerSm * sms));
         grid = (n_items + kitems - 1) / kitems;  // contiguous runs of kitems items
@@ -109,10 +101,11 @@ tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev
 
 using namespace tq;
 
-extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
-                                         const int32_t* block_table, const int32_t* seq_lens, const void* tail_k,
-                                         const void* tail_v, const int32_t* tail_lens, float scale, int batch,
-                                         void* out, int out_dtype, void* stream) {
+namespace tq {
+
+tq_status decode_args(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
+                      const int32_t* block_table, const int32_t* seq_lens, const void* tail_k, const void* tail_v,
+                      const int32_t* tail_lens, float scale, int batch, void* out, int out_dtype, DecodeArgs* a) {
     if (!c || !q || !cache_buf || !block_table || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
     if (batch < 1 || batch > c->cfg.max_batch) return TQ_ERR_INVALID_ARG;
     if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
@@ -124,45 +117,66 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     if (has_tail && (!tail_k || !tail_v || !tail_lens || c->cfg.tail_cap == 0)) return TQ_ERR_INVALID_ARG;
     if (((uintptr_t)tail_k | (uintptr_t)tail_v) & 15) return TQ_ERR_MISALIGNED;
     if ((uintptr_t)cache_buf & 15) return TQ_ERR_MISALIGNED;
-    DecodeArgs a;
-    a.q = q;
-    a.q_dtype = q_dtype;
-    a.cache = static_cast<const uint8_t*>(cache_buf);
-    a.block_table = block_table;
-    a.seq_lens = seq_lens;
-    a.tail_k = static_cast<const uint16_t*>(tail_k);
-    a.tail_v = static_cast<const uint16_t*>(tail_v);
-    a.tail_lens = tail_lens;
-    a.out = out;
-    a.out_dtype = out_dtype;
-    a.out_rotated = out_rot;
-    a.k_uniform = c->cfg.k_codebook == TQ_CODEBOOK_UNIFORM;
+    a->q = q;
+    a->q_dtype = q_dtype;
+    a->cache = static_cast<const uint8_t*>(cache_buf);
+    a->block_table = block_table;
+    a->seq_lens = seq_lens;
+    a->tail_k = static_cast<const uint16_t*>(tail_k);
+    a->tail_v = static_cast<const uint16_t*>(tail_v);
+    a->tail_lens = tail_lens;
+    a->out = out;
+    a->out_dtype = out_dtype;
+    a->out_rotated = out_rot;
+    a->k_uniform = c->cfg.k_codebook == TQ_CODEBOOK_UNIFORM;
     const int d = c->cfg.head_dim;
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
-    a.scale_log2e = sc * 1.4426950408889634f;
-    a.batch = batch;
-    a.num_blocks = c->cfg.num_blocks;
-    a.heads = c->cfg.num_kv_heads;
-    a.q_heads = c->cfg.num_q_heads;
-    a.group = a.q_heads / a.heads;
-    a.max_blocks = c->cfg.max_blocks_per_seq;
-    a.split_blocks = c->cfg.split_blocks;
-    a.tail_cap = has_tail ? c->cfg.tail_cap : 0;
-    a.sp = c->splits;
-    a.lay = c->lay;
-    a.dp = c->dp;
-    a.gm = c->geom;
-    a.ws_q = c->ws_q;
-    a.ws_bimg = c->ws_bimg;
-    a.ws_cst = c->ws_cst;
-    a.ws_acc = c->ws_acc;
-    a.ws_ml = c->ws_ml;
-    cudaStream_t s = (cudaStream_t)stream;
+    a->scale_log2e = sc * 1.4426950408889634f;
+    a->batch = batch;
+    a->num_blocks = c->cfg.num_blocks;
+    a->heads = c->cfg.num_kv_heads;
+    a->q_heads = c->cfg.num_q_heads;
+    a->group = a->q_heads / a->heads;
+    a->max_blocks = c->cfg.max_blocks_per_seq;
+    a->split_blocks = c->cfg.split_blocks;
+    a->tail_cap = has_tail ? c->cfg.tail_cap : 0;
+    a->sp = c->splits;
+    a->lay = c->lay;
+    a->dp = c->dp;
+    a->gm = c->geom;
+    a->ws_q = c->ws_q;
+    a->ws_bimg = c->ws_bimg;
+    a->ws_cst = c->ws_cst;
+    a->ws_acc = c->ws_acc;
+    a->ws_ml = c->ws_ml;
+    return TQ_OK;
+}
+
+}  // namespace tq
+
+extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
+                                         const int32_t* block_table, const int32_t* seq_lens, const void* tail_k,
+                                         const void* tail_v, const int32_t* tail_lens, float scale, int batch,
+                                         void* out, int out_dtype, void* stream) {
+    DecodeArgs a;
+    const tq_status st = decode_args(c, q, q_dtype, cache_buf, block_table, seq_lens, tail_k, tail_v, tail_lens,
+                                     scale, batch, out, out_dtype, &a);
+    if (st != TQ_OK) return st;
     void *e0 = c->prof_start[TQ_PROF_DECODE_SPLIT], *e1 = c->prof_stop[TQ_PROF_DECODE_SPLIT];
-    return launch_decode(a, s, e0, e1);
+    return launch_decode(a, (cudaStream_t)stream, e0, e1);
 }
 
 namespace tq {
+
+// One thread waits for phase 0 of a shared-memory mbarrier that expects one
+// arrival and gets none, through the decode kernels' bounded wait.
+__global__ void wait_timeout_kernel(uint32_t* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(smem_u32(&bar), 0, err, limit_ns);
+}
 
 // One thread per new token t: find the sequence whose chunk holds row t (the
 // last b with cu_q[b] <= t) and write the token's decode-entry view: compressed
@@ -260,4 +274,11 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
     a.ws_acc = c->ws_acc;
     a.ws_ml = c->ws_ml;
     return launch_decode(a, s, c->prof_start[TQ_PROF_DECODE_SPLIT], c->prof_stop[TQ_PROF_DECODE_SPLIT]);
+}
+
+extern "C" tq_status tq_check_wait_timeout(uint32_t* err_word, uint32_t limit_us, void* stream) {
+    if (!err_word || limit_us == 0 || limit_us > 10000000u) return TQ_ERR_INVALID_ARG;
+    if ((uintptr_t)err_word & 3) return TQ_ERR_MISALIGNED;
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_word, (uint64_t)limit_us * 1000ull);
+    return cuda_status(cudaGetLastError());
 }

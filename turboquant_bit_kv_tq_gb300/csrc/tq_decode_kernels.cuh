@@ -156,11 +156,21 @@ __device__ __forceinline__ float piece_sum(const uint32_t* c) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// bounded mbarrier wait; records TQ_DEVERR_TIMEOUT and returns false if the
-// phase never completes
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+// bounded mbarrier wait: gives up once limit_ns nanoseconds of the device's
+// global timer have passed since the first unsuccessful poll (or after 2^26
+// polls, should the timer not advance), records TQ_DEVERR_TIMEOUT and returns
+// false.  A phase that completes returns true; the first poll reads no timer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every wait of a decode call is microseconds
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    uint64_t t0 = 0;
 #pragma unroll 1
-    for (int it = 0; it < (1 << 24); ++it) {
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -168,6 +178,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
+        const uint64_t now = global_ns();
+        if (it == 0)
+            t0 = now;
+        else if (now - t0 > limit_ns)
+            break;
     }
     set_error(err, TQ_DEVERR_TIMEOUT);
     return false;
@@ -1520,13 +1535,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 template <int D, int KB, bool G32, int VB, int NTH>
 inline tq_status launch_split(const DecodeArgs& a, cudaStream_t s, size_t smem) {
     auto kern = split_kernel<D, KB, G32, VB, NTH>;
-    static bool attr_set = false;  // once per kernel instance, before any capture
-    if (!attr_set) {
-        {
-            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
-            if (fs != TQ_OK) return fs;
-        }
-        attr_set = true;
+    {
+        const tq_status fs = ensure_dynamic_smem((const void*)kern, 227 * 1024, "split_kernel");
+        if (fs != TQ_OK) return fs;
     }
     {
         const cudaError_t e =
@@ -1586,5 +1597,14 @@ inline tq_status split_config(const DecodeArgs& a, int* stages, size_t* smem) {
 // caller's stream.  Defined in tq_decode.cu, the one translation unit that
 // instantiates the prep and combine kernels.
 tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1);
+
+// The argument checks of tq_decode_attention (TQ_ERR_INVALID_ARG or
+// TQ_ERR_MISALIGNED, launching nothing) and the DecodeArgs they describe, with
+// the scratch pointers of the handle's workspace.  Defined in tq_decode.cu; the
+// allocation-free entry point uses it too and then points the scratch
+// elsewhere.
+tq_status decode_args(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
+                      const int32_t* block_table, const int32_t* seq_lens, const void* tail_k, const void* tail_v,
+                      const int32_t* tail_lens, float scale, int batch, void* out, int out_dtype, DecodeArgs* a);
 
 }  // namespace tq

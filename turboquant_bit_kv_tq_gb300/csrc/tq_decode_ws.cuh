@@ -946,13 +946,9 @@ __global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
 template <int D, int KB, bool KU, bool G32, int VB, int NTH>
 inline tq_status launch_split_ws(const DecodeArgs& a, cudaStream_t s, size_t smem, int grid) {
     auto kern = split_ws_kernel<D, KB, KU, G32, VB, NTH>;
-    static bool attr_set = false;  // once per kernel instance, before any capture
-    if (!attr_set) {
-        {
-            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
-            if (fs != TQ_OK) return fs;
-        }
-        attr_set = true;
+    {
+        const tq_status fs = ensure_dynamic_smem((const void*)kern, 227 * 1024, "split_ws_kernel");
+        if (fs != TQ_OK) return fs;
     }
     const cudaError_t e = launch_pdl(a.pdl, kern, dim3(grid), dim3(kWsThreads), smem, s, a);
     if (e != cudaSuccess) {

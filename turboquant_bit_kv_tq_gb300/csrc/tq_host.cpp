@@ -8,7 +8,10 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "tq_internal.h"
@@ -336,6 +339,50 @@ tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...) {
         }
     }
     return TQ_ERR_CUDA;
+}
+
+// Per-device launch state, shared by every host thread: each device's SM
+// count, and the dynamic shared-memory limit already granted to each kernel on
+// each device (cudaFuncSetAttribute acts on the calling thread's current
+// device).  One mutex guards both; a lookup costs one uncontended lock.
+static std::mutex g_dev_mu;
+static std::vector<int> g_dev_sms;
+static std::map<std::pair<int, const void*>, int> g_dev_smem;
+
+static tq_status current_device(int* dev) {
+    const tq_status st = cuda_status(cudaGetDevice(dev));
+    return st != TQ_OK ? st : (*dev < 0 ? TQ_ERR_CUDA : TQ_OK);
+}
+
+tq_status device_sms(int* sms) {
+    int dev = 0;
+    const tq_status st = current_device(&dev);
+    if (st != TQ_OK) return st;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if ((int)g_dev_sms.size() <= dev) g_dev_sms.resize(dev + 1, 0);
+    if (g_dev_sms[dev] <= 0) {
+        int n = 0;
+        const tq_status a = cuda_status(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+        if (a != TQ_OK) return a;
+        if (n <= 0) return TQ_ERR_CUDA;
+        g_dev_sms[dev] = n;
+    }
+    *sms = g_dev_sms[dev];
+    return TQ_OK;
+}
+
+tq_status ensure_dynamic_smem(const void* func, int bytes, const char* name) {
+    int dev = 0;
+    const tq_status st = current_device(&dev);
+    if (st != TQ_OK) return st;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int& granted = g_dev_smem[std::make_pair(dev, func)];
+    if (granted >= bytes) return TQ_OK;
+    const tq_status a = cuda_status_detail(
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+        "%s dynamic shared memory %d on device %d", name, bytes, dev);
+    if (a == TQ_OK) granted = bytes;
+    return a;
 }
 }  // namespace tq
 

@@ -88,6 +88,15 @@ tq_status cuda_status(cudaError_t e);
 // the same, with printf-style context appended to the message
 tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...);
 
+// Per-device launch set-up, safe to call from any host thread, any number of
+// times: the current device's SM count (looked up once per device), and
+// raising `func`'s dynamic shared-memory limit to at least `bytes` on the
+// current device (done once per device and kernel).  Both run on the first
+// call of an entry point on a device, so that call should precede any stream
+// capture on it.
+tq_status device_sms(int* sms);
+tq_status ensure_dynamic_smem(const void* func, int bytes, const char* name);
+
 tq_status compute_layout(const tq_cache_config& c, Layout* lay);
 Splits compute_splits(const tq_cache_config& c);
 ParamsLayout params_layout(const tq_cache_config& c);

@@ -10,6 +10,7 @@
 // memory); for a few vectors, on CUDA cores from S rows in L2.
 
 #include <algorithm>
+#include <atomic>
 
 #include "tq_device.cuh"
 
@@ -484,26 +485,23 @@ __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
 }
 
 // largest vector count for store_small_kernel; negative: 16 x the SM count
-static int64_t g_small_max = -1;
+static std::atomic<int64_t> g_small_max{-1};
 
 template <int D, typename Tin>
 static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1) {
     const size_t smem = StoreBulkLayout<D>::total;
     auto kern = store_kernel<D, Tin>;
-    // one-time setup per kernel instance (before any stream capture)
-    static int sms = 0;
-    if (sms == 0) {
-        {
-            const tq_status fs = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-            if (fs != TQ_OK) return fs;
-        }
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // per-device set-up (the first call on a device does it; before any capture)
+    int sms = 0;
+    {
+        tq_status fs = device_sms(&sms);
+        if (fs == TQ_OK) fs = ensure_dynamic_smem((const void*)kern, (int)smem, "store_kernel");
+        if (fs != TQ_OK) return fs;
     }
     const int64_t nvec = a.num_tokens * a.heads;
+    const int64_t small_max = g_small_max.load(std::memory_order_relaxed);
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
-    if (nvec <= (g_small_max < 0 ? (int64_t)sms * 16 : g_small_max)) {
+    if (nvec <= (small_max < 0 ? (int64_t)sms * 16 : small_max)) {
         // few vectors: one CTA each (no shared copy of S to stage)
         store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
     } else {
@@ -520,7 +518,7 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
 using namespace tq;
 
 extern "C" tq_status tq_set_store_small_max(int64_t max_vectors) {
-    g_small_max = max_vectors < 0 ? -1 : max_vectors;
+    g_small_max.store(max_vectors < 0 ? -1 : max_vectors, std::memory_order_relaxed);
     return TQ_OK;
 }
 
