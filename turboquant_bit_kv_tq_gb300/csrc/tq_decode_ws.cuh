@@ -157,12 +157,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void named_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 // bounded wait that is skipped once the caller has given up (dead)
 __device__ __forceinline__ void ws_wait(uint32_t bar, uint32_t parity, bool& dead, uint32_t* err) {
     if (!dead) dead = !mbar_wait(bar, parity, err);

@@ -101,6 +101,10 @@ ParamsLayout params_layout(const tq_cache_config& c) {
     off = up256(off + 9 * 4);
     p.v_walsh = off;
     off = up256(off + 9 * 4);
+    p.t_hi = off;
+    off = up256(off + d * d * 2);
+    p.t_lo = off;
+    off = up256(off + d * d * 2);
     p.err = off;
     off = up256(off + 4);
     p.total = off;
@@ -174,6 +178,27 @@ static uint16_t bf16_bits_from_double(double x) {
     uint32_t b;
     memcpy(&b, &f, 4);
     return (uint16_t)(b >> 16);
+}
+
+// fp16 bit pattern of a float, round to nearest even (finite inputs of
+// magnitude below 65504; subnormal results included)
+static uint16_t f16_bits(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    x &= 0x7FFFFFFFu;
+    if (x >= 0x477FF000u) return sign | 0x7C00u;  // rounds past the largest fp16: infinity
+    if (x < 0x38800000u) {                         // below 2^-14: a multiple of 2^-24
+        const float m = nearbyintf(fabsf(f) * 16777216.0f);
+        return sign | (uint16_t)m;                  // (m = 1024 encodes 2^-14 exactly)
+    }
+    return sign | (uint16_t)((x + 0x00000FFFu + ((x >> 13) & 1u) - 0x38000000u) >> 13);
+}
+
+static float f16_to_float(uint16_t h) {
+    const uint32_t e = (h >> 10) & 31u, m = h & 1023u;
+    const float v = e == 0 ? ldexpf((float)m, -24) : ldexpf((float)(m | 1024u), (int)e - 25);
+    return (h & 0x8000u) ? -v : v;
 }
 
 static float bf16_to_float(uint16_t b) {
@@ -551,6 +576,31 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     put(pl.v_cent, h->v_cent);
     put(pl.v_bound, h->v_bound);
     walsh_planes(h->k_cent, cfg->k_bits, (float*)(img.data() + pl.k_walsh), cfg->k_codebook == TQ_CODEBOOK_UNIFORM);
+    {
+        // T = S D H / sqrt(d) in fp64 (H_ki = (-1)^popcount(k & i)), split
+        // into fp16 high and low parts
+        uint16_t* thi = (uint16_t*)(img.data() + pl.t_hi);
+        uint16_t* tlo = (uint16_t*)(img.data() + pl.t_lo);
+        std::vector<double> row(d);
+        const double inv = 1.0 / sqrt((double)d);
+        for (int j = 0; j < d; ++j) {
+            for (int k = 0; k < d; ++k) row[k] = (double)bf16_to_float(h->s_bf16[(size_t)j * d + k]) * h->signs[k];
+            // row <- row H (Sylvester H is symmetric: a Walsh-Hadamard transform)
+            for (int len = 1; len < d; len <<= 1)
+                for (int k = 0; k < d; k += 2 * len)
+                    for (int u = k; u < k + len; ++u) {
+                        const double a = row[u], b = row[u + len];
+                        row[u] = a + b;
+                        row[u + len] = a - b;
+                    }
+            for (int i = 0; i < d; ++i) {
+                const double t = row[i] * inv;
+                const uint16_t hb = f16_bits((float)t);
+                thi[(size_t)j * d + i] = hb;
+                tlo[(size_t)j * d + i] = f16_bits((float)(t - (double)f16_to_float(hb)));
+            }
+        }
+    }
     if (cfg->v_mode == TQ_V_MSE)
         walsh_planes(h->v_cent, cfg->v_bits, (float*)(img.data() + pl.v_walsh), cfg->v_codebook == TQ_CODEBOOK_UNIFORM);
     cudaStream_t s = (cudaStream_t)stream;
@@ -571,6 +621,8 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     h->dp.v_bound = (const float*)(base + pl.v_bound);
     h->dp.k_walsh = (const float*)(base + pl.k_walsh);
     h->dp.v_walsh = (const float*)(base + pl.v_walsh);
+    h->dp.t_hi = (const uint16_t*)(base + pl.t_hi);
+    h->dp.t_lo = (const uint16_t*)(base + pl.t_lo);
     h->dp.err = (uint32_t*)(base + pl.err);
     const WorkspaceLayout wl = workspace_layout(*cfg);
     uint8_t* ws = (uint8_t*)workspace_dev;

@@ -37,6 +37,11 @@ struct DeviceParams {
     // code bits in the P-th odd subset (plane_subset); [0] = alpha
     const float* k_walsh;    // [1 + 8]
     const float* v_walsh;    // [1 + 8] (MSE values)
+    // T = S R^T = S D H / sqrt(d) as fp16 high and low parts (T ~ t_hi + t_lo
+    // to ~22 significant bits), row-major [d][d]: the tensor-core store projects
+    // the rotated residual with it (S r = T R r)
+    const uint16_t* t_hi;
+    const uint16_t* t_lo;
     uint32_t* err;           // device error word
 };
 
@@ -56,7 +61,8 @@ struct Splits {
 };
 
 struct ParamsLayout {
-    size_t signs, s_f32, st_f32, s_bf16, st_bf16, k_cent, k_bound, v_cent, v_bound, k_walsh, v_walsh, err, total;
+    size_t signs, s_f32, st_f32, s_bf16, st_bf16, k_cent, k_bound, v_cent, v_bound, k_walsh, v_walsh, t_hi, t_lo, err,
+        total;
 };
 
 // Query-side fp8 pieces of the score contraction: piece k carries the

@@ -11,24 +11,13 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
-#include "tq_device.cuh"
+#include "tq_store.cuh"
 
 namespace tq {
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-struct StoreArgs {
-    const void* k;
-    const void* v;
-    const int64_t* slots;
-    uint8_t* cache;
-    int64_t num_tokens;
-    int64_t num_slots;  // num_blocks * 16
-    int heads;
-    Layout lay;
-    DeviceParams dp;
-};
 
 // Pack codes[0..d) (one byte each, b bits used) into the row's LSB-first
 // bitstream; lanes write whole 32-bit words.
@@ -504,6 +493,10 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
     if (nvec <= (small_max < 0 ? (int64_t)sms * 16 : small_max)) {
         // few vectors: one CTA each (no shared copy of S to stage)
         store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
+    } else if (store_tc_supported(a.lay, std::is_same<Tin, float>::value ? TQ_DTYPE_F32 : TQ_DTYPE_BF16)) {
+        // bulk appends at d = 128 from bf16: tiles of 128 vectors on the tensor cores
+        const tq_status st = launch_store_tc(a, s, sms);
+        if (st != TQ_OK) return st;
     } else {
         constexpr int kPerCta = StoreBulkLayout<D>::kWarps * kStoreNB;  // vectors per CTA pass
         const int grid = (int)std::min<int64_t>((nvec + kPerCta - 1) / kPerCta, (int64_t)sms);

@@ -1,0 +1,537 @@
+// Bulk KV-cache store on the tensor cores (d = 128, bf16 inputs): the same
+// bytes as store_kernel, for appends of many vectors ([Roadmap] §3.1: the WHT
+// rotation and the quantisation fused into the store; [Hub] "Technical
+// principle" steps 1-5; [Paged] "Which path vLLM takes").
+//
+// A tile is 128 consecutive (token, KV head) vectors.  Per tile:
+//   1. the tile's K and V rows land in shared memory (cp.async, 16-byte chunks)
+//      in the tensor cores' K-major layout;
+//   2. tcgen05 MMAs rotate them: Y = X (D H)^T, i.e. y = H D x for every row
+//      (the input is bf16 and D H is +-1, so every product is exact; the sums
+//      accumulate in fp32 in tensor memory);
+//   3. one thread per vector reads its row of Y: the norm n = ||y|| / sqrt(d),
+//      the codes (the number of Lloyd-Max boundaries below y / (n sqrt(d)),
+//      found by comparing |y| against the positive boundaries scaled by
+//      n sqrt(d)), the bit planes, and for keys the rotated residual
+//        r~ = R k - n16 c[idx] = y / sqrt(d) - n16 c[idx]   (= R r)
+//      scaled by a power of two and split into fp16 high and low parts;
+//   4. for keys with QJL, tcgen05 MMAs project it: z = T r~ with
+//      T = S R^T = S D H / sqrt(d) (so z = S r), as T_hi r~_hi + T_hi r~_lo +
+//      T_lo r~_hi (T_hi, T_lo: T's fp16 parts from the cache parameters);
+//      bit j = [z_j >= 0];
+//   5. the thread writes its vector's page rows.
+// Group-32 values skip the rotation: their thread reads its row from shared
+// memory.  Two warpgroups of four warps take alternate tiles, each with its
+// own MMA-issue warp, so one tile's CUDA-core work overlaps the other's MMAs.
+
+#include <algorithm>
+
+#include "tq_store.cuh"
+
+namespace tq {
+
+constexpr int kTcWG = 2;                                  // compute warpgroups per CTA
+constexpr int kTcThreads = 32 * (4 * kTcWG + kTcWG);      // + one MMA-issue warp each
+constexpr float kTcRsd = 0.08838834764831845f;            // 1 / sqrt(128)
+
+struct TcLayout {
+    static constexpr uint32_t x_bytes = 65536;            // per warpgroup: X_k (32 KB) then X_v (32 KB)
+    static constexpr uint32_t mt = kTcWG * x_bytes;       // rotation operand (D H)^T, bf16
+    static constexpr uint32_t th = mt + 32768;            // T high part, fp16
+    static constexpr uint32_t tl = th + 32768;            // T low part, fp16
+    static constexpr uint32_t tab = tl + 32768;           // float tables
+    static constexpr uint32_t bars = tab + 256;           // 4 mbarriers per warpgroup
+    static constexpr uint32_t tslot = bars + 8 * 4 * kTcWG;
+    static constexpr uint32_t total = tslot + 16;
+};
+static_assert(TcLayout::total <= 227 * 1024, "shared memory");
+
+// Byte offset of the 16-byte chunk j (elements 8j .. 8j+7) of row r in the
+// no-swizzle K-major layout: 8-row x 16-byte core matrices, 8-row groups 128 B
+// apart, chunk columns 2048 B apart.  A thread's row is 16 B per chunk and a
+// warp's 32 rows are 512 contiguous bytes.
+__device__ __forceinline__ uint32_t tc_chunk(int r, int j) {
+    return (uint32_t)j * 2048u + ((uint32_t)r >> 3) * 128u + ((uint32_t)r & 7u) * 16u;
+}
+
+// D[128 x 128] (+)= A[128 x 16] B[128 x 16]^T, both operands in shared memory
+// (kind::f16: fp16 or bf16 inputs, fp32 accumulation), issued by one thread
+__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// instruction descriptor: fp32 accumulate, A and B bf16 (or fp16), K-major,
+// M = 128, N = 128
+__host__ __device__ constexpr uint32_t f16kind_idesc(bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((128u >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr) { return smem_desc(addr, 2048, 128); }
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// all ones if a > b, else zero
+__device__ __forceinline__ uint32_t gt_mask(float a, float b) {
+    uint32_t m;
+    asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
+    return m;
+}
+// (w << 1) | top bit of m
+__device__ __forceinline__ uint32_t push_bit(uint32_t w, uint32_t m) { return __funnelshift_l(m, w, 1); }
+__device__ __forceinline__ float sel(uint32_t m, float a, float b) {  // m ? a : b (m all ones or zero)
+    return __uint_as_float((m & __float_as_uint(a)) | (~m & __float_as_uint(b)));
+}
+
+// The NB low bits of cnt = #{positive boundaries below a}, as masks m[q] for
+// bit q (binary search over the 2^NB - 1 sorted positive boundaries T).
+template <int NB>
+__device__ __forceinline__ void cnt_bits(float a, const float* T, uint32_t (&m)[3]) {
+    if constexpr (NB == 1) {
+        m[0] = gt_mask(a, T[0]);
+    } else if constexpr (NB == 2) {
+        m[1] = gt_mask(a, T[1]);
+        m[0] = gt_mask(a, sel(m[1], T[2], T[0]));
+    } else {
+        m[2] = gt_mask(a, T[3]);
+        m[1] = gt_mask(a, sel(m[2], T[5], T[1]));
+        m[0] = gt_mask(a, sel(m[2], sel(m[1], T[6], T[4]), sel(m[1], T[2], T[0])));
+    }
+}
+// G[cnt]: the positive centroid of the cell
+template <int NB>
+__device__ __forceinline__ float cell_value(const uint32_t (&m)[3], const float* G) {
+    if constexpr (NB == 1) {
+        return sel(m[0], G[1], G[0]);
+    } else if constexpr (NB == 2) {
+        return sel(m[1], sel(m[0], G[3], G[2]), sel(m[0], G[1], G[0]));
+    } else {
+        const float lo = sel(m[1], sel(m[0], G[3], G[2]), sel(m[0], G[1], G[0]));
+        const float hi = sel(m[1], sel(m[0], G[7], G[6]), sel(m[0], G[5], G[4]));
+        return sel(m[2], hi, lo);
+    }
+}
+
+// Codes of a symmetric codebook with B bits: idx = 2^(B-1) + cnt for y > 0,
+// 2^(B-1) - 1 - cnt otherwise (cnt = #{positive boundaries below |y|}), i.e.
+// plane B-1 = [y > 0] and plane q < B-1 = bit q of cnt XOR [y <= 0].  The
+// words are built 32 coordinates at a time, highest coordinate first (so
+// coordinate c ends at bit c % 32 of word c / 32).
+template <int B>
+struct PlaneWords {
+    uint32_t w[B][4];
+};
+
+// sum of squares of 128 values: 8 running sums of 16, then a tree
+__device__ __forceinline__ float sumsq128(const float (&y)[128]) {
+    float s[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s[k] = y[k] * y[k];
+#pragma unroll
+    for (int i = 8; i < 128; ++i) s[i & 7] = fmaf(y[i], y[i], s[i & 7]);
+    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
+// the 128 fp32 columns of this thread's lane of tensor memory at `taddr`
+__device__ __forceinline__ void tmem_row128(uint32_t taddr, float (&y)[128]) {
+    uint32_t r[4][32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tmem_ld32(taddr + 32 * q, r[q]);
+    tc_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) y[32 * q + c] = __uint_as_float(r[q][c]);
+}
+
+// MSE codes of a rotated row (values, or keys without QJL): returns the fp32
+// norm; planes in pw.  PB: positive boundaries of the codebook (2^(B-1) - 1).
+template <int B>
+__device__ __forceinline__ float mse_planes(const float (&y)[128], const float* PB, PlaneWords<B>& pw) {
+    constexpr int NB = B - 1;
+    const float n = sqrtf(sumsq128(y) * (1.f / 128.f));
+    float T[7];
+    const float sc = n * 11.313708498984761f;  // n sqrt(d)
+#pragma unroll
+    for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = PB[k] * sc;
+#pragma unroll
+    for (int wd = 3; wd >= 0; --wd) {
+        uint32_t S = 0, C[3] = {0, 0, 0};
+#pragma unroll
+        for (int i = 31; i >= 0; --i) {
+            const float yi = y[32 * wd + i];
+            uint32_t m[3];
+            cnt_bits<NB>(fabsf(yi), T, m);
+            S = push_bit(S, gt_mask(yi, 0.f));
+#pragma unroll
+            for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
+        }
+        pw.w[B - 1][wd] = S;
+#pragma unroll
+        for (int q = 0; q < NB; ++q) pw.w[q][wd] = C[q] ^ ~S;
+    }
+    return n;
+}
+
+template <int B>
+__device__ __forceinline__ void put_planes(uint8_t* base, int row, const PlaneWords<B>& pw) {
+#pragma unroll
+    for (int p = 0; p < B; ++p)
+        *reinterpret_cast<uint4*>(base + (p * kBlock + row) * 16) = make_uint4(pw.w[p][0], pw.w[p][1], pw.w[p][2],
+                                                                                 pw.w[p][3]);
+}
+
+// Group-32 value fields of one row read from shared memory (bf16, canonical
+// layout): zero = fp16(min), scale = fp16((max - min)/(2^VB - 1)),
+// q = clamp(floor((v - zero)/scale + 1/2)); fields in the page's slot order.
+template <int VB>
+__device__ __forceinline__ void g32_row(const uint8_t* xrow_base, int v, uint8_t* codes, uint8_t* meta) {
+    constexpr int top = (1 << VB) - 1;
+    uint32_t words[VB * 4];  // the 128 x VB-bit row: 16 (VB = 4) or 8 (VB = 2) words
+#pragma unroll
+    for (int k = 0; k < VB * 4; ++k) words[k] = 0u;
+    uint32_t mw[4];
+#pragma unroll
+    for (int gr = 0; gr < 4; ++gr) {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(xrow_base + tc_chunk(v, 4 * gr + j));
+            const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * j + 2 * e] = __uint_as_float(ww[e] << 16);
+                x[8 * j + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+        }
+        float lo = x[0], hi = x[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) {
+            lo = fminf(lo, x[i]);
+            hi = fmaxf(hi, x[i]);
+        }
+        const __half z16 = __float2half_rn(lo);
+        const __half s16 = __float2half_rn((hi - lo) / (float)top);
+        const float zf = __half2float(z16), sf = __half2float(s16);
+        mw[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            int q = 0;
+            if (sf > 0.f) {
+                const float t = (x[i] - zf) / sf;
+                const float fl = floorf(t);
+                q = min(max((int)fl + ((t - fl) >= 0.5f ? 1 : 0), 0), top);
+            }
+            // coordinate c = 32 gr + i = 32 (m >> 1) + 4 g + 2 (m & 1) + e
+            const int g = (i >> 2) & 7, m = 2 * gr + ((i >> 1) & 1), e = i & 1;
+            const int slot = 16 * g + 2 * m + e;
+            words[(slot * VB) >> 5] |= (uint32_t)q << ((slot * VB) & 31);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < VB; ++k)
+        *reinterpret_cast<uint4*>(codes + 16 * k) =
+            make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
+    *reinterpret_cast<uint4*>(meta) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+}
+
+// KB: key bits; VG: group-32 values (else MSE); VB: value bits
+template <int KB, bool VG, int VB>
+__global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Layout& L = a.lay;
+    const bool qjl = L.k_qjl;
+    const int64_t nvec = a.num_tokens * a.heads;
+    const int64_t ntiles = (nvec + 127) / 128;
+    float* tab = reinterpret_cast<float*>(smem + TcLayout::tab);
+    float* kpb = tab;        // [7] key positive boundaries
+    float* kpc = tab + 8;    // [8] key positive centroids
+    float* vpb = tab + 16;   // [7] value positive boundaries
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + TcLayout::tslot);
+    uint32_t* err = a.dp.err;
+
+    // ---- set-up: tables, the rotation operand, T's parts; barriers; tensor memory
+    constexpr int kh = 1 << (KB - 1), vh = 1 << (VB - 1);
+    if (tid < kh - 1) kpb[tid] = a.dp.k_bound[kh + tid];
+    if (tid < kh) kpc[tid] = a.dp.k_cent[kh + tid];
+    if (!VG && tid < vh - 1) vpb[tid] = a.dp.v_bound[vh + tid];
+    for (int e = tid; e < 2048; e += blockDim.x) {
+        // (D H)^T as the B operand of the rotation: row i (output), column j:
+        // D_j H_ij, bf16 +-1; T parts: row j (output), column i, fp16
+        const int i = e & 127, j8 = e >> 7;
+        uint32_t wd[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t pr = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 8 * j8 + 2 * u + h;
+                const bool neg = (a.dp.signs[j] < 0.f) != (bool)(__popc(i & j) & 1);
+                pr |= (uint32_t)(neg ? 0xBF80u : 0x3F80u) << (16 * h);
+            }
+            wd[u] = pr;
+        }
+        *reinterpret_cast<uint4*>(smem + TcLayout::mt + tc_chunk(i, j8)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        if (qjl) {
+            *reinterpret_cast<uint4*>(smem + TcLayout::th + tc_chunk(i, j8)) =
+                __ldg(reinterpret_cast<const uint4*>(a.dp.t_hi + i * 128 + 8 * j8));
+            *reinterpret_cast<uint4*>(smem + TcLayout::tl + tc_chunk(i, j8)) =
+                __ldg(reinterpret_cast<const uint4*>(a.dp.t_lo + i * 128 + 8 * j8));
+        }
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 4 * kTcWG; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int g = warp < 4 * kTcWG ? warp >> 2 : warp - 4 * kTcWG;  // this thread's warpgroup
+    uint64_t* xready = &bars[4 * g + 0];  // tile staged (one arrival after the warpgroup's barrier)
+    uint64_t* ydone = &bars[4 * g + 1];   // rotation MMAs done (commit)
+    uint64_t* rready = &bars[4 * g + 2];  // residual pieces staged (as xready)
+    uint64_t* zdone = &bars[4 * g + 3];   // projection MMAs done (commit)
+    const uint32_t xk_s = smem_u32(smem) + g * TcLayout::x_bytes;
+    const uint32_t xv_s = xk_s + 32768;
+    const uint32_t tcol = tmem + 256u * g;  // Y_k: columns 0..127; Y_v, then Z: 128..255
+    const int64_t tstep = (int64_t)gridDim.x * kTcWG;
+    bool dead = false;
+
+    if (warp >= 4 * kTcWG) {
+        // ------------------------------------------------ MMA issue (lane 0)
+        if (lane == 0) {
+            const uint32_t id_bf = f16kind_idesc(true), id_h = f16kind_idesc(false);
+            const uint32_t mt_s = smem_u32(smem) + TcLayout::mt, th_s = smem_u32(smem) + TcLayout::th,
+                           tl_s = smem_u32(smem) + TcLayout::tl;
+            int it = 0, ny = 0, nz = 0;  // tiles begun; commits made on ydone and zdone
+            for (int64_t tile = (int64_t)blockIdx.x * kTcWG + g; tile < ntiles && !dead; tile += tstep, ++it) {
+                dead = !mbar_wait(smem_u32(xready), it & 1, err);
+                if (dead) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s)
+                    mma_f16_ss(tcol, tc_desc(xk_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
+                if constexpr (!VG) {
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s)
+                        mma_f16_ss(tcol + 128, tc_desc(xv_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
+                }
+                tc_commit(smem_u32(ydone));
+                ++ny;
+                if (!qjl) continue;
+                dead = !mbar_wait(smem_u32(rready), it & 1, err);
+                if (dead) break;
+                tc_fence_after();
+                // z = T_hi r_hi + T_hi r_lo + T_lo r_hi (r_hi in X_k, r_lo in X_v)
+#pragma unroll 1
+                for (int s = 0; s < 24; ++s) {
+                    const uint32_t as = (s < 8 || s >= 16 ? xk_s : xv_s) + 4096 * (s & 7);
+                    const uint32_t bs = (s < 16 ? th_s : tl_s) + 4096 * (s & 7);
+                    mma_f16_ss(tcol + 128, tc_desc(as), tc_desc(bs), id_h, s > 0);
+                }
+                tc_commit(smem_u32(zdone));
+                ++nz;
+            }
+            // the last commits must land before tensor memory is freed (bounded
+            // waits, also after a wait above gave up)
+            if (ny > 0) mbar_wait(smem_u32(ydone), (ny - 1) & 1, err);
+            if (nz > 0) mbar_wait(smem_u32(zdone), (nz - 1) & 1, err);
+        }
+    } else {
+        // --------------------------------------------- compute (thread = row)
+        const int v = tid & 127;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        uint8_t* xk = smem + g * TcLayout::x_bytes;
+        uint8_t* xv = xk + 32768;
+        const uint8_t* gk0 = static_cast<const uint8_t*>(a.k);
+        const uint8_t* gv0 = static_cast<const uint8_t*>(a.v);
+        int it = 0;
+        for (int64_t tile = (int64_t)blockIdx.x * kTcWG + g; tile < ntiles; tile += tstep, ++it) {
+            named_sync(1 + g, 128);  // the warpgroup is done with the previous tile's rows
+            const int64_t w0 = tile * 128;
+            const int nv = nvec - w0 < 128 ? (int)(nvec - w0) : 128;
+            const uint8_t* gk = gk0 + w0 * 256;
+            const uint8_t* gv = gv0 + w0 * 256;
+            // 2048 chunks per matrix; a warp's 32 copies cover 8 rows x 4 chunks
+            for (int e = v; e < 2048; e += 128) {
+                const int l = e & 31, grp = e >> 5;
+                const int r = 8 * (grp & 15) + (l & 7), j = 4 * (grp >> 4) + (l >> 3);
+                const bool in = r < nv;
+                cp_async16(xk_s + tc_chunk(r, j), in ? gk + r * 256 + j * 16 : gk0, in ? 16u : 0u);
+                cp_async16(xv_s + tc_chunk(r, j), in ? gv + r * 256 + j * 16 : gv0, in ? 16u : 0u);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            // this row's destination, while the copies fly
+            const bool live = v < nv;
+            int64_t slot = -1;
+            int h = 0;
+            if (live) {
+                const int64_t w = w0 + v;
+                const int64_t t = nvec < ((int64_t)1 << 31) ? (int64_t)((uint32_t)w / (uint32_t)a.heads) : w / a.heads;
+                h = (int)(w - t * a.heads);
+                slot = a.slots[t];
+            }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            named_sync(1 + g, 128);  // every row of the tile is in shared memory
+            if (v == 0) mbar_arrive(smem_u32(xready));
+            if (!dead) dead = !mbar_wait(smem_u32(ydone), it & 1, err);
+            tc_fence_after();
+            const bool ok = live && !dead && slot >= 0 && slot < a.num_slots;
+            if (live && slot != -1 && !(slot >= 0 && slot < a.num_slots) && h == 0) set_error(err, TQ_DEVERR_SLOT);
+            const int row = (int)(slot & 15);
+            uint8_t* page = ok ? a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes : nullptr;
+
+            // ---------------------------------------------------------- value
+            if constexpr (VG) {
+                if (ok) g32_row<VB>(xv, v, page + L.v_codes + row * L.v_code_row, page + L.v_meta + row * 16);
+            } else {
+                float y[128];
+                tmem_row128(tcol + 128 + lane_base, y);
+                PlaneWords<VB> pw;
+                const float n = mse_planes<VB>(y, vpb, pw);
+                if (ok) {
+                    put_planes<VB>(page + L.v_codes, row, pw);
+                    reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
+                }
+            }
+
+            // ------------------------------------------------------------ key
+            {
+                constexpr int NB = KB - 1;
+                float y[128];
+                tmem_row128(tcol + lane_base, y);
+                const float n = sqrtf(sumsq128(y) * (1.f / 128.f));
+                const __half n16 = __float2half_rn(n);
+                float T[7], G[8];
+                const float sc = n * 11.313708498984761f;
+#pragma unroll
+                for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = kpb[k] * sc;
+                // residual scale 2^(7 - e) for n in [2^(e-1), 2^e): the scaled
+                // residual's entries stay well inside fp16's normal range
+                int e2 = 0;
+                frexpf(n, &e2);
+                const float rs = ldexpf(1.f, 7 - e2);
+                const float s1 = rs * kTcRsd;
+                const float cs = __half2float(n16) * rs;
+#pragma unroll
+                for (int k = 0; k < (1 << NB); ++k) G[k] = kpc[k] * cs;
+                PlaneWords<KB> pw;
+                float rr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int wd = 3; wd >= 0; --wd) {
+                    uint32_t S = 0, C[3] = {0, 0, 0};
+#pragma unroll
+                    for (int jj = 3; jj >= 0; --jj) {
+                        const int j = 4 * wd + jj;  // chunk of coordinates 8j .. 8j+7
+                        float r8[8];
+#pragma unroll
+                        for (int i = 7; i >= 0; --i) {
+                            const float yi = y[8 * j + i];
+                            uint32_t m[3];
+                            cnt_bits<NB>(fabsf(yi), T, m);
+                            const uint32_t pos = gt_mask(yi, 0.f);
+                            S = push_bit(S, pos);
+#pragma unroll
+                            for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
+                            // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt] otherwise
+                            const float cneg = __uint_as_float(__float_as_uint(cell_value<NB>(m, G)) ^ (pos & 0x80000000u));
+                            r8[i] = fmaf(yi, s1, cneg);
+                            rr4[i & 3] = fmaf(r8[i], r8[i], rr4[i & 3]);
+                        }
+                        if (qjl) {
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const __half2 hh = __floats2half2_rn(r8[2 * u], r8[2 * u + 1]);
+                                const float2 hf = __half22float2(hh);
+                                const __half2 ll = __floats2half2_rn(r8[2 * u] - hf.x, r8[2 * u + 1] - hf.y);
+                                hi[u] = *reinterpret_cast<const uint32_t*>(&hh);
+                                lo[u] = *reinterpret_cast<const uint32_t*>(&ll);
+                            }
+                            *reinterpret_cast<uint4*>(xk + tc_chunk(v, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *reinterpret_cast<uint4*>(xv + tc_chunk(v, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    }
+                    pw.w[KB - 1][wd] = S;
+#pragma unroll
+                    for (int q = 0; q < NB; ++q) pw.w[q][wd] = C[q] ^ ~S;
+                }
+                if (ok) {
+                    put_planes<KB>(page + L.k_codes, row, pw);
+                    reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
+                }
+                if (qjl) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_before();
+                    named_sync(1 + g, 128);  // every row's residual pieces are in shared memory
+                    if (v == 0) mbar_arrive(smem_u32(rready));
+                    if (!dead) dead = !mbar_wait(smem_u32(zdone), it & 1, err);
+                    tc_fence_after();
+                    float z[128];
+                    tmem_row128(tcol + 128 + lane_base, z);
+                    uint32_t sw[4];
+#pragma unroll
+                    for (int wd = 3; wd >= 0; --wd) {
+                        uint32_t neg = 0;
+#pragma unroll
+                        for (int i = 31; i >= 0; --i) neg = push_bit(neg, __float_as_uint(z[32 * wd + i]));
+                        sw[wd] = ~neg;  // bit j = [z_j >= 0]
+                    }
+                    if (ok && !dead) {
+                        *reinterpret_cast<uint4*>(page + L.k_signs + row * 16) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+                        const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+                        reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(sqrtf(rr) / rs);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int KB, bool VG, int VB>
+static tq_status launch_tc(const StoreArgs& a, cudaStream_t s, int sms) {
+    auto kern = store_tc_kernel<KB, VG, VB>;
+    const tq_status fs = ensure_dynamic_smem((const void*)kern, (int)TcLayout::total, "store_tc_kernel");
+    if (fs != TQ_OK) return fs;
+    const int64_t tiles = (a.num_tokens * a.heads + 127) / 128;
+    const int grid = (int)std::min<int64_t>((tiles + kTcWG - 1) / kTcWG, (int64_t)sms);
+    kern<<<grid, kTcThreads, TcLayout::total, s>>>(a);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int KB>
+static tq_status launch_tc_v(const StoreArgs& a, cudaStream_t s, int sms) {
+    if (a.lay.v_mode == TQ_V_G32) return a.lay.v_bits == 4 ? launch_tc<KB, true, 4>(a, s, sms)
+                                                            : launch_tc<KB, true, 2>(a, s, sms);
+    switch (a.lay.v_bits) {
+        case 2: return launch_tc<KB, false, 2>(a, s, sms);
+        case 3: return launch_tc<KB, false, 3>(a, s, sms);
+        default: return launch_tc<KB, false, 4>(a, s, sms);
+    }
+}
+
+tq_status launch_store_tc(const StoreArgs& a, cudaStream_t s, int sms) {
+    switch (a.lay.k_bits) {
+        case 2: return launch_tc_v<2>(a, s, sms);
+        case 3: return launch_tc_v<3>(a, s, sms);
+        default: return launch_tc_v<4>(a, s, sms);
+    }
+}
+
+}  // namespace tq
