@@ -220,14 +220,18 @@ __device__ __forceinline__ void g32_row(const uint8_t* xrow_base, int v, uint8_t
         const __half s16 = __float2half_rn((hi - lo) / (float)top);
         const float zf = __half2float(z16), sf = __half2float(s16);
         mw[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+        // t = (v - zero) / scale from the correctly rounded reciprocal and one
+        // fma correction (the quotient correctly rounded but for ties of the
+        // rounding itself, one ulp -- below 1e-6 at t <= 15 -- away at most);
+        // a zero scale gives t = 0 and so q = 0
+        const float rs = sf > 0.f ? __frcp_rn(sf) : 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            int q = 0;
-            if (sf > 0.f) {
-                const float t = (x[i] - zf) / sf;
-                const float fl = floorf(t);
-                q = min(max((int)fl + ((t - fl) >= 0.5f ? 1 : 0), 0), top);
-            }
+            const float num = x[i] - zf;
+            const float q0 = num * rs;
+            const float t = fmaf(fmaf(-q0, sf, num), rs, q0);
+            const float fl = floorf(t);
+            const int q = min(max((int)fl + ((t - fl) >= 0.5f ? 1 : 0), 0), top);
             // coordinate c = 32 gr + i = 32 (m >> 1) + 4 g + 2 (m & 1) + e
             const int g = (i >> 2) & 7, m = 2 * gr + ((i >> 1) & 1), e = i & 1;
             const int slot = 16 * g + 2 * m + e;
