@@ -331,7 +331,7 @@ tq_status tq_get_device_error(const tq_cache* cache, uint32_t* flags, void* stre
  * TQ_DEVERR_TIMEOUT, drains its copies in flight and returns, so a stalled
  * copy becomes an error status instead of a hung GPU.  This call launches one
  * thread that makes that same wait on an mbarrier nothing ever completes, with
- * the limit set to limit_us microseconds (1 .. 10^7), and OR-s
+ * the limit set to limit_us microseconds (1 .. 4 * 10^6), and OR-s
  * TQ_DEVERR_TIMEOUT into *err_word (caller-owned device uint32, 4-byte
  * aligned) when it gives up.  Asynchronous on `stream`; lets a test check that
  * a wait that runs out ends its kernel with the error bit set and leaves the

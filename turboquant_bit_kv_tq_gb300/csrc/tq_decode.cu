@@ -170,7 +170,7 @@ namespace tq {
 
 // One thread waits for phase 0 of a shared-memory mbarrier that expects one
 // arrival and gets none, through the decode kernels' bounded wait.
-__global__ void wait_timeout_kernel(uint32_t* err, uint64_t limit_ns) {
+__global__ void wait_timeout_kernel(uint32_t* err, uint32_t limit_ns) {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x != 0) return;
     mbar_init(smem_u32(&bar), 1);
@@ -277,8 +277,8 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
 }
 
 extern "C" tq_status tq_check_wait_timeout(uint32_t* err_word, uint32_t limit_us, void* stream) {
-    if (!err_word || limit_us == 0 || limit_us > 10000000u) return TQ_ERR_INVALID_ARG;
+    if (!err_word || limit_us == 0 || limit_us > 4000000u) return TQ_ERR_INVALID_ARG;
     if ((uintptr_t)err_word & 3) return TQ_ERR_MISALIGNED;
-    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_word, (uint64_t)limit_us * 1000ull);
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_word, limit_us * 1000u);
     return cuda_status(cudaGetLastError());
 }

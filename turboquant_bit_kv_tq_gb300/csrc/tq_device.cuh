@@ -96,36 +96,34 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) { atomicO
 // ------------------------------------------- mbarriers, bulk copies, tcgen05
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// bounded mbarrier wait: gives up once limit_ns nanoseconds of the device's
-// global timer have passed (read every 64 unsuccessful polls, so that a
-// waiting thread issues little beside its polls), or after 2^26 polls should
-// the timer not advance; records TQ_DEVERR_TIMEOUT and returns false.  A phase
-// that completes returns true.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every wait of a store or decode call is microseconds
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+// bounded mbarrier wait: gives up once limit_ns nanoseconds have passed on the
+// low 32 bits of the device's global timer (read every 64 unsuccessful polls;
+// differences taken modulo 2^32, so limits below 4.29 s never see a wrap), or
+// after 2^26 polls should the timer not advance; records TQ_DEVERR_TIMEOUT
+// and returns false.  A phase that completes returns true.
+constexpr uint32_t kWaitLimitNs = 2000000000u;  // 2 s: every wait of a store or decode call is microseconds
+__device__ __forceinline__ uint32_t global_ns_lo() {
+    uint32_t t;
+    asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
     return t;
 }
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-    uint64_t t0 = 0;
+                                          uint32_t limit_ns = kWaitLimitNs) {
+    if (mbar_try(bar, parity)) return true;
+    const uint32_t t0 = global_ns_lo();
 #pragma unroll 1
     for (uint32_t it = 1; it <= (1u << 26); ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((it & 63u) == 0u) {
-            const uint64_t now = global_ns();
-            if (it == 64u)
-                t0 = now;
-            else if (now - t0 > limit_ns)
-                break;
-        }
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63u) == 0u && global_ns_lo() - t0 > limit_ns) break;
     }
     set_error(err, TQ_DEVERR_TIMEOUT);
     return false;
@@ -151,6 +149,9 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 // 32 consecutive 32-bit columns of the calling thread's lane
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]) : "r"(taddr) : "memory");

@@ -64,6 +64,14 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t 
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
 }
+// the same with A (fp16 pairs per 32-bit column) from tensor memory
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
 // instruction descriptor: fp32 accumulate, A and B bf16 (or fp16), K-major,
 // M = 128, N = 128
 __host__ __device__ constexpr uint32_t f16kind_idesc(bool bf16) {
@@ -120,71 +128,73 @@ __device__ __forceinline__ float cell_value(const uint32_t (&m)[3], const float*
 
 // Codes of a symmetric codebook with B bits: idx = 2^(B-1) + cnt for y > 0,
 // 2^(B-1) - 1 - cnt otherwise (cnt = #{positive boundaries below |y|}), i.e.
-// plane B-1 = [y > 0] and plane q < B-1 = bit q of cnt XOR [y <= 0].  The
-// words are built 32 coordinates at a time, highest coordinate first (so
-// coordinate c ends at bit c % 32 of word c / 32).
-template <int B>
-struct PlaneWords {
-    uint32_t w[B][4];
-};
+// plane B-1 = [y > 0] and plane q < B-1 = bit q of cnt XOR [y <= 0].  A word
+// is built from 32 coordinates, highest first (coordinate c ends at bit
+// c % 32 of word c / 32).
 
-// sum of squares of 128 values: 8 running sums of 16, then a tree
-__device__ __forceinline__ float sumsq128(const float (&y)[128]) {
-    float s[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s[k] = y[k] * y[k];
-#pragma unroll
-    for (int i = 8; i < 128; ++i) s[i & 7] = fmaf(y[i], y[i], s[i & 7]);
-    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-}
-
-// the 128 fp32 columns of this thread's lane of tensor memory at `taddr`
-__device__ __forceinline__ void tmem_row128(uint32_t taddr, float (&y)[128]) {
-    uint32_t r[4][32];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) tmem_ld32(taddr + 32 * q, r[q]);
+// 32 consecutive fp32 columns of this thread's lane of tensor memory
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&y)[32]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
     tc_wait_ld();
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) y[32 * q + c] = __uint_as_float(r[q][c]);
+    for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(r[c]);
 }
 
-// MSE codes of a rotated row (values, or keys without QJL): returns the fp32
-// norm; planes in pw.  PB: positive boundaries of the codebook (2^(B-1) - 1).
+// ||y|| / sqrt(128) of the 128 columns at taddr: four loads, eight running
+// sums of 16 squares, then a tree
+__device__ __forceinline__ float row_norm128(uint32_t taddr) {
+    float s[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s[k] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[2][32];
+        tmem_ld32(taddr + 64 * h, r[0]);
+        tmem_ld32(taddr + 64 * h + 32, r[1]);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float y = __uint_as_float(r[q][c]);
+                s[c & 7] = fmaf(y, y, s[c & 7]);
+            }
+    }
+    return sqrtf((((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]))) * (1.f / 128.f));
+}
+
+// MSE codes of the rotated row at taddr (values): the fp32 norm; the plane
+// words go straight to the page's rows (planes at `planes`, row `row`) when
+// `planes` is not null.  PB: the codebook's positive boundaries (2^(B-1) - 1).
 template <int B>
-__device__ __forceinline__ float mse_planes(const float (&y)[128], const float* PB, PlaneWords<B>& pw) {
+__device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uint8_t* planes, int row) {
     constexpr int NB = B - 1;
-    const float n = sqrtf(sumsq128(y) * (1.f / 128.f));
+    const float n = row_norm128(taddr);
     float T[7];
     const float sc = n * 11.313708498984761f;  // n sqrt(d)
 #pragma unroll
     for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = PB[k] * sc;
-#pragma unroll
-    for (int wd = 3; wd >= 0; --wd) {
+#pragma unroll 1
+    for (int wd = 0; wd < 4; ++wd) {
+        float y[32];
+        tmem_row32(taddr + 32 * wd, y);
         uint32_t S = 0, C[3] = {0, 0, 0};
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
-            const float yi = y[32 * wd + i];
             uint32_t m[3];
-            cnt_bits<NB>(fabsf(yi), T, m);
-            S = push_bit(S, gt_mask(yi, 0.f));
+            cnt_bits<NB>(fabsf(y[i]), T, m);
+            S = push_bit(S, gt_mask(y[i], 0.f));
 #pragma unroll
             for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
         }
-        pw.w[B - 1][wd] = S;
+        if (planes) {
+            reinterpret_cast<uint32_t*>(planes + ((B - 1) * kBlock + row) * 16)[wd] = S;
 #pragma unroll
-        for (int q = 0; q < NB; ++q) pw.w[q][wd] = C[q] ^ ~S;
+            for (int q = 0; q < NB; ++q) reinterpret_cast<uint32_t*>(planes + (q * kBlock + row) * 16)[wd] = C[q] ^ ~S;
+        }
     }
     return n;
-}
-
-template <int B>
-__device__ __forceinline__ void put_planes(uint8_t* base, int row, const PlaneWords<B>& pw) {
-#pragma unroll
-    for (int p = 0; p < B; ++p)
-        *reinterpret_cast<uint4*>(base + (p * kBlock + row) * 16) = make_uint4(pw.w[p][0], pw.w[p][1], pw.w[p][2],
-                                                                                 pw.w[p][3]);
 }
 
 // Group-32 value fields of one row read from shared memory (bf16, canonical
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
     if (!VG && tid < vh - 1) vpb[tid] = a.dp.v_bound[vh + tid];
     for (int e = tid; e < 2048; e += blockDim.x) {
         // (D H)^T as the B operand of the rotation: row i (output), column j:
-        // D_j H_ij, bf16 +-1; T parts: row j (output), column i, fp16
+        // D_j H_ij, bf16 +-1; T parts: row i (output), column j8.., fp16
         const int i = e & 127, j8 = e >> 7;
         uint32_t wd[4];
 #pragma unroll
@@ -304,11 +314,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
     const int g = warp < 4 * kTcWG ? warp >> 2 : warp - 4 * kTcWG;  // this thread's warpgroup
     uint64_t* xready = &bars[4 * g + 0];  // tile staged (one arrival after the warpgroup's barrier)
     uint64_t* ydone = &bars[4 * g + 1];   // rotation MMAs done (commit)
-    uint64_t* rready = &bars[4 * g + 2];  // residual pieces staged (as xready)
+    uint64_t* rready = &bars[4 * g + 2];  // residual pieces in tensor memory (as xready)
     uint64_t* zdone = &bars[4 * g + 3];   // projection MMAs done (commit)
     const uint32_t xk_s = smem_u32(smem) + g * TcLayout::x_bytes;
     const uint32_t xv_s = xk_s + 32768;
-    const uint32_t tcol = tmem + 256u * g;  // Y_k: columns 0..127; Y_v, then Z: 128..255
+    // tensor memory of the warpgroup: Y_k in columns 0..127, Y_v in 128..255;
+    // then the key residual's fp16 parts (the projection's A operand) over
+    // Y_v (high 128..191, low 192..255) and the projection z over Y_k
+    const uint32_t tcol = tmem + 256u * g;
     const int64_t tstep = (int64_t)gridDim.x * kTcWG;
     bool dead = false;
 
@@ -337,12 +350,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                 dead = !mbar_wait(smem_u32(rready), it & 1, err);
                 if (dead) break;
                 tc_fence_after();
-                // z = T_hi r_hi + T_hi r_lo + T_lo r_hi (r_hi in X_k, r_lo in X_v)
+                // z = T_hi r_hi + T_hi r_lo + T_lo r_hi, the residual parts
+                // from tensor memory (fp16 pairs: K = 16 is 8 columns)
 #pragma unroll 1
                 for (int s = 0; s < 24; ++s) {
-                    const uint32_t as = (s < 8 || s >= 16 ? xk_s : xv_s) + 4096 * (s & 7);
+                    const uint32_t acol = tcol + 128 + (s >= 8 && s < 16 ? 64 : 0) + 8 * (s & 7);
                     const uint32_t bs = (s < 16 ? th_s : tl_s) + 4096 * (s & 7);
-                    mma_f16_ss(tcol + 128, tc_desc(as), tc_desc(bs), id_h, s > 0);
+                    mma_f16_ts(tcol, acol, tc_desc(bs), id_h, s > 0);
                 }
                 tc_commit(smem_u32(zdone));
                 ++nz;
@@ -356,18 +370,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
         // --------------------------------------------- compute (thread = row)
         const int v = tid & 127;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        uint8_t* xk = smem + g * TcLayout::x_bytes;
-        uint8_t* xv = xk + 32768;
+        const uint32_t yk = tcol + lane_base, yv = tcol + 128 + lane_base;
+        const uint8_t* xv = smem + g * TcLayout::x_bytes + 32768;
         const uint8_t* gk0 = static_cast<const uint8_t*>(a.k);
         const uint8_t* gv0 = static_cast<const uint8_t*>(a.v);
-        int it = 0;
-        for (int64_t tile = (int64_t)blockIdx.x * kTcWG + g; tile < ntiles; tile += tstep, ++it) {
-            named_sync(1 + g, 128);  // the warpgroup is done with the previous tile's rows
+        // cp.async of tile `tile`'s K and V rows: 2048 chunks each; a warp's
+        // 32 copies cover 8 rows x 4 chunks (full 32-byte sectors)
+        auto stage = [&](int64_t tile) {
             const int64_t w0 = tile * 128;
             const int nv = nvec - w0 < 128 ? (int)(nvec - w0) : 128;
             const uint8_t* gk = gk0 + w0 * 256;
             const uint8_t* gv = gv0 + w0 * 256;
-            // 2048 chunks per matrix; a warp's 32 copies cover 8 rows x 4 chunks
+#pragma unroll
             for (int e = v; e < 2048; e += 128) {
                 const int l = e & 31, grp = e >> 5;
                 const int r = 8 * (grp & 15) + (l & 7), j = 4 * (grp >> 4) + (l >> 3);
@@ -376,7 +390,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                 cp_async16(xv_s + tc_chunk(r, j), in ? gv + r * 256 + j * 16 : gv0, in ? 16u : 0u);
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
-            // this row's destination, while the copies fly
+        };
+        int64_t tile = (int64_t)blockIdx.x * kTcWG + g;
+        if (tile < ntiles) stage(tile);
+        int it = 0;
+        for (; tile < ntiles; tile += tstep, ++it) {
+            const int64_t w0 = tile * 128;
+            const int nv = nvec - w0 < 128 ? (int)(nvec - w0) : 128;
+            // this row's destination while the copies land
             const bool live = v < nv;
             int64_t slot = -1;
             int h = 0;
@@ -389,7 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
-            named_sync(1 + g, 128);  // every row of the tile is in shared memory
+            named_sync(1 + g, 128);  // every row of the tile is in shared memory; the last tile's tensor memory is read
             if (v == 0) mbar_arrive(smem_u32(xready));
             if (!dead) dead = !mbar_wait(smem_u32(ydone), it & 1, err);
             tc_fence_after();
@@ -401,23 +422,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
             // ---------------------------------------------------------- value
             if constexpr (VG) {
                 if (ok) g32_row<VB>(xv, v, page + L.v_codes + row * L.v_code_row, page + L.v_meta + row * 16);
+                named_sync(1 + g, 128);  // every row's values are read from shared memory
             } else {
-                float y[128];
-                tmem_row128(tcol + 128 + lane_base, y);
-                PlaneWords<VB> pw;
-                const float n = mse_planes<VB>(y, vpb, pw);
-                if (ok) {
-                    put_planes<VB>(page + L.v_codes, row, pw);
-                    reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
-                }
+                const float n = mse_planes<VB>(yv, vpb, ok ? page + L.v_codes : nullptr, row);
+                if (ok) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
             }
+            // the shared-memory tile is free (the rotation MMAs have read it):
+            // the next tile's rows load while this one is encoded
+            if (tile + tstep < ntiles) stage(tile + tstep);
 
             // ------------------------------------------------------------ key
             {
                 constexpr int NB = KB - 1;
-                float y[128];
-                tmem_row128(tcol + lane_base, y);
-                const float n = sqrtf(sumsq128(y) * (1.f / 128.f));
+                const float n = row_norm128(yk);
                 const __half n16 = __float2half_rn(n);
                 float T[7], G[8];
                 const float sc = n * 11.313708498984761f;
@@ -432,76 +449,73 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                 const float cs = __half2float(n16) * rs;
 #pragma unroll
                 for (int k = 0; k < (1 << NB); ++k) G[k] = kpc[k] * cs;
-                PlaneWords<KB> pw;
+                uint8_t* kplanes = ok ? page + L.k_codes : nullptr;
                 float rr4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int wd = 3; wd >= 0; --wd) {
+#pragma unroll 1
+                for (int wd = 0; wd < 4; ++wd) {
+                    float y[32];
+                    tmem_row32(yk + 32 * wd, y);
                     uint32_t S = 0, C[3] = {0, 0, 0};
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int jj = 3; jj >= 0; --jj) {
-                        const int j = 4 * wd + jj;  // chunk of coordinates 8j .. 8j+7
-                        float r8[8];
+                    for (int i = 31; i >= 0; --i) {
+                        uint32_t m[3];
+                        cnt_bits<NB>(fabsf(y[i]), T, m);
+                        const uint32_t pos = gt_mask(y[i], 0.f);
+                        S = push_bit(S, pos);
 #pragma unroll
-                        for (int i = 7; i >= 0; --i) {
-                            const float yi = y[8 * j + i];
-                            uint32_t m[3];
-                            cnt_bits<NB>(fabsf(yi), T, m);
-                            const uint32_t pos = gt_mask(yi, 0.f);
-                            S = push_bit(S, pos);
-#pragma unroll
-                            for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
-                            // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt] otherwise
-                            const float cneg = __uint_as_float(__float_as_uint(cell_value<NB>(m, G)) ^ (pos & 0x80000000u));
-                            r8[i] = fmaf(yi, s1, cneg);
-                            rr4[i & 3] = fmaf(r8[i], r8[i], rr4[i & 3]);
-                        }
-                        if (qjl) {
-                            uint32_t hi[4], lo[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const __half2 hh = __floats2half2_rn(r8[2 * u], r8[2 * u + 1]);
-                                const float2 hf = __half22float2(hh);
-                                const __half2 ll = __floats2half2_rn(r8[2 * u] - hf.x, r8[2 * u + 1] - hf.y);
-                                hi[u] = *reinterpret_cast<const uint32_t*>(&hh);
-                                lo[u] = *reinterpret_cast<const uint32_t*>(&ll);
-                            }
-                            *reinterpret_cast<uint4*>(xk + tc_chunk(v, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *reinterpret_cast<uint4*>(xv + tc_chunk(v, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        }
+                        for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
+                        // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt] otherwise
+                        const float cneg = __uint_as_float(__float_as_uint(cell_value<NB>(m, G)) ^ (pos & 0x80000000u));
+                        y[i] = fmaf(y[i], s1, cneg);  // the scaled rotated residual
+                        rr4[i & 3] = fmaf(y[i], y[i], rr4[i & 3]);
                     }
-                    pw.w[KB - 1][wd] = S;
+                    if (qjl) {
 #pragma unroll
-                    for (int q = 0; q < NB; ++q) pw.w[q][wd] = C[q] ^ ~S;
+                        for (int u = 0; u < 16; ++u) {
+                            const __half2 hh = __floats2half2_rn(y[2 * u], y[2 * u + 1]);
+                            const float2 hf = __half22float2(hh);
+                            const __half2 ll = __floats2half2_rn(y[2 * u] - hf.x, y[2 * u + 1] - hf.y);
+                            hi[u] = *reinterpret_cast<const uint32_t*>(&hh);
+                            lo[u] = *reinterpret_cast<const uint32_t*>(&ll);
+                        }
+                        tmem_st16(yv + 16 * wd, hi);
+                        tmem_st16(yv + 64 + 16 * wd, lo);
+                    }
+                    if (kplanes) {
+                        reinterpret_cast<uint32_t*>(kplanes + ((KB - 1) * kBlock + row) * 16)[wd] = S;
+#pragma unroll
+                        for (int q = 0; q < NB; ++q)
+                            reinterpret_cast<uint32_t*>(kplanes + (q * kBlock + row) * 16)[wd] = C[q] ^ ~S;
+                    }
                 }
-                if (ok) {
-                    put_planes<KB>(page + L.k_codes, row, pw);
-                    reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
-                }
+                if (ok) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
                 if (qjl) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_wait_st();
                     tc_fence_before();
-                    named_sync(1 + g, 128);  // every row's residual pieces are in shared memory
+                    named_sync(1 + g, 128);  // every row's residual parts are in tensor memory
                     if (v == 0) mbar_arrive(smem_u32(rready));
                     if (!dead) dead = !mbar_wait(smem_u32(zdone), it & 1, err);
                     tc_fence_after();
-                    float z[128];
-                    tmem_row128(tcol + 128 + lane_base, z);
-                    uint32_t sw[4];
-#pragma unroll
-                    for (int wd = 3; wd >= 0; --wd) {
+                    uint32_t* srow = ok && !dead ? reinterpret_cast<uint32_t*>(page + L.k_signs + row * 16) : nullptr;
+#pragma unroll 1
+                    for (int wd = 0; wd < 4; ++wd) {
+                        uint32_t z[32];
+                        tmem_ld32(yk + 32 * wd, z);
+                        tc_wait_ld();
                         uint32_t neg = 0;
 #pragma unroll
-                        for (int i = 31; i >= 0; --i) neg = push_bit(neg, __float_as_uint(z[32 * wd + i]));
-                        sw[wd] = ~neg;  // bit j = [z_j >= 0]
+                        for (int i = 31; i >= 0; --i) neg = push_bit(neg, z[i]);
+                        if (srow) srow[wd] = ~neg;  // bit j = [z_j >= 0]
                     }
-                    if (ok && !dead) {
-                        *reinterpret_cast<uint4*>(page + L.k_signs + row * 16) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+                    if (srow) {
                         const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
                         reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(sqrtf(rr) / rs);
                     }
                 }
             }
         }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
