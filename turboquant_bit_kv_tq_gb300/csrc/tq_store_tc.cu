@@ -40,8 +40,8 @@ struct TcLayout {
     static constexpr uint32_t th = mt + 32768;            // T high part, fp16
     static constexpr uint32_t tl = th + 32768;            // T low part, fp16
     static constexpr uint32_t tab = tl + 32768;           // float tables
-    static constexpr uint32_t bars = tab + 256;           // 4 mbarriers per warpgroup
-    static constexpr uint32_t tslot = bars + 8 * 4 * kTcWG;
+    static constexpr uint32_t bars = tab + 256;           // 5 mbarriers per warpgroup
+    static constexpr uint32_t tslot = bars + 8 * 5 * kTcWG;
     static constexpr uint32_t total = tslot + 16;
 };
 static_assert(TcLayout::total <= 227 * 1024, "shared memory");
@@ -85,52 +85,66 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-// all ones if a > b, else zero
-__device__ __forceinline__ uint32_t gt_mask(float a, float b) {
-    uint32_t m;
-    asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
-    return m;
-}
 // (w << 1) | top bit of m
 __device__ __forceinline__ uint32_t push_bit(uint32_t w, uint32_t m) { return __funnelshift_l(m, w, 1); }
-__device__ __forceinline__ float sel(uint32_t m, float a, float b) {  // m ? a : b (m all ones or zero)
-    return __uint_as_float((m & __float_as_uint(a)) | (~m & __float_as_uint(b)));
+__device__ __forceinline__ uint32_t sel_u(uint32_t m, uint32_t a, uint32_t b) { return (m & a) | (~m & b); }
+__device__ __forceinline__ uint32_t all_if_neg(uint32_t d) { return (uint32_t)((int32_t)d >> 31); }
+
+// Comparisons of non-negative floats as integers: for a = bits(|y|) and
+// t = bits(T) (both below 2^31), t - a has its top bit set iff |y| > T.  cnt =
+// #{positive boundaries below |y|} by a binary search over the 2^NB - 1 sorted
+// positive boundaries T: d[q] has the top bit = bit q of cnt; m[q] the same
+// bit as a full mask.
+template <int NB>
+__device__ __forceinline__ void cnt_bits(uint32_t a, const uint32_t* T, uint32_t (&d)[3], uint32_t (&m)[3]) {
+    if constexpr (NB == 1) {
+        d[0] = T[0] - a;
+        m[0] = all_if_neg(d[0]);
+    } else if constexpr (NB == 2) {
+        d[1] = T[1] - a;
+        m[1] = all_if_neg(d[1]);
+        d[0] = sel_u(m[1], T[2], T[0]) - a;
+        m[0] = all_if_neg(d[0]);
+    } else {
+        d[2] = T[3] - a;
+        m[2] = all_if_neg(d[2]);
+        d[1] = sel_u(m[2], T[5], T[1]) - a;
+        m[1] = all_if_neg(d[1]);
+        d[0] = sel_u(m[2], sel_u(m[1], T[6], T[4]), sel_u(m[1], T[2], T[0])) - a;
+        m[0] = all_if_neg(d[0]);
+    }
+}
+// G[cnt]: the positive centroid of the cell (float bits)
+template <int NB>
+__device__ __forceinline__ uint32_t cell_value(const uint32_t (&m)[3], const uint32_t* G) {
+    if constexpr (NB == 1) {
+        return sel_u(m[0], G[1], G[0]);
+    } else if constexpr (NB == 2) {
+        return sel_u(m[1], sel_u(m[0], G[3], G[2]), sel_u(m[0], G[1], G[0]));
+    } else {
+        const uint32_t lo = sel_u(m[1], sel_u(m[0], G[3], G[2]), sel_u(m[0], G[1], G[0]));
+        const uint32_t hi = sel_u(m[1], sel_u(m[0], G[7], G[6]), sel_u(m[0], G[5], G[4]));
+        return sel_u(m[2], hi, lo);
+    }
 }
 
-// The NB low bits of cnt = #{positive boundaries below a}, as masks m[q] for
-// bit q (binary search over the 2^NB - 1 sorted positive boundaries T).
-template <int NB>
-__device__ __forceinline__ void cnt_bits(float a, const float* T, uint32_t (&m)[3]) {
-    if constexpr (NB == 1) {
-        m[0] = gt_mask(a, T[0]);
-    } else if constexpr (NB == 2) {
-        m[1] = gt_mask(a, T[1]);
-        m[0] = gt_mask(a, sel(m[1], T[2], T[0]));
-    } else {
-        m[2] = gt_mask(a, T[3]);
-        m[1] = gt_mask(a, sel(m[2], T[5], T[1]));
-        m[0] = gt_mask(a, sel(m[2], sel(m[1], T[6], T[4]), sel(m[1], T[2], T[0])));
+// Plane words of 32 coordinates are built from four 8-bit accumulators
+// (coordinates 8q+7 .. 8q pushed, highest first, into accumulator q), joined
+// as bytes: four short dependency chains instead of one of 32.
+struct Bits32 {
+    uint32_t q[4] = {0u, 0u, 0u, 0u};
+    __device__ __forceinline__ void push(int i, uint32_t m) { q[i >> 3] = push_bit(q[i >> 3], m); }
+    __device__ __forceinline__ uint32_t word() const {
+        return __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
     }
-}
-// G[cnt]: the positive centroid of the cell
-template <int NB>
-__device__ __forceinline__ float cell_value(const uint32_t (&m)[3], const float* G) {
-    if constexpr (NB == 1) {
-        return sel(m[0], G[1], G[0]);
-    } else if constexpr (NB == 2) {
-        return sel(m[1], sel(m[0], G[3], G[2]), sel(m[0], G[1], G[0]));
-    } else {
-        const float lo = sel(m[1], sel(m[0], G[3], G[2]), sel(m[0], G[1], G[0]));
-        const float hi = sel(m[1], sel(m[0], G[7], G[6]), sel(m[0], G[5], G[4]));
-        return sel(m[2], hi, lo);
-    }
-}
+};
 
 // Codes of a symmetric codebook with B bits: idx = 2^(B-1) + cnt for y > 0,
 // 2^(B-1) - 1 - cnt otherwise (cnt = #{positive boundaries below |y|}), i.e.
-// plane B-1 = [y > 0] and plane q < B-1 = bit q of cnt XOR [y <= 0].  A word
-// is built from 32 coordinates, highest first (coordinate c ends at bit
-// c % 32 of word c / 32).
+// plane B-1 = [y > 0] and plane q < B-1 = bit q of cnt XOR [y <= 0].  [y > 0]
+// is taken as "sign bit clear" on a non-zero row (a coordinate exactly +0 of a
+// non-zero row is a boundary case; an all-zero row gets [y > 0] = 0 and so
+// the middle-low code, as the definition gives).
 
 // 32 consecutive fp32 columns of this thread's lane of tensor memory
 __device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&y)[32]) {
@@ -171,27 +185,31 @@ template <int B>
 __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uint8_t* planes, int row) {
     constexpr int NB = B - 1;
     const float n = row_norm128(taddr);
-    float T[7];
+    const uint32_t nz = n > 0.f ? 0xFFFFFFFFu : 0u;
+    uint32_t T[7];
     const float sc = n * 11.313708498984761f;  // n sqrt(d)
 #pragma unroll
-    for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = PB[k] * sc;
-#pragma unroll 1
+    for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = __float_as_uint(PB[k] * sc);
+#pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
         float y[32];
         tmem_row32(taddr + 32 * wd, y);
-        uint32_t S = 0, C[3] = {0, 0, 0};
+        Bits32 S, C[NB];
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
-            uint32_t m[3];
-            cnt_bits<NB>(fabsf(y[i]), T, m);
-            S = push_bit(S, gt_mask(y[i], 0.f));
+            const uint32_t yb = __float_as_uint(y[i]);
+            uint32_t d[3], m[3];
+            cnt_bits<NB>(yb & 0x7FFFFFFFu, T, d, m);
+            S.push(i, yb);  // the sign bit
 #pragma unroll
-            for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
+            for (int q = 0; q < NB; ++q) C[q].push(i, d[q]);
         }
         if (planes) {
-            reinterpret_cast<uint32_t*>(planes + ((B - 1) * kBlock + row) * 16)[wd] = S;
+            const uint32_t pos = ~S.word() & nz;  // [y > 0]
+            reinterpret_cast<uint32_t*>(planes + ((B - 1) * kBlock + row) * 16)[wd] = pos;
 #pragma unroll
-            for (int q = 0; q < NB; ++q) reinterpret_cast<uint32_t*>(planes + (q * kBlock + row) * 16)[wd] = C[q] ^ ~S;
+            for (int q = 0; q < NB; ++q)
+                reinterpret_cast<uint32_t*>(planes + (q * kBlock + row) * 16)[wd] = C[q].word() ^ ~pos;
         }
     }
     return n;
@@ -302,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
         }
     }
     if (tid == 0) {
-        for (int b = 0; b < 4 * kTcWG; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        for (int b = 0; b < 5 * kTcWG; ++b) mbar_init(smem_u32(&bars[b]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -312,10 +330,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int g = warp < 4 * kTcWG ? warp >> 2 : warp - 4 * kTcWG;  // this thread's warpgroup
-    uint64_t* xready = &bars[4 * g + 0];  // tile staged (one arrival after the warpgroup's barrier)
-    uint64_t* ydone = &bars[4 * g + 1];   // rotation MMAs done (commit)
-    uint64_t* rready = &bars[4 * g + 2];  // residual pieces in tensor memory (as xready)
-    uint64_t* zdone = &bars[4 * g + 3];   // projection MMAs done (commit)
+    uint64_t* xready = &bars[5 * g + 0];  // tile staged (one arrival after the warpgroup's barrier)
+    uint64_t* ydone = &bars[5 * g + 1];   // key rotation MMAs done (commit)
+    uint64_t* rready = &bars[5 * g + 2];  // residual pieces in tensor memory (as xready)
+    uint64_t* zdone = &bars[5 * g + 3];   // projection MMAs done (commit)
+    uint64_t* vdone = &bars[5 * g + 4];   // value rotation MMAs done (commit; MSE values)
     const uint32_t xk_s = smem_u32(smem) + g * TcLayout::x_bytes;
     const uint32_t xv_s = xk_s + 32768;
     // tensor memory of the warpgroup: Y_k in columns 0..127, Y_v in 128..255;
@@ -331,19 +350,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
             const uint32_t id_bf = f16kind_idesc(true), id_h = f16kind_idesc(false);
             const uint32_t mt_s = smem_u32(smem) + TcLayout::mt, th_s = smem_u32(smem) + TcLayout::th,
                            tl_s = smem_u32(smem) + TcLayout::tl;
-            int it = 0, ny = 0, nz = 0;  // tiles begun; commits made on ydone and zdone
+            int it = 0, ny = 0, nz = 0, nvd = 0;  // tiles begun; commits made on ydone, zdone, vdone
             for (int64_t tile = (int64_t)blockIdx.x * kTcWG + g; tile < ntiles && !dead; tile += tstep, ++it) {
                 dead = !mbar_wait(smem_u32(xready), it & 1, err);
                 if (dead) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int s = 0; s < 8; ++s)
-                    mma_f16_ss(tcol, tc_desc(xk_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
+                // values first (their encoding starts while the keys rotate)
                 if constexpr (!VG) {
 #pragma unroll 1
                     for (int s = 0; s < 8; ++s)
                         mma_f16_ss(tcol + 128, tc_desc(xv_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
+                    tc_commit(smem_u32(vdone));
+                    ++nvd;
                 }
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s)
+                    mma_f16_ss(tcol, tc_desc(xk_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
                 tc_commit(smem_u32(ydone));
                 ++ny;
                 if (!qjl) continue;
@@ -363,6 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
             }
             // the last commits must land before tensor memory is freed (bounded
             // waits, also after a wait above gave up)
+            if (nvd > 0) mbar_wait(smem_u32(vdone), (nvd - 1) & 1, err);
             if (ny > 0) mbar_wait(smem_u32(ydone), (ny - 1) & 1, err);
             if (nz > 0) mbar_wait(smem_u32(zdone), (nz - 1) & 1, err);
         }
@@ -412,21 +435,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
             tc_fence_before();
             named_sync(1 + g, 128);  // every row of the tile is in shared memory; the last tile's tensor memory is read
             if (v == 0) mbar_arrive(smem_u32(xready));
-            if (!dead) dead = !mbar_wait(smem_u32(ydone), it & 1, err);
-            tc_fence_after();
-            const bool ok = live && !dead && slot >= 0 && slot < a.num_slots;
+            const bool ok = live && slot >= 0 && slot < a.num_slots;
             if (live && slot != -1 && !(slot >= 0 && slot < a.num_slots) && h == 0) set_error(err, TQ_DEVERR_SLOT);
             const int row = (int)(slot & 15);
             uint8_t* page = ok ? a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes : nullptr;
 
             // ---------------------------------------------------------- value
             if constexpr (VG) {
+                // (from shared memory, while the keys rotate)
                 if (ok) g32_row<VB>(xv, v, page + L.v_codes + row * L.v_code_row, page + L.v_meta + row * 16);
                 named_sync(1 + g, 128);  // every row's values are read from shared memory
             } else {
-                const float n = mse_planes<VB>(yv, vpb, ok ? page + L.v_codes : nullptr, row);
-                if (ok) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
+                if (!dead) dead = !mbar_wait(smem_u32(vdone), it & 1, err);
+                tc_fence_after();
+                const float n = mse_planes<VB>(yv, vpb, ok && !dead ? page + L.v_codes : nullptr, row);
+                if (ok && !dead) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
             }
+            if (!dead) dead = !mbar_wait(smem_u32(ydone), it & 1, err);
+            tc_fence_after();
             // the shared-memory tile is free (the rotation MMAs have read it):
             // the next tile's rows load while this one is encoded
             if (tile + tstep < ntiles) stage(tile + tstep);
@@ -449,24 +475,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                 const float cs = __half2float(n16) * rs;
 #pragma unroll
                 for (int k = 0; k < (1 << NB); ++k) G[k] = kpc[k] * cs;
-                uint8_t* kplanes = ok ? page + L.k_codes : nullptr;
+                uint8_t* kplanes = ok && !dead ? page + L.k_codes : nullptr;
+                const uint32_t nz = n > 0.f ? 0xFFFFFFFFu : 0u;
+                uint32_t Tb[7], Gb[8];
+#pragma unroll
+                for (int k = 0; k < (1 << NB) - 1; ++k) Tb[k] = __float_as_uint(T[k]);
+#pragma unroll
+                for (int k = 0; k < (1 << NB); ++k) Gb[k] = __float_as_uint(G[k]);
                 float rr4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
                 for (int wd = 0; wd < 4; ++wd) {
                     float y[32];
                     tmem_row32(yk + 32 * wd, y);
-                    uint32_t S = 0, C[3] = {0, 0, 0};
+                    Bits32 S, C[NB];
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int i = 31; i >= 0; --i) {
-                        uint32_t m[3];
-                        cnt_bits<NB>(fabsf(y[i]), T, m);
-                        const uint32_t pos = gt_mask(y[i], 0.f);
-                        S = push_bit(S, pos);
+                        const uint32_t yb = __float_as_uint(y[i]);
+                        uint32_t d[3], m[3];
+                        cnt_bits<NB>(yb & 0x7FFFFFFFu, Tb, d, m);
+                        S.push(i, yb);
 #pragma unroll
-                        for (int q = 0; q < NB; ++q) C[q] = push_bit(C[q], m[q]);
-                        // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt] otherwise
-                        const float cneg = __uint_as_float(__float_as_uint(cell_value<NB>(m, G)) ^ (pos & 0x80000000u));
+                        for (int q = 0; q < NB; ++q) C[q].push(i, d[q]);
+                        // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt]
+                        // otherwise, i.e. -c takes the sign bit of y flipped
+                        const float cneg = __uint_as_float(cell_value<NB>(m, Gb) ^ (~yb & 0x80000000u));
                         y[i] = fmaf(y[i], s1, cneg);  // the scaled rotated residual
                         rr4[i & 3] = fmaf(y[i], y[i], rr4[i & 3]);
                     }
@@ -483,13 +516,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                         tmem_st16(yv + 64 + 16 * wd, lo);
                     }
                     if (kplanes) {
-                        reinterpret_cast<uint32_t*>(kplanes + ((KB - 1) * kBlock + row) * 16)[wd] = S;
+                        const uint32_t pos = ~S.word() & nz;  // [y > 0]
+                        reinterpret_cast<uint32_t*>(kplanes + ((KB - 1) * kBlock + row) * 16)[wd] = pos;
 #pragma unroll
                         for (int q = 0; q < NB; ++q)
-                            reinterpret_cast<uint32_t*>(kplanes + (q * kBlock + row) * 16)[wd] = C[q] ^ ~S;
+                            reinterpret_cast<uint32_t*>(kplanes + (q * kBlock + row) * 16)[wd] = C[q].word() ^ ~pos;
                     }
                 }
-                if (ok) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
+                if (ok && !dead) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
                 if (qjl) {
                     tc_wait_st();
                     tc_fence_before();
@@ -498,15 +532,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                     if (!dead) dead = !mbar_wait(smem_u32(zdone), it & 1, err);
                     tc_fence_after();
                     uint32_t* srow = ok && !dead ? reinterpret_cast<uint32_t*>(page + L.k_signs + row * 16) : nullptr;
-#pragma unroll 1
+#pragma unroll
                     for (int wd = 0; wd < 4; ++wd) {
                         uint32_t z[32];
                         tmem_ld32(yk + 32 * wd, z);
                         tc_wait_ld();
-                        uint32_t neg = 0;
+                        Bits32 neg;
 #pragma unroll
-                        for (int i = 31; i >= 0; --i) neg = push_bit(neg, z[i]);
-                        if (srow) srow[wd] = ~neg;  // bit j = [z_j >= 0]
+                        for (int i = 31; i >= 0; --i) neg.push(i, z[i]);
+                        if (srow) srow[wd] = ~neg.word();  // bit j = [z_j >= 0]
                     }
                     if (srow) {
                         const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
