@@ -190,6 +190,7 @@ __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uin
     const float sc = n * 11.313708498984761f;  // n sqrt(d)
 #pragma unroll
     for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = __float_as_uint(PB[k] * sc);
+    uint32_t W[B][4];
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
         float y[32];
@@ -204,13 +205,15 @@ __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uin
 #pragma unroll
             for (int q = 0; q < NB; ++q) C[q].push(i, d[q]);
         }
-        if (planes) {
-            const uint32_t pos = ~S.word() & nz;  // [y > 0]
-            reinterpret_cast<uint32_t*>(planes + ((B - 1) * kBlock + row) * 16)[wd] = pos;
+        const uint32_t pos = ~S.word() & nz;  // [y > 0]
+        W[B - 1][wd] = pos;
 #pragma unroll
-            for (int q = 0; q < NB; ++q)
-                reinterpret_cast<uint32_t*>(planes + (q * kBlock + row) * 16)[wd] = C[q].word() ^ ~pos;
-        }
+        for (int q = 0; q < NB; ++q) W[q][wd] = C[q].word() ^ ~pos;
+    }
+    if (planes) {
+#pragma unroll
+        for (int p = 0; p < B; ++p)
+            *reinterpret_cast<uint4*>(planes + (p * kBlock + row) * 16) = make_uint4(W[p][0], W[p][1], W[p][2], W[p][3]);
     }
     return n;
 }
@@ -483,6 +486,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
 #pragma unroll
                 for (int k = 0; k < (1 << NB); ++k) Gb[k] = __float_as_uint(G[k]);
                 float rr4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t KW[KB][4];
 #pragma unroll
                 for (int wd = 0; wd < 4; ++wd) {
                     float y[32];
@@ -515,13 +519,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                         tmem_st16(yv + 16 * wd, hi);
                         tmem_st16(yv + 64 + 16 * wd, lo);
                     }
-                    if (kplanes) {
-                        const uint32_t pos = ~S.word() & nz;  // [y > 0]
-                        reinterpret_cast<uint32_t*>(kplanes + ((KB - 1) * kBlock + row) * 16)[wd] = pos;
+                    const uint32_t pos = ~S.word() & nz;  // [y > 0]
+                    KW[KB - 1][wd] = pos;
 #pragma unroll
-                        for (int q = 0; q < NB; ++q)
-                            reinterpret_cast<uint32_t*>(kplanes + (q * kBlock + row) * 16)[wd] = C[q].word() ^ ~pos;
-                    }
+                    for (int q = 0; q < NB; ++q) KW[q][wd] = C[q].word() ^ ~pos;
+                }
+                if (kplanes) {
+#pragma unroll
+                    for (int p = 0; p < KB; ++p)
+                        *reinterpret_cast<uint4*>(kplanes + (p * kBlock + row) * 16) =
+                            make_uint4(KW[p][0], KW[p][1], KW[p][2], KW[p][3]);
                 }
                 if (ok && !dead) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
                 if (qjl) {
@@ -531,7 +538,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                     if (v == 0) mbar_arrive(smem_u32(rready));
                     if (!dead) dead = !mbar_wait(smem_u32(zdone), it & 1, err);
                     tc_fence_after();
-                    uint32_t* srow = ok && !dead ? reinterpret_cast<uint32_t*>(page + L.k_signs + row * 16) : nullptr;
+                    uint32_t sw[4];
 #pragma unroll
                     for (int wd = 0; wd < 4; ++wd) {
                         uint32_t z[32];
@@ -540,9 +547,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                         Bits32 neg;
 #pragma unroll
                         for (int i = 31; i >= 0; --i) neg.push(i, z[i]);
-                        if (srow) srow[wd] = ~neg.word();  // bit j = [z_j >= 0]
+                        sw[wd] = ~neg.word();  // bit j = [z_j >= 0]
                     }
-                    if (srow) {
+                    if (ok && !dead) {
+                        *reinterpret_cast<uint4*>(page + L.k_signs + row * 16) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
                         const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
                         reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(sqrtf(rr) / rs);
                     }
