@@ -347,6 +347,13 @@ tq_status cuda_status(cudaError_t e) {
     snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     return TQ_ERR_CUDA;
 }
+tq_status driver_failure(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_cuda_msg, sizeof g_cuda_msg, fmt, ap);
+    va_end(ap);
+    return TQ_ERR_CUDA;
+}
 tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...) {
     if (cuda_status(e) == TQ_OK) return TQ_OK;
     const size_t n = strlen(g_cuda_msg);

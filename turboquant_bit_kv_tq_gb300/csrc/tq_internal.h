@@ -93,6 +93,8 @@ struct WorkspaceLayout {
 tq_status cuda_status(cudaError_t e);
 // the same, with printf-style context appended to the message
 tq_status cuda_status_detail(cudaError_t e, const char* fmt, ...);
+// TQ_ERR_CUDA with a printf-style message for a failed driver-level step
+tq_status driver_failure(const char* fmt, ...);
 
 // Per-device launch set-up, safe to call from any host thread, any number of
 // times: the current device's SM count (looked up once per device), and

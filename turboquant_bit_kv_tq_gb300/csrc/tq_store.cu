@@ -493,7 +493,7 @@ static tq_status launch(const StoreArgs& a, cudaStream_t s, void* ev0, void* ev1
     if (nvec <= (small_max < 0 ? (int64_t)sms * 16 : small_max)) {
         // few vectors: one CTA each (no shared copy of S to stage)
         store_small_kernel<D, Tin><<<(unsigned)nvec, D, 0, s>>>(a);
-    } else if (store_tc_supported(a.lay, std::is_same<Tin, float>::value ? TQ_DTYPE_F32 : TQ_DTYPE_BF16)) {
+    } else if (store_tc_supported(a, std::is_same<Tin, float>::value ? TQ_DTYPE_F32 : TQ_DTYPE_BF16)) {
         // bulk appends at d = 128 from bf16: tiles of 128 vectors on the tensor cores
         const tq_status st = launch_store_tc(a, s, sms);
         if (st != TQ_OK) return st;

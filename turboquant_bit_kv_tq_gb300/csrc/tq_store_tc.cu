@@ -4,8 +4,10 @@
 // principle" steps 1-5; [Paged] "Which path vLLM takes").
 //
 // A tile is 128 consecutive (token, KV head) vectors.  Per tile:
-//   1. the tile's K and V rows land in shared memory (cp.async, 16-byte chunks)
-//      in the tensor cores' K-major layout;
+//   1. the tile's K and V rows land in shared memory by bulk-tensor copies
+//      (16 boxes of 8 elements x 128 rows each) in the tensor cores' K-major
+//      layout, issued by the MMA warp as soon as the last tile's rotation
+//      MMAs have read the buffer;
 //   2. tcgen05 MMAs rotate them: Y = X (D H)^T, i.e. y = H D x for every row
 //      (the input is bf16 and D H is +-1, so every product is exact; the sums
 //      accumulate in fp32 in tensor memory);
@@ -15,7 +17,8 @@
 //      n sqrt(d)), the bit planes, and for keys the rotated residual
 //        r~ = R k - n16 c[idx] = y / sqrt(d) - n16 c[idx]   (= R r)
 //      scaled by a power of two and split into fp16 high and low parts;
-//   4. for keys with QJL, tcgen05 MMAs project it: z = T r~ with
+//   4. for keys with QJL, tcgen05 MMAs project it word by word (32
+//      coordinates, as the threads finish them): z = T r~ with
 //      T = S R^T = S D H / sqrt(d) (so z = S r), as T_hi r~_hi + T_hi r~_lo +
 //      T_lo r~_hi (T_hi, T_lo: T's fp16 parts from the cache parameters);
 //      bit j = [z_j >= 0];
@@ -24,7 +27,14 @@
 // memory.  Two warpgroups of four warps take alternate tiles, each with its
 // own MMA-issue warp, so one tile's CUDA-core work overlaps the other's MMAs.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <dlfcn.h>
+
 #include <algorithm>
+#include <cstdio>
+#include <mutex>
 
 #include "tq_store.cuh"
 
@@ -33,6 +43,7 @@ namespace tq {
 constexpr int kTcWG = 2;                                  // compute warpgroups per CTA
 constexpr int kTcThreads = 32 * (4 * kTcWG + kTcWG);      // + one MMA-issue warp each
 constexpr float kTcRsd = 0.08838834764831845f;            // 1 / sqrt(128)
+constexpr int kTcBars = 10;                               // mbarriers per warpgroup
 
 struct TcLayout {
     static constexpr uint32_t x_bytes = 65536;            // per warpgroup: X_k (32 KB) then X_v (32 KB)
@@ -40,8 +51,8 @@ struct TcLayout {
     static constexpr uint32_t th = mt + 32768;            // T high part, fp16
     static constexpr uint32_t tl = th + 32768;            // T low part, fp16
     static constexpr uint32_t tab = tl + 32768;           // float tables
-    static constexpr uint32_t bars = tab + 256;           // 5 mbarriers per warpgroup
-    static constexpr uint32_t tslot = bars + 8 * 5 * kTcWG;
+    static constexpr uint32_t bars = tab + 256;           // kTcBars mbarriers per warpgroup
+    static constexpr uint32_t tslot = bars + 8 * kTcBars * kTcWG;
     static constexpr uint32_t total = tslot + 16;
 };
 static_assert(TcLayout::total <= 227 * 1024, "shared memory");
@@ -79,11 +90,6 @@ __host__ __device__ constexpr uint32_t f16kind_idesc(bool bf16) {
            ((128u >> 4) << 24);
 }
 __device__ __forceinline__ uint64_t tc_desc(uint32_t addr) { return smem_desc(addr, 2048, 128); }
-
-// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
 
 // (w << 1) | top bit of m
 __device__ __forceinline__ uint32_t push_bit(uint32_t w, uint32_t m) { return __funnelshift_l(m, w, 1); }
@@ -276,9 +282,21 @@ __device__ __forceinline__ void g32_row(const uint8_t* xrow_base, int v, uint8_t
     *reinterpret_cast<uint4*>(meta) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
 }
 
-// KB: key bits; VG: group-32 values (else MSE); VB: value bits
+// 2-D tiled bulk-tensor load: the box at (x, y) of the map into shared memory
+// at dst, completing on the mbarrier bar (transaction bytes)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// KB: key bits; VG: group-32 values (else MSE); VB: value bits.  mk, mv: the
+// K and V rows ([vectors][128] bf16) as 2-D maps with 8 x 128 boxes, so that
+// box j of a tile lands as chunk column j of the K-major layout.
 template <int KB, bool VG, int VB>
-__global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    store_tc_kernel(StoreArgs a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Layout& L = a.lay;
@@ -323,7 +341,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
         }
     }
     if (tid == 0) {
-        for (int b = 0; b < 5 * kTcWG; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        for (int g = 0; g < kTcWG; ++g) {
+            uint64_t* b = &bars[kTcBars * g];
+            for (int k = 0; k < 4; ++k) mbar_init(smem_u32(&b[k]), 1);  // xfull, ydone, zdone, vdone
+            for (int k = 4; k < kTcBars; ++k) mbar_init(smem_u32(&b[k]), 4);  // xfree, tfree, rready[4]
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -333,64 +355,92 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int g = warp < 4 * kTcWG ? warp >> 2 : warp - 4 * kTcWG;  // this thread's warpgroup
-    uint64_t* xready = &bars[5 * g + 0];  // tile staged (one arrival after the warpgroup's barrier)
-    uint64_t* ydone = &bars[5 * g + 1];   // key rotation MMAs done (commit)
-    uint64_t* rready = &bars[5 * g + 2];  // residual pieces in tensor memory (as xready)
-    uint64_t* zdone = &bars[5 * g + 3];   // projection MMAs done (commit)
-    uint64_t* vdone = &bars[5 * g + 4];   // value rotation MMAs done (commit; MSE values)
+    uint64_t* wb = &bars[kTcBars * g];
+    const uint32_t xfull = smem_u32(&wb[0]);   // tile's K and V rows landed (transaction bytes)
+    const uint32_t ydone = smem_u32(&wb[1]);   // key rotation MMAs done (commit)
+    const uint32_t zdone = smem_u32(&wb[2]);   // projection MMAs done (commit)
+    const uint32_t vdone = smem_u32(&wb[3]);   // value rotation MMAs done (commit; MSE values)
+    const uint32_t xfree = smem_u32(&wb[4]);   // X_v read by the compute warps (group-32 values; one arrival per warp)
+    const uint32_t tfree = smem_u32(&wb[5]);   // tile's tensor memory read (one arrival per warp)
+    const uint32_t rready0 = smem_u32(&wb[6]); // + 8 wd: residual parts of word wd in tensor memory (per warp)
     const uint32_t xk_s = smem_u32(smem) + g * TcLayout::x_bytes;
     const uint32_t xv_s = xk_s + 32768;
     // tensor memory of the warpgroup: Y_k in columns 0..127, Y_v in 128..255;
-    // then the key residual's fp16 parts (the projection's A operand) over
-    // Y_v (high 128..191, low 192..255) and the projection z over Y_k
+    // word wd of the key residual's fp16 parts (the projection's A operand)
+    // goes over Y_k's columns 32 wd .. 32 wd + 31 once they are read (high
+    // half first), and the projection z over Y_v
     const uint32_t tcol = tmem + 256u * g;
     const int64_t tstep = (int64_t)gridDim.x * kTcWG;
     bool dead = false;
 
     if (warp >= 4 * kTcWG) {
-        // ------------------------------------------------ MMA issue (lane 0)
+        // ------------------------------------------------ MMA and copy issue (lane 0)
         if (lane == 0) {
             const uint32_t id_bf = f16kind_idesc(true), id_h = f16kind_idesc(false);
             const uint32_t mt_s = smem_u32(smem) + TcLayout::mt, th_s = smem_u32(smem) + TcLayout::th,
                            tl_s = smem_u32(smem) + TcLayout::tl;
-            int it = 0, ny = 0, nz = 0, nvd = 0;  // tiles begun; commits made on ydone, zdone, vdone
-            for (int64_t tile = (int64_t)blockIdx.x * kTcWG + g; tile < ntiles && !dead; tile += tstep, ++it) {
-                dead = !mbar_wait(smem_u32(xready), it & 1, err);
-                if (dead) break;
+            int nx = 0, it = 0, ny = 0, nz = 0, nvd = 0;  // loads issued; tiles begun; commits on ydone, zdone, vdone
+            auto load_x = [&](int64_t tile) {
+                const int y = (int)(tile * 128);
+                mbar_expect_tx(xfull, 65536u);
+#pragma unroll 1
+                for (int j = 0; j < 16; ++j) {
+                    tma_load_2d(xk_s + 2048 * j, &mk, 8 * j, y, xfull);
+                    tma_load_2d(xv_s + 2048 * j, &mv, 8 * j, y, xfull);
+                }
+                ++nx;
+            };
+            int64_t tile = (int64_t)blockIdx.x * kTcWG + g;
+            if (tile < ntiles) load_x(tile);
+            for (; tile < ntiles && !dead; tile += tstep, ++it) {
+                // the compute warps are done with the last tile's tensor memory
+                if (it > 0 && (dead = !mbar_wait(tfree, (it - 1) & 1, err))) break;
+                if ((dead = !mbar_wait(xfull, it & 1, err))) break;
                 tc_fence_after();
                 // values first (their encoding starts while the keys rotate)
                 if constexpr (!VG) {
 #pragma unroll 1
                     for (int s = 0; s < 8; ++s)
                         mma_f16_ss(tcol + 128, tc_desc(xv_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
-                    tc_commit(smem_u32(vdone));
+                    tc_commit(vdone);
                     ++nvd;
                 }
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s)
                     mma_f16_ss(tcol, tc_desc(xk_s + 4096 * s), tc_desc(mt_s + 4096 * s), id_bf, s > 0);
-                tc_commit(smem_u32(ydone));
+                tc_commit(ydone);
                 ++ny;
+                // the next tile's rows load once the MMAs (and, for group-32
+                // values, the compute warps) have read this one's
+                if ((dead = !mbar_wait(ydone, it & 1, err))) break;
+                if (VG && (dead = !mbar_wait(xfree, it & 1, err))) break;
+                if (tile + tstep < ntiles) load_x(tile + tstep);
                 if (!qjl) continue;
-                dead = !mbar_wait(smem_u32(rready), it & 1, err);
-                if (dead) break;
-                tc_fence_after();
-                // z = T_hi r_hi + T_hi r_lo + T_lo r_hi, the residual parts
-                // from tensor memory (fp16 pairs: K = 16 is 8 columns)
+                // z = T_hi r_hi + T_hi r_lo + T_lo r_hi, word by word as the
+                // compute warps leave the residual's parts in tensor memory
+                // (fp16 pairs: K = 16 is 8 columns)
 #pragma unroll 1
-                for (int s = 0; s < 24; ++s) {
-                    const uint32_t acol = tcol + 128 + (s >= 8 && s < 16 ? 64 : 0) + 8 * (s & 7);
-                    const uint32_t bs = (s < 16 ? th_s : tl_s) + 4096 * (s & 7);
-                    mma_f16_ts(tcol, acol, tc_desc(bs), id_h, s > 0);
+                for (int wd = 0; wd < 4 && !dead; ++wd) {
+                    if ((dead = !mbar_wait(rready0 + 8 * wd, it & 1, err))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int u = 0; u < 6; ++u) {
+                        const int s = 2 * wd + (u & 1), p = u >> 1;  // k-block; product hi.hi, hi.lo, lo.hi
+                        const uint32_t acol = tcol + 32 * wd + 8 * (s & 1) + (p == 1 ? 16 : 0);
+                        const uint32_t bs = (p < 2 ? th_s : tl_s) + 4096 * s;
+                        mma_f16_ts(tcol + 128, acol, tc_desc(bs), id_h, (wd | u) ? 1u : 0u);
+                    }
                 }
-                tc_commit(smem_u32(zdone));
+                if (dead) break;
+                tc_commit(zdone);
                 ++nz;
             }
-            // the last commits must land before tensor memory is freed (bounded
-            // waits, also after a wait above gave up)
-            if (nvd > 0) mbar_wait(smem_u32(vdone), (nvd - 1) & 1, err);
-            if (ny > 0) mbar_wait(smem_u32(ydone), (ny - 1) & 1, err);
-            if (nz > 0) mbar_wait(smem_u32(zdone), (nz - 1) & 1, err);
+            // the last commits and copies must land before the CTA's memory is
+            // freed (bounded waits, also after a wait above gave up)
+            if (nvd > 0) mbar_wait(vdone, (nvd - 1) & 1, err);
+            if (ny > 0) mbar_wait(ydone, (ny - 1) & 1, err);
+            if (nz > 0) mbar_wait(zdone, (nz - 1) & 1, err);
+            if (nx > it) mbar_wait(xfull, (nx - 1) & 1, err);
         }
     } else {
         // --------------------------------------------- compute (thread = row)
@@ -398,67 +448,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t yk = tcol + lane_base, yv = tcol + 128 + lane_base;
         const uint8_t* xv = smem + g * TcLayout::x_bytes + 32768;
-        const uint8_t* gk0 = static_cast<const uint8_t*>(a.k);
-        const uint8_t* gv0 = static_cast<const uint8_t*>(a.v);
-        // cp.async of tile `tile`'s K and V rows: 2048 chunks each; a warp's
-        // 32 copies cover 8 rows x 4 chunks (full 32-byte sectors)
-        auto stage = [&](int64_t tile) {
-            const int64_t w0 = tile * 128;
-            const int nv = nvec - w0 < 128 ? (int)(nvec - w0) : 128;
-            const uint8_t* gk = gk0 + w0 * 256;
-            const uint8_t* gv = gv0 + w0 * 256;
-#pragma unroll
-            for (int e = v; e < 2048; e += 128) {
-                const int l = e & 31, grp = e >> 5;
-                const int r = 8 * (grp & 15) + (l & 7), j = 4 * (grp >> 4) + (l >> 3);
-                const bool in = r < nv;
-                cp_async16(xk_s + tc_chunk(r, j), in ? gk + r * 256 + j * 16 : gk0, in ? 16u : 0u);
-                cp_async16(xv_s + tc_chunk(r, j), in ? gv + r * 256 + j * 16 : gv0, in ? 16u : 0u);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
+        // this row's (slot, head) in tile `tile` (slot -2: no such row), loaded
+        // a tile ahead
+        auto row_slot = [&](int64_t tile, int& h) -> int64_t {
+            const int64_t w = tile * 128 + v;
+            h = 0;
+            if (w >= nvec) return -2;
+            const int64_t t = nvec < ((int64_t)1 << 31) ? (int64_t)((uint32_t)w / (uint32_t)a.heads) : w / a.heads;
+            h = (int)(w - t * a.heads);
+            return a.slots[t];
         };
         int64_t tile = (int64_t)blockIdx.x * kTcWG + g;
-        if (tile < ntiles) stage(tile);
-        int it = 0;
-        for (; tile < ntiles; tile += tstep, ++it) {
-            const int64_t w0 = tile * 128;
-            const int nv = nvec - w0 < 128 ? (int)(nvec - w0) : 128;
-            // this row's destination while the copies land
-            const bool live = v < nv;
-            int64_t slot = -1;
-            int h = 0;
-            if (live) {
-                const int64_t w = w0 + v;
-                const int64_t t = nvec < ((int64_t)1 << 31) ? (int64_t)((uint32_t)w / (uint32_t)a.heads) : w / a.heads;
-                h = (int)(w - t * a.heads);
-                slot = a.slots[t];
-            }
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_fence_before();
-            named_sync(1 + g, 128);  // every row of the tile is in shared memory; the last tile's tensor memory is read
-            if (v == 0) mbar_arrive(smem_u32(xready));
+        int h_next = 0;
+        int64_t slot_next = tile < ntiles ? row_slot(tile, h_next) : -2;
+        for (int it = 0; tile < ntiles; tile += tstep, ++it) {
+            const int64_t slot = slot_next;
+            const int h = h_next;
+            if (tile + tstep < ntiles) slot_next = row_slot(tile + tstep, h_next);
+            const bool live = slot != -2;
             const bool ok = live && slot >= 0 && slot < a.num_slots;
-            if (live && slot != -1 && !(slot >= 0 && slot < a.num_slots) && h == 0) set_error(err, TQ_DEVERR_SLOT);
+            if (live && slot != -1 && !ok && h == 0) set_error(err, TQ_DEVERR_SLOT);
             const int row = (int)(slot & 15);
             uint8_t* page = ok ? a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes : nullptr;
 
             // ---------------------------------------------------------- value
             if constexpr (VG) {
                 // (from shared memory, while the keys rotate)
-                if (ok) g32_row<VB>(xv, v, page + L.v_codes + row * L.v_code_row, page + L.v_meta + row * 16);
-                named_sync(1 + g, 128);  // every row's values are read from shared memory
+                if (!dead) dead = !mbar_wait(xfull, it & 1, err);
+                if (ok && !dead) g32_row<VB>(xv, v, page + L.v_codes + row * L.v_code_row, page + L.v_meta + row * 16);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfree);
             } else {
-                if (!dead) dead = !mbar_wait(smem_u32(vdone), it & 1, err);
+                if (!dead) dead = !mbar_wait(vdone, it & 1, err);
                 tc_fence_after();
                 const float n = mse_planes<VB>(yv, vpb, ok && !dead ? page + L.v_codes : nullptr, row);
                 if (ok && !dead) reinterpret_cast<__half*>(page + L.v_meta)[row] = __float2half_rn(n);
             }
-            if (!dead) dead = !mbar_wait(smem_u32(ydone), it & 1, err);
+            if (!dead) dead = !mbar_wait(ydone, it & 1, err);
             tc_fence_after();
-            // the shared-memory tile is free (the rotation MMAs have read it):
-            // the next tile's rows load while this one is encoded
-            if (tile + tstep < ntiles) stage(tile + tstep);
 
             // ------------------------------------------------------------ key
             {
@@ -516,8 +543,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                             hi[u] = *reinterpret_cast<const uint32_t*>(&hh);
                             lo[u] = *reinterpret_cast<const uint32_t*>(&ll);
                         }
-                        tmem_st16(yv + 16 * wd, hi);
-                        tmem_st16(yv + 64 + 16 * wd, lo);
+                        tmem_st16(yk + 32 * wd, hi);
+                        tmem_st16(yk + 32 * wd + 16, lo);
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rready0 + 8 * wd);  // this warp's rows of word wd
                     }
                     const uint32_t pos = ~S.word() & nz;  // [y > 0]
                     KW[KB - 1][wd] = pos;
@@ -532,17 +563,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                 }
                 if (ok && !dead) reinterpret_cast<__half*>(page + L.k_norm)[row] = n16;
                 if (qjl) {
-                    tc_wait_st();
-                    tc_fence_before();
-                    named_sync(1 + g, 128);  // every row's residual parts are in tensor memory
-                    if (v == 0) mbar_arrive(smem_u32(rready));
-                    if (!dead) dead = !mbar_wait(smem_u32(zdone), it & 1, err);
+                    if (!dead) dead = !mbar_wait(zdone, it & 1, err);
                     tc_fence_after();
                     uint32_t sw[4];
 #pragma unroll
                     for (int wd = 0; wd < 4; ++wd) {
                         uint32_t z[32];
-                        tmem_ld32(yk + 32 * wd, z);
+                        tmem_ld32(yv + 32 * wd, z);
                         tc_wait_ld();
                         Bits32 neg;
 #pragma unroll
@@ -556,12 +583,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) store_tc_kernel(StoreArgs a) {
                     }
                 }
             }
+            // this warp's rows of the tile's tensor memory are read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tfree);
         }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// The driver's tensor-map encoder: from the runtime's entry-point query, else
+// the driver library's own export; looked up under a lock until found.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(char* why, size_t why_len) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (fn) return fn;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) p = nullptr;
+    if (!p) {
+        if (void* h = dlopen("libcuda.so.1", RTLD_NOW | RTLD_LOCAL)) p = dlsym(h, "cuTensorMapEncodeTiled");
+    }
+    if (!p) {
+        snprintf(why, why_len, "cuTensorMapEncodeTiled not found (entry-point query: %s, result %d; libcuda.so.1: %s)",
+                 cudaGetErrorName(e), (int)q, dlerror() ? "no symbol" : "not loaded");
+        return nullptr;
+    }
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return fn;
+}
+
+// rows [n][128] bf16 at base as a 2-D map with 8 x 128 boxes (zero fill past n)
+static tq_status rows_map(CUtensorMap* m, const void* base, int64_t n) {
+    char why[200] = "";
+    auto enc = tensor_map_encoder(why, sizeof why);
+    if (!enc) return driver_failure("%s", why);
+    // the encoder wants a current context: a host thread whose first call this
+    // is has none until the runtime binds the device's primary context
+    static thread_local bool bound = false;
+    if (!bound) {
+        int dev = 0;
+        const tq_status st = cuda_status_detail(cudaGetDevice(&dev), "binding the device context");
+        if (st == TQ_OK) bound = cuda_status_detail(cudaSetDevice(dev), "binding the device context") == TQ_OK;
+        if (!bound) return TQ_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {128, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {8, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return driver_failure("cuTensorMapEncodeTiled failed (CUresult %d) for rows at %p, n = %lld", (int)r, base,
+                              (long long)n);
+    return TQ_OK;
 }
 
 template <int KB, bool VG, int VB>
@@ -569,9 +649,14 @@ static tq_status launch_tc(const StoreArgs& a, cudaStream_t s, int sms) {
     auto kern = store_tc_kernel<KB, VG, VB>;
     const tq_status fs = ensure_dynamic_smem((const void*)kern, (int)TcLayout::total, "store_tc_kernel");
     if (fs != TQ_OK) return fs;
-    const int64_t tiles = (a.num_tokens * a.heads + 127) / 128;
+    const int64_t nvec = a.num_tokens * a.heads;
+    CUtensorMap mk, mv;
+    tq_status ms = rows_map(&mk, a.k, nvec);
+    if (ms == TQ_OK) ms = rows_map(&mv, a.v, nvec);
+    if (ms != TQ_OK) return ms;
+    const int64_t tiles = (nvec + 127) / 128;
     const int grid = (int)std::min<int64_t>((tiles + kTcWG - 1) / kTcWG, (int64_t)sms);
-    kern<<<grid, kTcThreads, TcLayout::total, s>>>(a);
+    kern<<<grid, kTcThreads, TcLayout::total, s>>>(a, mk, mv);
     return cuda_status(cudaGetLastError());
 }
 
