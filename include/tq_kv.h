@@ -311,10 +311,13 @@ tq_status tq_set_profile_events(tq_cache* cache, int kernel, void* start_event, 
 /*
  * Tuning: tq_store encodes at most `max_vectors` (token, KV head) vectors with
  * one CTA per vector, without staging S in shared memory (the latency-bound
- * shape of a decode step's new tokens), and larger calls with the persistent
- * eight-vectors-per-CTA kernel.  Both write identical bytes.  A negative value
- * restores the default, 16 x the device's SM count.  Process-wide; takes
- * effect for later calls.  Returns TQ_OK.
+ * shape of a decode step's new tokens), and larger calls with a bulk kernel
+ * (tiles of 128 vectors on the tensor cores for d = 128 bf16 inputs, else
+ * eight vectors per CTA).  Every path computes the same definition; their
+ * fp32 sums round in different orders, so their bytes can differ only in the
+ * boundary cases where such a rounding decides a code, an fp16 field or a sign.
+ * A negative value restores the default, 16 x the device's SM count.
+ * Process-wide; takes effect for later calls.  Returns TQ_OK.
  */
 tq_status tq_set_store_small_max(int64_t max_vectors);
 

@@ -197,10 +197,16 @@ __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uin
 #pragma unroll
     for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = __float_as_uint(PB[k] * sc);
     uint32_t W[B][4];
+    // word wd + 1 loads from tensor memory while word wd is encoded
+    uint32_t ybuf[32];
+    tmem_ld32(taddr, ybuf);
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
         float y[32];
-        tmem_row32(taddr + 32 * wd, y);
+        tc_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(ybuf[c]);
+        if (wd < 3) tmem_ld32(taddr + 32 * (wd + 1), ybuf);
         Bits32 S, C[NB];
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
@@ -267,12 +273,16 @@ __device__ __forceinline__ void g32_row(const uint8_t* xrow_base, int v, uint8_t
             const float num = x[i] - zf;
             const float q0 = num * rs;
             const float t = fmaf(fmaf(-q0, sf, num), rs, q0);
-            const float fl = floorf(t);
-            const int q = min(max((int)fl + ((t - fl) >= 0.5f ? 1 : 0), 0), top);
+            // floor(t + 1/2), exactly, by two round-down additions (the second
+            // against 1.5 * 2^23 leaves the integer in the low bits), clamped
+            // in float: no conversion instructions
+            float y = __fadd_rd(__fadd_rd(t, 0.5f), 12582912.f);
+            y = fminf(fmaxf(y, 12582912.f), 12582912.f + (float)top);
+            const uint32_t q = __float_as_uint(y) & (uint32_t)top;
             // coordinate c = 32 gr + i = 32 (m >> 1) + 4 g + 2 (m & 1) + e
             const int g = (i >> 2) & 7, m = 2 * gr + ((i >> 1) & 1), e = i & 1;
             const int slot = 16 * g + 2 * m + e;
-            words[(slot * VB) >> 5] |= (uint32_t)q << ((slot * VB) & 31);
+            words[(slot * VB) >> 5] |= q << ((slot * VB) & 31);
         }
     }
 #pragma unroll
@@ -514,10 +524,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int k = 0; k < (1 << NB); ++k) Gb[k] = __float_as_uint(G[k]);
                 float rr4[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t KW[KB][4];
+                // word wd + 1 loads from tensor memory while word wd is encoded
+                uint32_t ybuf[32];
+                tmem_ld32(yk, ybuf);
 #pragma unroll
                 for (int wd = 0; wd < 4; ++wd) {
                     float y[32];
-                    tmem_row32(yk + 32 * wd, y);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(ybuf[c]);
+                    if (wd < 3) tmem_ld32(yk + 32 * (wd + 1), ybuf);
                     Bits32 S, C[NB];
                     uint32_t hi[16], lo[16];
 #pragma unroll
@@ -566,11 +582,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!dead) dead = !mbar_wait(zdone, it & 1, err);
                     tc_fence_after();
                     uint32_t sw[4];
+                    uint32_t zbuf[32];
+                    tmem_ld32(yv, zbuf);
 #pragma unroll
                     for (int wd = 0; wd < 4; ++wd) {
                         uint32_t z[32];
-                        tmem_ld32(yv + 32 * wd, z);
                         tc_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) z[c] = zbuf[c];
+                        if (wd < 3) tmem_ld32(yv + 32 * (wd + 1), zbuf);
                         Bits32 neg;
 #pragma unroll
                         for (int i = 31; i >= 0; --i) neg.push(i, z[i]);
