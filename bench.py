@@ -60,6 +60,8 @@ def _args():
     p.add_argument("--no-decode-workloads", action="store_true",
                    help="skip the d=256 and 70B-shaped hybrid decode lines")
     p.add_argument("--no-boundary-cases", action="store_true")
+    p.add_argument("--store-only", action="store_true",
+                   help="time only the store workload and print its line (a profiling entry point)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -646,6 +648,13 @@ def run_ours(args):
         w = wl.scaled(w, k_bits=args.k_bits)
     if args.codebook != "lloyd":
         w = wl.scaled(w, k_codebook=args.codebook, v_codebook=args.codebook if w.v_mode == "mse" else "lloyd")
+    if args.store_only:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        line, _ = _store_workload(torch, tq, wl, device, max(1, args.steps), max(3, args.warmup), flush,
+                                  _peaks()[0], with_boundary_cases=False)
+        if rank == 0:
+            print(json.dumps({"store_workload": line}), flush=True)
+        return
     split_blocks = _split_blocks(w, args.split_blocks)
     c, st, table = _setup_decode(w, split_blocks, torch, tq, wl, device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)

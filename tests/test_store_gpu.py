@@ -64,6 +64,8 @@ CASES = [
     ("k4_v3mse_d256", 256, 1, 4, "mse", 3, "bf16", True, 5, 15.0),
     ("uniform_k4_v4mse", 128, 2, 4, "mse", 4, "bf16", True, 3, 10.0, "uniform"),
     ("uniform_k3_v2mse_d256", 256, 1, 3, "mse", 2, "f32", True, 5, 15.0, "uniform"),
+    ("k2_v3mse", 128, 4, 2, "mse", 3, "bf16", True, 3, 10.0),
+    ("k2_v4g32", 128, 2, 2, "g32", 4, "bf16", True, 3, 10.0),
 ]
 
 

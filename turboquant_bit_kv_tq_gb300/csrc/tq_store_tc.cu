@@ -93,53 +93,109 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t addr) { return smem_desc(ad
 
 // (w << 1) | top bit of m
 __device__ __forceinline__ uint32_t push_bit(uint32_t w, uint32_t m) { return __funnelshift_l(m, w, 1); }
-__device__ __forceinline__ uint32_t sel_u(uint32_t m, uint32_t a, uint32_t b) { return (m & a) | (~m & b); }
-__device__ __forceinline__ uint32_t all_if_neg(uint32_t d) { return (uint32_t)((int32_t)d >> 31); }
+// a * b + c on the integer multiply-add pipe (the FMA pipe): with b01 in
+// {0, 1}, imad(b01, A - B, B) selects A or B and imad(w, 2, b01) pushes a bit,
+// leaving the ALU pipe (logic, shifts, integer adds) to what only it does
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// 1 if x is negative (its sign bit), else 0
+__device__ __forceinline__ uint32_t neg01(float x) { return __float_as_uint(x) >> 31; }
 
-// Comparisons of non-negative floats as integers: for a = bits(|y|) and
-// t = bits(T) (both below 2^31), t - a has its top bit set iff |y| > T.  cnt =
-// #{positive boundaries below |y|} by a binary search over the 2^NB - 1 sorted
-// positive boundaries T: d[q] has the top bit = bit q of cnt; m[q] the same
-// bit as a full mask.
+// The cells of |y| against a symmetric codebook's sorted positive boundaries
+// T_0 < ... < T_{2^NB - 2} (scaled by n sqrt(d)) and positive centroids G_c:
+// cnt = #{T below |y|} by a binary search whose steps are the signs of
+// T - |y| (fp32 subtraction without flush-to-zero: the computed difference is
+// negative iff |y| > T, and +0 when they are equal), the threshold of each
+// step chosen by bit-weighted multiply-adds on T's bit patterns; G_cnt by the
+// same multiply-adds over the bits of cnt.
 template <int NB>
-__device__ __forceinline__ void cnt_bits(uint32_t a, const uint32_t* T, uint32_t (&d)[3], uint32_t (&m)[3]) {
-    if constexpr (NB == 1) {
-        d[0] = T[0] - a;
-        m[0] = all_if_neg(d[0]);
-    } else if constexpr (NB == 2) {
-        d[1] = T[1] - a;
-        m[1] = all_if_neg(d[1]);
-        d[0] = sel_u(m[1], T[2], T[0]) - a;
-        m[0] = all_if_neg(d[0]);
-    } else {
-        d[2] = T[3] - a;
-        m[2] = all_if_neg(d[2]);
-        d[1] = sel_u(m[2], T[5], T[1]) - a;
-        m[1] = all_if_neg(d[1]);
-        d[0] = sel_u(m[2], sel_u(m[1], T[6], T[4]), sel_u(m[1], T[2], T[0])) - a;
-        m[0] = all_if_neg(d[0]);
+struct Cells {
+    float tf;          // the first step's threshold: T_{2^(NB-1) - 1}
+    uint32_t tb[4];    // the later steps' base patterns and differences
+    uint32_t gb[8];    // G_0 and the bit-weighted differences of the centroids
+    __device__ __forceinline__ void init(const float* T, const float* G) {
+        auto u = [](float x) { return __float_as_uint(x); };
+        if constexpr (NB == 1) {
+            tf = T[0];
+            gb[0] = u(G[0]);
+            gb[1] = u(G[1]) - u(G[0]);
+        } else if constexpr (NB == 2) {
+            tf = T[1];
+            tb[0] = u(T[0]);
+            tb[1] = u(T[2]) - u(T[0]);
+            gb[0] = u(G[0]);
+            gb[1] = u(G[1]) - u(G[0]);
+            gb[2] = u(G[2]) - u(G[0]);
+            gb[3] = u(G[3]) - u(G[2]) - u(G[1]) + u(G[0]);
+        } else {
+            tf = T[3];
+            tb[0] = u(T[1]);                              // second step: T_1 or T_5
+            tb[1] = u(T[5]) - u(T[1]);
+            tb[2] = u(T[2]) - u(T[0]);                    // third step: T_{4 b2 + 2 b1}
+            tb[3] = u(T[6]) - u(T[4]) - u(T[2]) + u(T[0]);
+            gb[0] = u(G[0]);                              // G_{b0 + 2 b1} and G_{4 + b0 + 2 b1}
+            gb[1] = u(G[1]) - u(G[0]);
+            gb[2] = u(G[2]) - u(G[0]);
+            gb[3] = u(G[3]) - u(G[2]) - u(G[1]) + u(G[0]);
+            gb[4] = u(G[4]);
+            gb[5] = u(G[5]) - u(G[4]);
+            gb[6] = u(G[6]) - u(G[4]);
+            gb[7] = u(G[7]) - u(G[6]) - u(G[5]) + u(G[4]);
+            t0 = u(T[0]);
+            t40 = u(T[4]) - u(T[0]);
+        }
     }
-}
-// G[cnt]: the positive centroid of the cell (float bits)
-template <int NB>
-__device__ __forceinline__ uint32_t cell_value(const uint32_t (&m)[3], const uint32_t* G) {
-    if constexpr (NB == 1) {
-        return sel_u(m[0], G[1], G[0]);
-    } else if constexpr (NB == 2) {
-        return sel_u(m[1], sel_u(m[0], G[3], G[2]), sel_u(m[0], G[1], G[0]));
-    } else {
-        const uint32_t lo = sel_u(m[1], sel_u(m[0], G[3], G[2]), sel_u(m[0], G[1], G[0]));
-        const uint32_t hi = sel_u(m[1], sel_u(m[0], G[7], G[6]), sel_u(m[0], G[5], G[4]));
-        return sel_u(m[2], hi, lo);
+    uint32_t t0 = 0, t40 = 0;  // NB = 3: T_0 and T_4 - T_0
+    // bits b[q] (0/1) of cnt for a = |y|
+    __device__ __forceinline__ void bits(float a, uint32_t (&b)[3]) const {
+        if constexpr (NB == 1) {
+            b[0] = neg01(tf - a);
+        } else if constexpr (NB == 2) {
+            b[1] = neg01(tf - a);
+            b[0] = neg01(__uint_as_float(imad(b[1], tb[1], tb[0])) - a);
+        } else {
+            b[2] = neg01(tf - a);
+            b[1] = neg01(__uint_as_float(imad(b[2], tb[1], tb[0])) - a);
+            const uint32_t p = imad(b[1], b[2], 0u);
+            uint32_t t = imad(b[1], tb[2], t0);
+            t = imad(b[2], t40, t);
+            t = imad(p, tb[3], t);
+            b[0] = neg01(__uint_as_float(t) - a);
+        }
     }
-}
+    // G_cnt (float bits)
+    __device__ __forceinline__ uint32_t centroid(const uint32_t (&b)[3]) const {
+        if constexpr (NB == 1) {
+            return imad(b[0], gb[1], gb[0]);
+        } else {
+            const uint32_t p = imad(b[0], b[1], 0u);
+            uint32_t lo = imad(b[0], gb[1], gb[0]);
+            lo = imad(b[1], gb[2], lo);
+            lo = imad(p, gb[3], lo);
+            if constexpr (NB == 2) {
+                return lo;
+            } else {
+                uint32_t hi = imad(b[0], gb[5], gb[4]);
+                hi = imad(b[1], gb[6], hi);
+                hi = imad(p, gb[7], hi);
+                return imad(b[2], hi - lo, lo);
+            }
+        }
+    }
+};
 
 // Plane words of 32 coordinates are built from four 8-bit accumulators
 // (coordinates 8q+7 .. 8q pushed, highest first, into accumulator q), joined
 // as bytes: four short dependency chains instead of one of 32.
 struct Bits32 {
     uint32_t q[4] = {0u, 0u, 0u, 0u};
+    // the top bit of m (a shift on the ALU pipe)
     __device__ __forceinline__ void push(int i, uint32_t m) { q[i >> 3] = push_bit(q[i >> 3], m); }
+    // a 0/1 bit (a multiply-add on the FMA pipe)
+    __device__ __forceinline__ void push01(int i, uint32_t b) { q[i >> 3] = imad(q[i >> 3], 2u, b); }
     __device__ __forceinline__ uint32_t word() const {
         return __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
     }
@@ -192,10 +248,12 @@ __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uin
     constexpr int NB = B - 1;
     const float n = row_norm128(taddr);
     const uint32_t nz = n > 0.f ? 0xFFFFFFFFu : 0u;
-    uint32_t T[7];
+    float T[7], G[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const float sc = n * 11.313708498984761f;  // n sqrt(d)
 #pragma unroll
-    for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = __float_as_uint(PB[k] * sc);
+    for (int k = 0; k < (1 << NB) - 1; ++k) T[k] = PB[k] * sc;
+    Cells<NB> cells;
+    cells.init(T, G);
     uint32_t W[B][4];
     // word wd + 1 loads from tensor memory while word wd is encoded
     uint32_t ybuf[32];
@@ -210,12 +268,11 @@ __device__ __forceinline__ float mse_planes(uint32_t taddr, const float* PB, uin
         Bits32 S, C[NB];
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
-            const uint32_t yb = __float_as_uint(y[i]);
-            uint32_t d[3], m[3];
-            cnt_bits<NB>(yb & 0x7FFFFFFFu, T, d, m);
-            S.push(i, yb);  // the sign bit
+            uint32_t b[3];
+            cells.bits(fabsf(y[i]), b);
+            S.push(i, __float_as_uint(y[i]));  // the sign bit
 #pragma unroll
-            for (int q = 0; q < NB; ++q) C[q].push(i, d[q]);
+            for (int q = 0; q < NB; ++q) C[q].push01(i, b[q]);
         }
         const uint32_t pos = ~S.word() & nz;  // [y > 0]
         W[B - 1][wd] = pos;
@@ -517,11 +574,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int k = 0; k < (1 << NB); ++k) G[k] = kpc[k] * cs;
                 uint8_t* kplanes = ok && !dead ? page + L.k_codes : nullptr;
                 const uint32_t nz = n > 0.f ? 0xFFFFFFFFu : 0u;
-                uint32_t Tb[7], Gb[8];
-#pragma unroll
-                for (int k = 0; k < (1 << NB) - 1; ++k) Tb[k] = __float_as_uint(T[k]);
-#pragma unroll
-                for (int k = 0; k < (1 << NB); ++k) Gb[k] = __float_as_uint(G[k]);
+                Cells<NB> cells;
+                cells.init(T, G);
                 float rr4[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t KW[KB][4];
                 // word wd + 1 loads from tensor memory while word wd is encoded
@@ -539,14 +593,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int i = 31; i >= 0; --i) {
                         const uint32_t yb = __float_as_uint(y[i]);
-                        uint32_t d[3], m[3];
-                        cnt_bits<NB>(yb & 0x7FFFFFFFu, Tb, d, m);
+                        uint32_t b[3];
+                        cells.bits(fabsf(y[i]), b);
                         S.push(i, yb);
 #pragma unroll
-                        for (int q = 0; q < NB; ++q) C[q].push(i, d[q]);
+                        for (int q = 0; q < NB; ++q) C[q].push01(i, b[q]);
                         // -n16 rs c[idx]: c[idx] = +G[cnt] for y > 0, -G[cnt]
                         // otherwise, i.e. -c takes the sign bit of y flipped
-                        const float cneg = __uint_as_float(cell_value<NB>(m, Gb) ^ (~yb & 0x80000000u));
+                        const float cneg = __uint_as_float(cells.centroid(b) ^ (~yb & 0x80000000u));
                         y[i] = fmaf(y[i], s1, cneg);  // the scaled rotated residual
                         rr4[i & 3] = fmaf(y[i], y[i], rr4[i & 3]);
                     }
