@@ -226,25 +226,32 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) rq[h * D + lane + 32 * k] = x[k] * rsqrtf((float)D) * f;
     }
-    // S q from the shared copy of S^T: thread (j, head parity)
+    // S q from the shared copy of S^T: thread (column pair j, j + 1; head h),
+    // 32-bit loads of S^T pairs and 128-bit loads of four query elements
     bool s_ok = mbar_wait(smem_u32(bar), 0, a.dp.err);
     const float kq = f * sqrtf(1.5707963267948966f) / (float)D;
     {
-        constexpr int HS = 256 / D;  // head strides covered by the block (2 at d=128, 1 at d=256)
-        const int j = tid % D, h0 = tid / D;
-        for (int hb = h0; hb < G; hb += 2 * HS) {
-            const int h1 = hb + HS;
-            float s0 = 0.f, s1 = 0.f;
+        constexpr int NP = D / 2;            // column pairs
+        constexpr int HS = 256 / NP;         // heads covered per pass (4 at d=128, 2 at d=256)
+        const int jp = tid % NP, h0 = tid / NP;
+        for (int h = h0; h < G; h += HS) {
+            float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};  // two partial sums per column
             if (s_ok) {
-#pragma unroll 8
-                for (int i = 0; i < D; ++i) {
-                    const float sv = bf16_bits_to_float(st[i * D + j]);
-                    s0 = fmaf(sv, qv[hb * D + i], s0);
-                    if (h1 < G) s1 = fmaf(sv, qv[h1 * D + i], s1);
+                const float4* q4 = reinterpret_cast<const float4*>(qv + h * D);
+#pragma unroll 4
+                for (int i4 = 0; i4 < D / 4; ++i4) {
+                    const float4 qq = q4[i4];
+                    const float qa[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t pr = *reinterpret_cast<const uint32_t*>(st + (4 * i4 + u) * D + 2 * jp);
+                        s0[u & 1] = fmaf(__uint_as_float(pr << 16), qa[u], s0[u & 1]);
+                        s1[u & 1] = fmaf(__uint_as_float(pr & 0xFFFF0000u), qa[u], s1[u & 1]);
+                    }
                 }
             }
-            sq[hb * D + j] = s0 * kq;
-            if (h1 < G) sq[h1 * D + j] = s1 * kq;
+            sq[h * D + 2 * jp] = (s0[0] + s0[1]) * kq;
+            sq[h * D + 2 * jp + 1] = (s1[0] + s1[1]) * kq;
         }
     }
     // a copy that never completed must land before the block exits
@@ -285,15 +292,20 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
         m_rq = warp_max(m_rq) * bmax;
         m_sq = warp_max(m_sq) * 2.f;
         if (lane == 0) {
-            const int ek = m_rq > 0.f ? (int)floorf(log2f(224.f / m_rq)) : 0;
-            const int eq = m_sq > 0.f ? (int)floorf(log2f(224.f / m_sq)) : 0;
+            // operand scales 2^e with 2^e m <= 224 (e4m3 holds up to 448): e is
+            // the binary exponent of 224 / m, read from its float bits
+            auto scale_exp = [](float m) {
+                return m > 0.f ? (int)((__float_as_uint(224.f / m) >> 23) & 0xFF) - 127 : 0;
+            };
+            auto pow2 = [](int e) { return __uint_as_float((uint32_t)(127 + e) << 23); };
+            const int ek = max(-120, min(120, scale_exp(m_rq))), eq = max(-120, min(120, scale_exp(m_sq)));
             float* c = a.ws_cst + (hbase + h) * 4;
             c[0] = kw[0] * s_rq + 0.5f * bsum * s_rq7;
             c[1] = -s_sq + s_sq7;
-            c[2] = ldexpf(1.f, -ek);
-            c[3] = ldexpf(1.f, -eq);
-            sig[2 * h] = ldexpf(1.f, ek);
-            sig[2 * h + 1] = ldexpf(1.f, eq);
+            c[2] = pow2(-ek);
+            c[3] = pow2(-eq);
+            sig[2 * h] = pow2(ek);
+            sig[2 * h + 1] = pow2(eq);
         }
     }
     __syncthreads();
@@ -1373,6 +1385,15 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     __shared__ float red[2][4];
     extern __shared__ float wgt[];  // [S] split weights 2^(m_s - M)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the first kPre splits' partials load now, beside the (m, l) pairs,
+    // instead of after the two reductions below
+    constexpr int kPre = 32;
+    const float* src = a.ws_acc + base * D + tid;
+    float pre[kPre][kPerThread];
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+#pragma unroll
+        for (int p = 0; p < kPerThread; ++p) pre[s][p] = s < S ? src[(int64_t)s * D + 128 * p] : 0.f;
     // every split's (m, l) at once; M = max m.  Compressed splits past the
     // sequence's length are empty and need not have been written.
     const int len = max(0, min(a.seq_lens[b], a.max_blocks * kBlock));
@@ -1401,10 +1422,15 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     float acc[kPerThread];
 #pragma unroll
     for (int p = 0; p < kPerThread; ++p) acc[p] = 0.f;
-    const float* src = a.ws_acc + base * D + tid;
     // an empty split (weight 0) may leave its partial unwritten: skip it
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) {
+        const float w = s < S ? wgt[s] : 0.f;
+#pragma unroll
+        for (int p = 0; p < kPerThread; ++p) acc[p] = w > 0.f ? fmaf(w, pre[s][p], acc[p]) : acc[p];
+    }
 #pragma unroll 8
-    for (int s = 0; s < S; ++s) {
+    for (int s = kPre; s < S; ++s) {
         const float w = wgt[s];
 #pragma unroll
         for (int p = 0; p < kPerThread; ++p) {
