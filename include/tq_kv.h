@@ -108,7 +108,7 @@ enum {
     TQ_DEVERR_BLOCK = 1u << 1,     /* decode: block id outside [0, num_blocks); block skipped */
     TQ_DEVERR_SEQLEN = 1u << 2,    /* decode: seq_len < 0 or > 16*max_blocks_per_seq; clamped */
     TQ_DEVERR_TAIL = 1u << 3,      /* decode: tail_len < 0 or > tail_cap; clamped */
-    TQ_DEVERR_TIMEOUT = 1u << 4,   /* decode: a bounded wait (2 s) for a staged page gave up; split abandoned */
+    TQ_DEVERR_TIMEOUT = 1u << 4,   /* a bounded wait (2^24 polls) on a staged tile or an MMA gave up; work abandoned */
     TQ_DEVERR_CHUNK = 1u << 5      /* extend: a token row outside every sequence's chunk (cu_q); its output is 0 */
 };
 
@@ -328,13 +328,13 @@ tq_status tq_set_store_small_max(int64_t max_vectors);
 tq_status tq_get_device_error(const tq_cache* cache, uint32_t* flags, void* stream);
 
 /*
- * Diagnostic; the pages have no counterpart.  Every wait of the decode kernels
- * on an mbarrier (a staged page, a tensor-core result) is bounded: after 2 s of
- * the device's global timer (or 2^26 polls) it gives up, sets
- * TQ_DEVERR_TIMEOUT, drains its copies in flight and returns, so a stalled
- * copy becomes an error status instead of a hung GPU.  This call launches one
- * thread that makes that same wait on an mbarrier nothing ever completes, with
- * the limit set to limit_us microseconds (1 .. 4 * 10^6), and OR-s
+ * Diagnostic; the pages have no counterpart.  Every wait of the store and
+ * decode kernels on an mbarrier (a staged page, a tensor-core result) is
+ * bounded: after 2^24 unsuccessful polls it gives up, sets TQ_DEVERR_TIMEOUT,
+ * drains its copies in flight and returns, so a stalled copy becomes an error
+ * status instead of a hung GPU.  This call launches one thread that makes that
+ * wait (the same polling loop, with a time limit of limit_us microseconds,
+ * 1 .. 4 * 10^6, added) on an mbarrier nothing ever completes, and OR-s
  * TQ_DEVERR_TIMEOUT into *err_word (caller-owned device uint32, 4-byte
  * aligned) when it gives up.  Asynchronous on `stream`; lets a test check that
  * a wait that runs out ends its kernel with the error bit set and leaves the

@@ -94,9 +94,9 @@ def test_first_calls_from_several_threads_at_once():
 
 
 def test_bounded_wait_gives_up_with_an_error_status():
-    # an mbarrier phase nothing completes, waited for through the decode
-    # kernels' bounded wait with a 20 ms limit: the kernel must end by itself,
-    # set TQ_DEVERR_TIMEOUT, and leave the context usable
+    # an mbarrier phase nothing completes, waited for through the kernels'
+    # bounded polling loop with a 20 ms time limit added: the kernel must end
+    # by itself, set TQ_DEVERR_TIMEOUT, and leave the context usable
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     t0 = time.perf_counter()

@@ -175,7 +175,7 @@ __global__ void wait_timeout_kernel(uint32_t* err, uint32_t limit_ns) {
     if (threadIdx.x != 0) return;
     mbar_init(smem_u32(&bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    mbar_wait(smem_u32(&bar), 0, err, limit_ns);
+    mbar_wait_timed(smem_u32(&bar), 0, err, limit_ns);
 }
 
 // One thread per new token t: find the sequence whose chunk holds row t (the

@@ -96,12 +96,17 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) { atomicO
 // ------------------------------------------- mbarriers, bulk copies, tcgen05
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// bounded mbarrier wait: gives up once limit_ns nanoseconds have passed on the
-// low 32 bits of the device's global timer (read every 64 unsuccessful polls;
-// differences taken modulo 2^32, so limits below 4.29 s never see a wrap), or
-// after 2^26 polls should the timer not advance; records TQ_DEVERR_TIMEOUT
-// and returns false.  A phase that completes returns true.
-constexpr uint32_t kWaitLimitNs = 2000000000u;  // 2 s: every wait of a store or decode call is microseconds
+// Bounded mbarrier waits.  mbar_wait gives up after kWaitPolls unsuccessful
+// polls (each mbarrier.try_wait may itself suspend for a hardware-defined
+// window), records TQ_DEVERR_TIMEOUT and returns false; a phase that completes
+// returns true.  Every wait of a store or decode call lasts microseconds.  The
+// loop is inlined at each wait site: a call would make every caller spill its
+// registers, and a global-timer limit in the loop measured 3.5 us slower on
+// the split kernel (instruction-cache misses), so the kernels bound by polls.
+// mbar_wait_timed adds a time limit on the low 32 bits of the global timer
+// (read every 64 polls; differences modulo 2^32, so limits below 4.29 s never
+// see a wrap): the wait-timeout check runs it with a short limit.
+constexpr uint32_t kWaitPolls = 1u << 24;
 __device__ __forceinline__ uint32_t global_ns_lo() {
     uint32_t t;
     asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
@@ -116,12 +121,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err,
-                                          uint32_t limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+    if (mbar_try(bar, parity)) return true;
+#pragma unroll 1
+    for (uint32_t it = 1; it < kWaitPolls; ++it)
+        if (mbar_try(bar, parity)) return true;
+    set_error(err, TQ_DEVERR_TIMEOUT);
+    return false;
+}
+__device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint32_t t0 = global_ns_lo();
 #pragma unroll 1
-    for (uint32_t it = 1; it <= (1u << 26); ++it) {
+    for (uint32_t it = 1; it < kWaitPolls; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 63u) == 0u && global_ns_lo() - t0 > limit_ns) break;
     }
