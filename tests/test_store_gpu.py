@@ -126,6 +126,40 @@ def test_store_skip_and_bad_slot_sets_device_error(store_path):
     parity.check_store(r, f"bad_slot/{store_path}")
 
 
+@pytest.mark.parametrize("offset_elems", [0, 2], ids=["aligned_full_tiles", "rows_4B_aligned_only"])
+def test_store_bulk_tile_edges(offset_elems):
+    # 256 tokens x 2 KV heads = 512 vectors, exactly four 128-vector tiles,
+    # through the bulk path.  With the K and V rows 4- but not 16-byte aligned
+    # (a view two bf16 elements into its buffer) the tensor-core store cannot
+    # use bulk-tensor copies and the eight-vectors-per-CTA kernel must take the
+    # call; either way every byte matches the oracle up to counted cases.
+    w = wl.Workload("tiles", 128, 2, 2, 3, "mse", 2, "bf16", 3, 10.0, seed=14, batch=1, seq_lens=[256])
+    T = 256
+    K, V = wl.kv_tokens(w, 0, 0, T)
+    num_blocks = 20
+    rng = np.random.default_rng(9)
+    slots = rng.permutation(num_blocks * 16)[:T].astype(np.int64)
+    c = _cache_for(w, num_blocks)
+
+    def dev_view(x):
+        flat = torch.zeros(x.size + offset_elems, dtype=torch.bfloat16, device="cuda")
+        flat[offset_elems:] = torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).cuda().to(torch.bfloat16)
+        return flat[offset_elems:].view(x.shape)
+
+    k, v = dev_view(K), dev_view(V)
+    assert (k.data_ptr() % 16 == 0) == (offset_elems == 0)
+    tq.tq_set_store_small_max(0)  # bulk path
+    try:
+        c.store(k, v, torch.from_numpy(slots).cuda())
+        torch.cuda.synchronize()
+    finally:
+        tq.tq_set_store_small_max(-1)
+    assert c.device_error() == 0
+    r = parity.compare_store(c.pages().cpu().numpy(), _oracle_params(w), K, V, slots, w.kv_heads)
+    parity.check_store(r, f"bulk_tiles/{offset_elems}")
+    assert r["checked_bytes"] > 0
+
+
 def test_store_zero_tokens_is_noop():
     w = wl.Workload("empty", 128, 1, 1, 2, "mse", 2, "bf16", 0, 1.0, seed=1, batch=1, seq_lens=[1])
     c = _cache_for(w, 2)

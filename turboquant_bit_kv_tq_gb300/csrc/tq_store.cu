@@ -446,7 +446,8 @@ __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
     if (!qjl) return;
     __syncthreads();
     // z_j = sum_i S[j][i] r_i for j = 32 warp + lane; bit j = [z_j >= 0]
-    float z = 0.f;
+    // (four partial sums: four short dependency chains instead of one of d)
+    float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int q0 = 0; q0 < D / 8; q0 += kChunk) {
         if (q0 > 0) {
@@ -458,16 +459,17 @@ __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
             const float4 ra = *reinterpret_cast<const float4*>(&r_s[8 * (q0 + q)]);
             const float4 rb = *reinterpret_cast<const float4*>(&r_s[8 * (q0 + q) + 4]);
             const uint4 u = sv[q];
-            z = fmaf(__uint_as_float(u.x << 16), ra.x, z);
-            z = fmaf(__uint_as_float(u.x & 0xFFFF0000u), ra.y, z);
-            z = fmaf(__uint_as_float(u.y << 16), ra.z, z);
-            z = fmaf(__uint_as_float(u.y & 0xFFFF0000u), ra.w, z);
-            z = fmaf(__uint_as_float(u.z << 16), rb.x, z);
-            z = fmaf(__uint_as_float(u.z & 0xFFFF0000u), rb.y, z);
-            z = fmaf(__uint_as_float(u.w << 16), rb.z, z);
-            z = fmaf(__uint_as_float(u.w & 0xFFFF0000u), rb.w, z);
+            z4[0] = fmaf(__uint_as_float(u.x << 16), ra.x, z4[0]);
+            z4[0] = fmaf(__uint_as_float(u.x & 0xFFFF0000u), ra.y, z4[0]);
+            z4[1] = fmaf(__uint_as_float(u.y << 16), ra.z, z4[1]);
+            z4[1] = fmaf(__uint_as_float(u.y & 0xFFFF0000u), ra.w, z4[1]);
+            z4[2] = fmaf(__uint_as_float(u.z << 16), rb.x, z4[2]);
+            z4[2] = fmaf(__uint_as_float(u.z & 0xFFFF0000u), rb.y, z4[2]);
+            z4[3] = fmaf(__uint_as_float(u.w << 16), rb.z, z4[3]);
+            z4[3] = fmaf(__uint_as_float(u.w & 0xFFFF0000u), rb.w, z4[3]);
         }
     }
+    const float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
     const uint32_t bits = __ballot_sync(0xffffffffu, z >= 0.f);
     if (lane == 0) reinterpret_cast<uint32_t*>(page + L.k_signs + row * (D / 8))[warp] = bits;
     if (threadIdx.x == 0) reinterpret_cast<__half*>(page + L.k_rnorm)[row] = __float2half_rn(rho_s);
