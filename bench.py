@@ -62,6 +62,8 @@ def _args():
     p.add_argument("--no-boundary-cases", action="store_true")
     p.add_argument("--store-only", action="store_true",
                    help="time only the store workload and print its line (a profiling entry point)")
+    p.add_argument("--extend-only", action="store_true",
+                   help="time only the extend workload and print its line (a profiling entry point)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -648,6 +650,12 @@ def run_ours(args):
         w = wl.scaled(w, k_bits=args.k_bits)
     if args.codebook != "lloyd":
         w = wl.scaled(w, k_codebook=args.codebook, v_codebook=args.codebook if w.v_mode == "mse" else "lloyd")
+    if args.extend_only:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        line = _extend_workload(torch, tq, wl, device, max(1, args.steps), max(3, args.warmup), flush)
+        if rank == 0:
+            print(json.dumps({"extend_workload": line}), flush=True)
+        return
     if args.store_only:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         line, _ = _store_workload(torch, tq, wl, device, max(1, args.steps), max(3, args.warmup), flush,

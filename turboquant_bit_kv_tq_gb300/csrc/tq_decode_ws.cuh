@@ -90,8 +90,8 @@ __host__ __device__ inline WsLayout ws_layout(int page_bytes, const DecodeGeom& 
     off = up(off + (size_t)stages * 4);
     l.bars = off;
     off = up(off + (size_t)(2 * stages + 10) * 8);
-    l.tslot = off;
-    off = up(off + 4);
+    l.tslot = off;  // the tensor-memory address, then 4 ints of the located first item
+    off = up(off + 20);
     l.total = off;
     return l;
 }
@@ -117,24 +117,17 @@ __device__ __forceinline__ int ws_seq_chunks(const DecodeArgs& a, int len) {
 // consecutive splits of one head group, which its consumers merge as one (the
 // other head group's CTAs, a few positions on, read the same pages at about
 // the same time and find them in L2)
-__device__ inline int ws_item_count(const DecodeArgs& a) {
-    int n = 0;
-    for (int b = 0; b < a.batch; ++b) {
-        bool bad;
-        n += a.heads * a.gm.nhg * ws_seq_chunks(a, ws_seq_len(a, b, &bad));
-    }
-    return n;
+// items of sequence b: its non-empty splits x KV heads x head groups
+__device__ __forceinline__ int ws_seq_items(const DecodeArgs& a, int b) {
+    bool bad;
+    return a.heads * a.gm.nhg * ws_seq_chunks(a, ws_seq_len(a, b, &bad));
 }
-__device__ inline WsItem ws_item(const DecodeArgs& a, int idx, bool* len_bad) {
+// item idx_in_seq (in the order above) of sequence b
+__device__ inline WsItem ws_item_at(const DecodeArgs& a, int b, int idx) {
     WsItem it;
+    bool bad;
     const int nhg = a.gm.nhg;
-    int b = 0, len = 0, nch = 0;
-    for (;; ++b) {
-        len = ws_seq_len(a, b, len_bad);
-        nch = ws_seq_chunks(a, len);
-        if (idx < a.heads * nhg * nch || b == a.batch - 1) break;
-        idx -= a.heads * nhg * nch;
-    }
+    const int len = ws_seq_len(a, b, &bad), nch = ws_seq_chunks(a, len);
     it.b = b;
     it.chunk = idx % nch;
     idx /= nch;
@@ -144,7 +137,61 @@ __device__ inline WsItem ws_item(const DecodeArgs& a, int idx, bool* len_bad) {
     it.t1 = min(len, it.t0 + a.split_blocks * kBlock);
     it.n_pages = it.t1 > it.t0 ? (it.t1 - it.t0 + kBlock - 1) / kBlock : 0;
     it.n_tiles = (it.n_pages + kTilePages - 1) / kTilePages;
+    it.slot = it.load = it.lidx = it.release = 0;
     return it;
+}
+// Warp-cooperative, every lane returning the same values: the launch's item
+// count, the items per CTA for `grid` CTAs, and for item `first` of CTA cta
+// the sequence that holds it and that sequence's first item index (lanes
+// read 32 sequences' lengths at a time; two passes over the batch).
+struct WsLocate {
+    int n_items, per_cta, b0, base0;
+};
+__device__ inline WsLocate ws_warp_locate(const DecodeArgs& a, int cta, int grid, int lane) {
+    WsLocate r;
+    int total = 0;
+    for (int c = 0; c < a.batch; c += 32) {
+        int n = c + lane < a.batch ? ws_seq_items(a, c + lane) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+        total += n;
+    }
+    r.n_items = total;
+    r.per_cta = ws_items_per_cta(total, grid);
+    const int first = cta * r.per_cta;
+    r.b0 = a.batch;
+    r.base0 = total;
+    int base = 0;
+    for (int c = 0; c < a.batch && first < total; c += 32) {
+        const int n = c + lane < a.batch ? ws_seq_items(a, c + lane) : 0;
+        int incl = n;  // inclusive prefix over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const bool hit = n > 0 && first >= base + incl - n && first < base + incl;
+        const uint32_t m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+            const int l = __ffs(m) - 1;
+            r.b0 = c + l;
+            r.base0 = base + __shfl_sync(0xffffffffu, incl - n, l);
+            break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return r;
+}
+// item idx of the launch, found by walking forward from sequence b (whose
+// first item index is base, with base <= idx)
+__device__ inline WsItem ws_item_from(const DecodeArgs& a, int b, int base, int idx) {
+    for (;;) {
+        const int n = ws_seq_items(a, b);
+        if (idx < base + n || b == a.batch - 1) break;
+        base += n;
+        ++b;
+    }
+    return ws_item_at(a, b, idx - base);
 }
 
 // non-blocking: has the phase of the given parity completed?
@@ -300,10 +347,6 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     // shared-memory arrays hold KI items (every split of every head group);
     // the non-empty ones are dealt out KR per CTA
     const int KI = ws_items_per_cta(a.batch * a.heads * gm.nhg * a.sp.n_chunks, gridDim.x);
-    const int n_items = ws_item_count(a);
-    const int KR = ws_items_per_cta(n_items, gridDim.x);
-    const int k0 = blockIdx.x * KR;                 // this CTA's first item
-    const int nk = max(0, min(KR, n_items - k0));  // and its item count
     const WsLayout sl = ws_layout<D>(L.page_bytes, gm, NSET, S, KI, a.split_blocks);
     uint8_t* ring = smem + sl.ring;
     uint8_t* bimg = smem + sl.bimg;
@@ -326,6 +369,11 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     uint32_t* smask = reinterpret_cast<uint32_t*>(smem + sl.smask);  // [stage] pages copied
     auto B = [&](const uint64_t* p) { return smem_u32(p); };
 
+    // Thread 0 initialises the barriers; warp 8 locates the CTA's first item
+    // (a warp-cooperative scan of the lengths instead of a walk over every
+    // sequence per item).  loc: [items, items per CTA, first item's sequence,
+    // that sequence's first item].
+    int* loc = reinterpret_cast<int*>(smem + sl.tslot) + 1;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(B(&full[s]), 1);
@@ -342,16 +390,29 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
         mbar_init(B(dfree), 4);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 8) {
+        const WsLocate w = ws_warp_locate(a, blockIdx.x, gridDim.x, lane);
+        if (lane == 0) {
+            loc[0] = w.n_items;
+            loc[1] = w.per_cta;
+            loc[2] = w.b0;
+            loc[3] = w.base0;
+        }
+    }
     if (warp == 0) tmem_alloc(tslot, kWsTmemCols);
     pdl_launch_dependents();
+    __syncthreads();  // the barriers and the located first item
+    const int n_items = loc[0], KR = loc[1];
+    const int k0 = blockIdx.x * KR;                 // this CTA's first item
+    const int nk = max(0, min(KR, n_items - k0));  // and its item count
 
     // prologue: this CTA's items, their per-head constants and block ids into
     // shared memory (batches of independent loads), so that the tile loop
     // below makes no global loads
     const int hc = gm.hc, SB = a.split_blocks;
-    for (int k = tid; k < nk; k += blockDim.x) {
-        bool bad = false;
-        items[k] = ws_item(a, k0 + k, &bad);
+    {
+        const int b0 = loc[2], base0 = loc[3];
+        for (int k = tid; k < nk; k += blockDim.x) items[k] = ws_item_from(a, b0, base0, k0 + k);
     }
     if (blockIdx.x == 0)
         for (int b = tid; b < a.batch; b += blockDim.x) {
@@ -378,44 +439,40 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
             last[sl_] = k;
         }
     }
-    pdl_wait();  // the query prep's results (and, through it, the stored pages)
-    for (int base = tid; base < nk * H4 * 4; base += blockDim.x * 4) {
-        float v[4];
+    pdl_wait();  // the query prep's results
+    {
+        // the items' per-head constants (from the prep) and block ids, their
+        // loads issued together
+        const int n_cst = nk * H4 * 4, n_ids = nk * SB, n_all = max(n_cst, n_ids);
+        for (int base = tid; base < n_all; base += blockDim.x * 4) {
+            float cv[4];
+            int32_t iv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = base + u * blockDim.x;
-            v[u] = 0.f;
-            if (e < nk * H4 * 4) {
-                const WsItem& it = items[e / (H4 * 4)];
-                const int h = (e >> 2) % H4;
-                if (h < hc) v[u] = a.ws_cst[((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc + h) * 4 + (e & 3)];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = base + u * blockDim.x;
-            if (e < nk * H4 * 4) icst[e] = v[u];
-        }
-    }
-    for (int base = tid; base < nk * SB; base += blockDim.x * 8) {
-        int32_t v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = base + u * blockDim.x;
-            v[u] = -1;
-            if (e < nk * SB) {
-                const WsItem& it = items[e / SB];
-                const int pg = e % SB;
-                if (pg < it.n_pages) {
-                    const int row = a.row_of ? a.row_of[it.b] : it.b;
-                    v[u] = a.block_table[(int64_t)row * a.max_blocks + it.t0 / kBlock + pg];
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * blockDim.x;
+                cv[u] = 0.f;
+                iv[u] = -1;
+                if (e < n_cst) {
+                    const WsItem& it = items[e / (H4 * 4)];
+                    const int h = (e >> 2) % H4;
+                    if (h < hc)
+                        cv[u] = a.ws_cst[((int64_t)it.b * a.q_heads + it.g * a.group + it.hgi * hc + h) * 4 + (e & 3)];
+                }
+                if (e < n_ids) {
+                    const WsItem& it = items[e / SB];
+                    const int pg = e % SB;
+                    if (pg < it.n_pages) {
+                        const int row = a.row_of ? a.row_of[it.b] : it.b;
+                        iv[u] = a.block_table[(int64_t)row * a.max_blocks + it.t0 / kBlock + pg];
+                    }
                 }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = base + u * blockDim.x;
-            if (e < nk * SB) ids[e] = v[u];
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * blockDim.x;
+                if (e < n_cst) icst[e] = cv[u];
+                if (e < n_ids) ids[e] = iv[u];
+            }
         }
     }
     tc_fence_before();
