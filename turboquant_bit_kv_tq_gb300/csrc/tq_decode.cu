@@ -72,7 +72,7 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         // in stream order (overlapping it with a preceding store measured
         // slower)
         a.pdl = ev0 == nullptr && ev1 == nullptr;
-        const cudaError_t e = launch_pdl(false, prep_kernel<D>, dim3(a.heads, a.batch), dim3(256), prep_smem, s, a);
+        const cudaError_t e = launch_pdl(false, prep_kernel<D>, dim3(a.heads, a.batch), dim3(kPrepThreads), prep_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {

@@ -184,8 +184,9 @@ __host__ __device__ constexpr size_t prep_smem_bytes(int G) {
     return (size_t)D * D * 2 + (size_t)3 * G * D * 4 + 2 * kMaxG * 4 + 16;
 }
 
+constexpr int kPrepThreads = 512;  // one CTA per (sequence, KV head): its phases are short serial chains
 template <int D>
-__global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     pdl_launch_dependents();  // the split kernel's prologue may start
     const int g = blockIdx.x, b = blockIdx.y;
     if (b >= a.batch) return;
@@ -217,14 +218,34 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
     __syncthreads();
     const float f = a.scale_log2e;
+    // per-head sums and maxima for the constants below, taken where the values
+    // are made: [head][0..2] sum, sum over i % 8 = 7, max of |v| bit_weight(i % 8)
+    // of R q (one entry per head) and of S q (one entry per warp of the head)
+    constexpr int kSqWarps = D / 64;  // warps per head in the S q phase
+    __shared__ float red_r[kMaxG][3], red_s[kMaxG][kSqWarps][3];
     // R q by an in-warp Hadamard transform (one warp per head)
     for (int h = warp; h < G; h += nwarps) {
         float x[D / 32];
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) x[k] = qv[h * D + lane + 32 * k] * s_signs[lane + 32 * k];
         fwht_warp<D / 32>(x, lane);
+        const float bw = fabsf(bit_weight(lane & 7));  // i % 8 = lane % 8 for i = lane + 32 k
+        float s0 = 0.f, m0 = 0.f;
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) rq[h * D + lane + 32 * k] = x[k] * rsqrtf((float)D) * f;
+        for (int k = 0; k < D / 32; ++k) {
+            const float r = x[k] * rsqrtf((float)D) * f;
+            rq[h * D + lane + 32 * k] = r;
+            s0 += r;
+            m0 = fmaxf(m0, fabsf(r) * bw);
+        }
+        const float s7 = warp_sum((lane & 7) == 7 ? s0 : 0.f);
+        s0 = warp_sum(s0);
+        m0 = warp_max(m0);
+        if (lane == 0) {
+            red_r[h][0] = s0;
+            red_r[h][1] = s7;
+            red_r[h][2] = m0;
+        }
     }
     // S q from the shared copy of S^T: thread (column pair j, j + 1; head h),
     // 32-bit loads of S^T pairs and 128-bit loads of four query elements
@@ -232,7 +253,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
     const float kq = f * sqrtf(1.5707963267948966f) / (float)D;
     {
         constexpr int NP = D / 2;            // column pairs
-        constexpr int HS = 256 / NP;         // heads covered per pass (4 at d=128, 2 at d=256)
+        constexpr int HS = kPrepThreads / NP;  // heads covered per pass (8 at d=128, 4 at d=256)
         const int jp = tid % NP, h0 = tid / NP;
         for (int h = h0; h < G; h += HS) {
             float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};  // two partial sums per column
@@ -250,8 +271,20 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
                     }
                 }
             }
-            sq[h * D + 2 * jp] = (s0[0] + s0[1]) * kq;
-            sq[h * D + 2 * jp + 1] = (s1[0] + s1[1]) * kq;
+            const float v0 = (s0[0] + s0[1]) * kq, v1 = (s1[0] + s1[1]) * kq;
+            sq[h * D + 2 * jp] = v0;
+            sq[h * D + 2 * jp + 1] = v1;
+            // columns 2jp (i % 8 even) and 2jp + 1 (i % 8 = 7 when jp % 4 = 3)
+            float sum = warp_sum(v0 + v1);
+            float s7 = warp_sum((jp & 3) == 3 ? v1 : 0.f);
+            float mx = warp_max(fmaxf(fabsf(v0) * fabsf(bit_weight((2 * jp) & 7)),
+                                      fabsf(v1) * fabsf(bit_weight((2 * jp + 1) & 7))));
+            if (lane == 0) {
+                const int wh = (jp >> 5);  // this warp's place among the head's warps
+                red_s[h][wh][0] = sum;
+                red_s[h][wh][1] = s7;
+                red_s[h][wh][2] = mx;
+            }
         }
     }
     // a copy that never completed must land before the block exits
@@ -272,26 +305,17 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeArgs a) {
         bmax = fmaxf(bmax, fabsf(kw[1 + p]));
         bsum += kw[1 + p];
     }
-    for (int h = warp; h < G; h += nwarps) {
-        float s_rq = 0.f, s_rq7 = 0.f, s_sq = 0.f, s_sq7 = 0.f, m_rq = 0.f, m_sq = 0.f;
-        for (int i = lane; i < D; i += 32) {
-            const float r = rq[h * D + i], sv = sq[h * D + i];
-            s_rq += r;
-            s_sq += sv;
-            if ((i & 7) == 7) {
-                s_rq7 += r;
-                s_sq7 += sv;
-            }
-            m_rq = fmaxf(m_rq, fabsf(r) * fabsf(bit_weight(i & 7)));
-            m_sq = fmaxf(m_sq, fabsf(sv) * fabsf(bit_weight(i & 7)));
+    for (int h = tid; h < G; h += blockDim.x) {
+        const float s_rq = red_r[h][0], s_rq7 = red_r[h][1], m_rq = red_r[h][2] * bmax;
+        float s_sq = 0.f, s_sq7 = 0.f, m_sq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSqWarps; ++w) {
+            s_sq += red_s[h][w][0];
+            s_sq7 += red_s[h][w][1];
+            m_sq = fmaxf(m_sq, red_s[h][w][2]);
         }
-        s_rq = warp_sum(s_rq);
-        s_rq7 = warp_sum(s_rq7);
-        s_sq = warp_sum(s_sq);
-        s_sq7 = warp_sum(s_sq7);
-        m_rq = warp_max(m_rq) * bmax;
-        m_sq = warp_max(m_sq) * 2.f;
-        if (lane == 0) {
+        m_sq *= 2.f;
+        {
             // operand scales 2^e with 2^e m <= 224 (e4m3 holds up to 448): e is
             // the binary exponent of 224 / m, read from its float bits
             auto scale_exp = [](float m) {
