@@ -1422,44 +1422,65 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     // sequence's length are empty and need not have been written.
     const int len = max(0, min(a.seq_lens[b], a.max_blocks * kBlock));
     const int nch = (len + a.split_blocks * kBlock - 1) / (a.split_blocks * kBlock);
-    float M = -INFINITY;
-    for (int s = tid; s < S; s += 128) {
-        const float m = (s < a.sp.n_chunks && s >= nch) ? -INFINITY : a.ws_ml[(base + s) * 2];
-        wgt[s] = m;
-        M = fmaxf(M, m);
-    }
-    M = warp_max(M);
-    if (lane == 0) red[0][warp] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    float lpart = 0.f;
-    for (int s = tid; s < S; s += 128) {
-        const float m = wgt[s];
-        const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);  // empty split: 0
-        wgt[s] = w;
-        if (w > 0.f) lpart = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lpart);
-    }
-    lpart = warp_sum(lpart);
-    if (lane == 0) red[1][warp] = lpart;
-    __syncthreads();
-    const float lsum = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+    float lsum;
     float acc[kPerThread];
 #pragma unroll
     for (int p = 0; p < kPerThread; ++p) acc[p] = 0.f;
-    // an empty split (weight 0) may leave its partial unwritten: skip it
+    if (S <= 32) {
+        // one split per lane: every warp finds M, the weights and their sum
+        // itself, with no barrier (the same arithmetic as below)
+        float m = -INFINITY, l = 0.f;
+        if (lane < S && !(lane < a.sp.n_chunks && lane >= nch)) {
+            m = a.ws_ml[(base + lane) * 2];
+            l = a.ws_ml[(base + lane) * 2 + 1];
+        }
+        const float M = warp_max(m);
+        const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);  // empty split: 0
+        lsum = warp_sum(w > 0.f ? fmaf(w, l, 0.f) : 0.f);
+        // an empty split (weight 0) may leave its partial unwritten: skip it
 #pragma unroll
-    for (int s = 0; s < kPre; ++s) {
-        const float w = s < S ? wgt[s] : 0.f;
+        for (int s = 0; s < kPre; ++s) {
+            const float ws = __shfl_sync(0xffffffffu, w, s);
 #pragma unroll
-        for (int p = 0; p < kPerThread; ++p) acc[p] = w > 0.f ? fmaf(w, pre[s][p], acc[p]) : acc[p];
-    }
+            for (int p = 0; p < kPerThread; ++p) acc[p] = ws > 0.f ? fmaf(ws, pre[s][p], acc[p]) : acc[p];
+        }
+    } else {
+        float M = -INFINITY;
+        for (int s = tid; s < S; s += 128) {
+            const float m = (s < a.sp.n_chunks && s >= nch) ? -INFINITY : a.ws_ml[(base + s) * 2];
+            wgt[s] = m;
+            M = fmaxf(M, m);
+        }
+        M = warp_max(M);
+        if (lane == 0) red[0][warp] = M;
+        __syncthreads();
+        M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+        float lpart = 0.f;
+        for (int s = tid; s < S; s += 128) {
+            const float m = wgt[s];
+            const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);  // empty split: 0
+            wgt[s] = w;
+            if (w > 0.f) lpart = fmaf(w, a.ws_ml[(base + s) * 2 + 1], lpart);
+        }
+        lpart = warp_sum(lpart);
+        if (lane == 0) red[1][warp] = lpart;
+        __syncthreads();
+        lsum = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+        // an empty split (weight 0) may leave its partial unwritten: skip it
+#pragma unroll
+        for (int s = 0; s < kPre; ++s) {
+            const float w = wgt[s];
+#pragma unroll
+            for (int p = 0; p < kPerThread; ++p) acc[p] = w > 0.f ? fmaf(w, pre[s][p], acc[p]) : acc[p];
+        }
 #pragma unroll 8
-    for (int s = kPre; s < S; ++s) {
-        const float w = wgt[s];
+        for (int s = kPre; s < S; ++s) {
+            const float w = wgt[s];
 #pragma unroll
-        for (int p = 0; p < kPerThread; ++p) {
-            const float v = src[(int64_t)s * D + 128 * p];
-            acc[p] = w > 0.f ? fmaf(w, v, acc[p]) : acc[p];
+            for (int p = 0; p < kPerThread; ++p) {
+                const float v = src[(int64_t)s * D + 128 * p];
+                acc[p] = w > 0.f ? fmaf(w, v, acc[p]) : acc[p];
+            }
         }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
