@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libtq_gb300.so")
 SOURCES = ["tq_host.cpp", "tq_store.cu", "tq_store_tc.cu", "tq_decode.cu", "tq_decode_noalloc.cu"] + [
     f"tq_decode_split_{d}_{kb}.cu" for d in (128, 256) for kb in (2, 3, 4)
-] + ["tq_decode_split_128_3u.cu"]
+] + ["tq_decode_split_128_3u.cu"] + [f"tq_extend_prefix_{k}.cu" for k in ("2", "3", "3u", "4u")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

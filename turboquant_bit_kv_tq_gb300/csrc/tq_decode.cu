@@ -3,9 +3,23 @@
 
 #include <algorithm>
 
-#include "tq_decode_ws.cuh"
+#include "tq_extend_prefix.cuh"
 
 namespace tq {
+
+// The score geometry the warp-specialized split kernel and the extend prefix
+// kernel run with: a uniform key codebook expands over its k_bits single-bit
+// planes only (every multi-bit Walsh term is zero), so its score contraction
+// is shorter; both kernels have instances for that at d = 128.
+static DecodeGeom ws_geom(const DecodeGeom& g, const Layout& L, bool k_uniform) {
+    DecodeGeom gw = g;
+    if (L.d == 128 && k_uniform && gw.npk > L.k_bits) {
+        gw.npk = L.k_bits;
+        gw.npl = gw.npk + (L.k_qjl ? 1 : 0);
+        gw.bimg_bytes = gw.n_cols * gw.npl * L.d;
+    }
+    return gw;
+}
 
 template <int D>
 static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) {
@@ -21,16 +35,14 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     }
     size_t smem = 0;
     int grid = 0;
-    // a uniform key codebook expands over its k_bits single-bit planes only
-    // (every multi-bit Walsh term is zero), so its score contraction is
-    // shorter; the warp-specialized kernel has instances for that at d = 128
-    DecodeGeom gw = a.gm;
-    if (D == 128 && a.k_uniform && gw.npk > a.lay.k_bits) {
-        gw.npk = a.lay.k_bits;
-        gw.npl = gw.npk + (a.lay.k_qjl ? 1 : 0);
-        gw.bimg_bytes = gw.n_cols * gw.npl * D;
-    }
-    if (ws_fits(gw, D)) {
+    const DecodeGeom gw = ws_geom(a.gm, a.lay, a.k_uniform);
+    // extend with a query-block plan: the compressed prefix of every block in
+    // one GEMM-shaped pass (extend_prefix_kernel), no split kernel
+    const bool xp = D == 128 && a.xblocks != nullptr && xp_supported(gw, D) &&
+                    xp_layout(a.lay.page_bytes, gw.bimg_bytes).total <= 227 * 1024;
+    if (xp) {
+        a.gm = gw;
+    } else if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel
         const int n_items = a.batch * a.heads * a.gm.nhg * a.sp.n_chunks;
@@ -48,7 +60,7 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         if (a.stages == 0) grid = 0;  // too many items per CTA for the staged schedule
         if (grid > 0) a.gm = gw;      // (the other kernels keep every plane)
     }
-    if (grid == 0) {
+    if (grid == 0 && !xp) {
         const tq_status cfg = split_config<D>(a, &a.stages, &smem);
         if (cfg != TQ_OK) return cfg;
     }
@@ -82,10 +94,27 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     }
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);
     tq_status st;
-    switch (a.lay.k_bits) {
-        case 2: st = dispatch_split<D, 2>(a, s, smem, grid); break;
-        case 3: st = dispatch_split<D, 3>(a, s, smem, grid); break;
-        default: st = dispatch_split<D, 4>(a, s, smem, grid); break;
+    if (xp) {
+        // enough CTAs (one per SM at least) that none takes more than
+        // kXpMaxItems items
+        const int64_t ub = (int64_t)a.xblocks_max * a.heads * a.gm.nhg * a.sp.n_chunks;
+        const int64_t xg = std::min<int64_t>(ub, std::max<int64_t>(sms, (ub + kXpMaxItems - 1) / kXpMaxItems));
+        if (xg <= 0) {
+            st = TQ_OK;
+        } else {
+            const int kb = a.lay.k_bits;
+            const bool ku = a.gm.npk == kb && kb >= 3;
+            st = kb == 2 ? dispatch_extend_prefix<2, false>(a, s, (int)xg)
+               : kb == 3 ? (ku ? dispatch_extend_prefix<3, true>(a, s, (int)xg)
+                               : dispatch_extend_prefix<3, false>(a, s, (int)xg))
+                         : dispatch_extend_prefix<4, true>(a, s, (int)xg);
+        }
+    } else {
+        switch (a.lay.k_bits) {
+            case 2: st = dispatch_split<D, 2>(a, s, smem, grid); break;
+            case 3: st = dispatch_split<D, 3>(a, s, smem, grid); break;
+            default: st = dispatch_split<D, 4>(a, s, smem, grid); break;
+        }
     }
     if (st != TQ_OK) return st;
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
@@ -210,6 +239,89 @@ __global__ void extend_entries_kernel(const int32_t* __restrict__ prefix_lens, c
     tail_base[t] = start;
 }
 
+// One CTA: extend's query blocks for the prefix kernel.  The chunk of
+// sequence b (rows cu_q[b] .. cu_q[b+1] - 1), when b has a compressed prefix,
+// splits into blocks of up to tpb consecutive new tokens; blocks[k] = {first
+// row, rows, b, index of the block's first prefix work item}, a block having
+// hn x (the prefix's non-empty splits) items.  counts = {blocks, items}.  A
+// cu_q that decreases or leaves [0, n_tokens] sets TQ_DEVERR_CHUNK and its
+// chunks are clamped; if the blocks would then exceed the capacity cap, the
+// plan is left empty (no prefix work) with the same error.
+__global__ void __launch_bounds__(1024) extend_blocks_kernel(const int32_t* __restrict__ prefix_lens,
+                                                             const int32_t* __restrict__ cu_q, int batch,
+                                                             int n_tokens, int tpb, int hn, int split_tokens,
+                                                             int max_len, int cap, int4* blocks, int32_t* counts,
+                                                             uint32_t* err) {
+    __shared__ int wsum[2][32];
+    __shared__ int carry[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    if (tid == 0) carry[0] = carry[1] = 0;
+    __syncthreads();
+    for (int base = 0; base < batch; base += blockDim.x) {
+        const int b = base + tid;
+        int lo = 0, chunk = 0, ns = 0, nb = 0, ni = 0;
+        if (b < batch) {
+            int l0 = cu_q[b], l1 = cu_q[b + 1];
+            if (l0 < 0 || l1 < l0 || l1 > n_tokens) {
+                set_error(err, TQ_DEVERR_CHUNK);
+                l0 = min(max(l0, 0), n_tokens);
+                l1 = min(max(l1, l0), n_tokens);
+            }
+            lo = l0;
+            chunk = l1 - l0;
+            const int len = min(max(prefix_lens[b], 0), max_len);
+            ns = (len + split_tokens - 1) / split_tokens;
+            nb = ns > 0 ? (chunk + tpb - 1) / tpb : 0;
+            ni = nb * hn * ns;
+        }
+        // block-wide inclusive scans of the block and item counts
+        int sb = nb, si = ni;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int xb = __shfl_up_sync(0xffffffffu, sb, o), xi = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) {
+                sb += xb;
+                si += xi;
+            }
+        }
+        if (lane == 31) {
+            wsum[0][warp] = sb;
+            wsum[1][warp] = si;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int vb = lane < nw ? wsum[0][lane] : 0, vi = lane < nw ? wsum[1][lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int xb = __shfl_up_sync(0xffffffffu, vb, o), xi = __shfl_up_sync(0xffffffffu, vi, o);
+                if (lane >= o) {
+                    vb += xb;
+                    vi += xi;
+                }
+            }
+            wsum[0][lane] = vb;
+            wsum[1][lane] = vi;
+        }
+        __syncthreads();
+        const int bb = carry[0] + (warp ? wsum[0][warp - 1] : 0) + sb - nb;
+        const int ib = carry[1] + (warp ? wsum[1][warp - 1] : 0) + si - ni;
+        for (int j = 0; j < nb; ++j)
+            if (bb + j < cap) blocks[bb + j] = make_int4(lo + tpb * j, min(tpb, chunk - tpb * j), b, ib + j * hn * ns);
+        __syncthreads();
+        if (tid == 0) {
+            carry[0] += wsum[0][nw - 1];
+            carry[1] += wsum[1][nw - 1];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const bool over = carry[0] > cap;
+        if (over) set_error(err, TQ_DEVERR_CHUNK);
+        counts[0] = over ? 0 : carry[0];
+        counts[1] = over ? 0 : carry[1];
+    }
+}
+
 }  // namespace tq
 
 extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q_dtype, const void* cache_buf,
@@ -273,6 +385,21 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
     a.ws_cst = c->ws_cst;
     a.ws_acc = c->ws_acc;
     a.ws_ml = c->ws_ml;
+    // d = 128 with full head groups: the query-block plan of the prefix
+    // kernel (launch_decode runs it when the score planes fit)
+    const DecodeGeom gw = ws_geom(a.gm, a.lay, a.k_uniform);
+    if (xp_supported(gw, d)) {
+        const int tpb = xp_block_tokens(gw.nhg);
+        a.xcounts = tail_base + B;
+        a.xblocks = reinterpret_cast<const int4*>(tail_base + B + 4);
+        a.xblocks_max = std::min(n_tokens, (n_tokens + tpb - 1) / tpb + batch);
+        extend_blocks_kernel<<<1, 1024, 0, s>>>(prefix_lens, cu_q, batch, n_tokens, tpb, a.heads * gw.nhg,
+                                                a.split_blocks * kBlock, a.max_blocks * kBlock, B,
+                                                const_cast<int4*>(a.xblocks), const_cast<int32_t*>(a.xcounts),
+                                                c->dp.err);
+        const tq_status st = cuda_status(cudaGetLastError());
+        if (st != TQ_OK) return st;
+    }
     return launch_decode(a, s, c->prof_start[TQ_PROF_DECODE_SPLIT], c->prof_stop[TQ_PROF_DECODE_SPLIT]);
 }
 

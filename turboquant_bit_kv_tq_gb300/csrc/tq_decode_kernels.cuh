@@ -68,6 +68,12 @@ struct DecodeArgs {
     const int32_t* row_of = nullptr;
     const int32_t* tail_base = nullptr;
     bool chunk_attn = false;  // the tail partials come from chunk_attn_kernel
+    // extend: query blocks {first entry, entries, sequence, index of the
+    // block's first prefix work item} and {block count, item count} for
+    // extend_prefix_kernel (null otherwise)
+    const int4* xblocks = nullptr;
+    const int32_t* xcounts = nullptr;
+    int xblocks_max = 0;  // the plan's capacity (an upper bound of the block count)
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;

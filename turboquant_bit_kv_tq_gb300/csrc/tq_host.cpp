@@ -142,8 +142,8 @@ WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     off = up256(off + bh * s.n_splits * d * 4);
     w.ml = off;
     off = up256(off + bh * s.n_splits * 2 * 4);
-    w.ext = off;
-    off = up256(off + size_t(c.max_batch) * 4 * 4);
+    w.ext = off;  // 4 x [B] int32, 4 int32 counts, [B] int4 query blocks
+    off = up256(off + size_t(c.max_batch) * 4 * 4 + 16 + size_t(c.max_batch) * 16);
     w.total = off;
     return w;
 }
