@@ -14,25 +14,28 @@
 //   softmax  online exp2 per query head with one lazily moved reference per
 //            head for the whole CTA (a tile maximum across the 4 consumer
 //            warps); rescaling the output accumulator in tensor memory is rare
-//   P V      a second tcgen05 contraction, D[128 coordinates x 32 heads] in
+//   P V      a second tcgen05 contraction, D[128 coordinates x 64] in
 //            tensor memory: A = the tile's dequantised values (fp16 high and
 //            low parts, MN-major: token-major rows as the thread that owns a
-//            token writes them), B = the probabilities (fp16 high and low
-//            parts, MN-major); hi*hi + hi*lo + lo*hi, fp32 accumulation
+//            token writes them), B = [P_hi | P_lo], the probabilities' fp16
+//            high and low parts side by side (MN-major, N = 64); the two
+//            column halves add up at the end; fp32 accumulation
 // Every (new token, query head) of the item gets the split's partial
 // (m, l, acc) in the decode's workspace format, which the combine merges with
 // the exact causal part (chunk_attn_kernel).
 //
-// Roles (320 threads, one CTA per SM: 448 of the 512 tensor-memory columns):
-//   warps 0-3  thread t = token t of the tile: key bit-plane operands into
-//              tensor memory, then the token's dequantised value row into
-//              shared memory
+// Roles (384 threads, one CTA per SM, all 512 tensor-memory columns):
+//   warps 0-3  thread t = token t of the tile: key bit-plane operands of the
+//              next tile into tensor memory, then the token's dequantised
+//              value row of this tile into shared memory
 //   warps 4-7  same token mapping: scores out of tensor memory, softmax,
 //              probability operands; at an item's end the output accumulator
 //              (lane = coordinate) becomes the partial
 //   warp 8     bulk async copies of the pages (ring of stages) and of the
 //              block's query operand images
-//   warp 9     one thread issues the MMAs
+//   warp 9     one thread issues the MMAs: the scores of tile i + 1, then
+//              the P V of tile i
+//   warps 10-11 idle (they complete the third warpgroup's register split)
 #pragma once
 
 #include "tq_decode_ws.cuh"
@@ -42,12 +45,15 @@ namespace tq {
 constexpr int kXpImgs = 8;                 // query operand images per item (16 columns each)
 constexpr int kXpHeads = 4 * kXpImgs;      // query heads per item
 constexpr int kXpCols = 16 * kXpImgs;      // score accumulator columns (key | sign each)
-constexpr int kXpThreads = 320;
-constexpr int kXpStages = 2;
+constexpr int kXpThreads = 384;           // score/value, consumer and copy/MMA warpgroups
+constexpr int kXpStages = 3;
+// setmaxnreg split of the 3 x 168 registers per thread a CTA launches with:
+// the copy/MMA warpgroup keeps 56, the two compute warpgroups take 224 each
+constexpr int kXpRegsLaunch = 168, kXpRegsIssue = 56, kXpRegsWork = (3 * kXpRegsLaunch - kXpRegsIssue) / 2;
 constexpr int kXpMaxItems = 64;            // items per CTA at most (the launch sizes the grid for it)
 constexpr int kXpTmemCols = 512;
 constexpr int kXpColA = 2 * kXpCols;       // A operand: npl planes x 32 columns
-constexpr int kXpColO = 448;               // P V accumulator: 32 columns
+constexpr int kXpColO = 448;               // P V accumulator: 64 columns (probability high | low part)
 constexpr int kXpTileTok = kTilePages * kBlock;  // 128 prefix tokens per tile
 constexpr int kXpVBytes = kXpTileTok * 128 * 2;  // one fp16 piece of the value operand
 constexpr int kXpPBytes = kXpTileTok * kXpHeads * 2;  // one fp16 piece of the probability operand
@@ -313,6 +319,7 @@ __device__ inline int xp_items(const DecodeArgs& a, XpItem* items, int cta, int 
 
 template <int KB, bool KU, bool G32, int VB>
 __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs a) {
+    static_assert(kXpRegsWork <= 256 && kXpRegsWork % 8 == 0, "register split");
     constexpr int D = 128;
     constexpr int NPK = KU ? KB : 1 << (KB - 1);
     constexpr int NW = D / 32;
@@ -377,62 +384,64 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
     bool dead = false;
     const int hc = gm.hc;
 
-    if (warp == 8) {
-        // ------------------------------------------------------ producer
-        int tseq = 0, nimg = 0;
-        auto wait_uniform = [&](uint64_t* bar, uint32_t par) {
-            int ok = 1;
-            if (lane == 0 && !dead) ok = mbar_wait(B(bar), par, err);
-            dead = dead || __shfl_sync(0xffffffffu, ok, 0) == 0;
-        };
-        for (int k = 0; k < nk && !dead; ++k) {
-            const XpItem it = items[k];
-            if (it.n_tiles == 0) continue;
-            if (it.load) {
-                if (it.lidx >= 1) wait_uniform(ifree, (it.lidx - 1) & 1);
-                if (dead) break;
-                if (lane == 0) mbar_expect_tx(B(ifull), (uint32_t)(it.n * gm.bimg_bytes));
-                __syncwarp();
-                if (lane < it.n)
-                    bulk_copy(smem_u32(img + (size_t)lane * gm.bimg_bytes),
-                              a.ws_bimg + (((int64_t)(it.t0 + lane) * a.heads + it.g) * gm.nhg + it.hgi) * gm.bimg_bytes,
-                              gm.bimg_bytes, B(ifull));
-                ++nimg;
-            }
-            for (int t = 0; t < it.n_tiles && !dead; ++t, ++tseq) {
-                const int s = tseq % S;
-                if (tseq >= S) wait_uniform(&empty[s], ((tseq / S) - 1) & 1);
-                if (dead) break;
-                const int p0 = t * kTilePages, np = min(kTilePages, it.n_pages - p0);
-                int blk = -1;
-                if (lane < np) blk = a.block_table[(int64_t)it.b * a.max_blocks + it.p0 + p0 + lane];
-                const bool ok = lane < np && blk >= 0 && blk < a.num_blocks;
-                const uint32_t mask = __ballot_sync(0xffffffffu, ok);
-                if (lane < np && !ok) set_error(err, TQ_DEVERR_BLOCK);
-                if (lane == 0) {
-                    smask[s] = mask;
-                    mbar_expect_tx(B(&full[s]), (uint32_t)__popc(mask) * L.page_bytes);
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kXpRegsIssue));
+        if (warp == 8) {
+            // -------------------------------------------------- producer
+            int tseq = 0, nimg = 0;
+            auto wait_uniform = [&](uint64_t* bar, uint32_t par) {
+                int ok = 1;
+                if (lane == 0 && !dead) ok = mbar_wait(B(bar), par, err);
+                dead = dead || __shfl_sync(0xffffffffu, ok, 0) == 0;
+            };
+            for (int k = 0; k < nk && !dead; ++k) {
+                const XpItem it = items[k];
+                if (it.n_tiles == 0) continue;
+                if (it.load) {
+                    if (it.lidx >= 1) wait_uniform(ifree, (it.lidx - 1) & 1);
+                    if (dead) break;
+                    if (lane == 0) mbar_expect_tx(B(ifull), (uint32_t)(it.n * gm.bimg_bytes));
+                    __syncwarp();
+                    if (lane < it.n)
+                        bulk_copy(smem_u32(img + (size_t)lane * gm.bimg_bytes),
+                                  a.ws_bimg +
+                                      (((int64_t)(it.t0 + lane) * a.heads + it.g) * gm.nhg + it.hgi) * gm.bimg_bytes,
+                                  gm.bimg_bytes, B(ifull));
+                    ++nimg;
                 }
-                __syncwarp();
-                if (ok)
-                    bulk_copy(smem_u32(ring + s * sl.tile + (size_t)lane * L.page_bytes),
-                              a.cache + ((int64_t)blk * a.heads + it.g) * L.page_bytes, L.page_bytes, B(&full[s]));
+                for (int t = 0; t < it.n_tiles && !dead; ++t, ++tseq) {
+                    const int s = tseq % S;
+                    if (tseq >= S) wait_uniform(&empty[s], ((tseq / S) - 1) & 1);
+                    if (dead) break;
+                    const int p0 = t * kTilePages, np = min(kTilePages, it.n_pages - p0);
+                    int blk = -1;
+                    if (lane < np) blk = a.block_table[(int64_t)it.b * a.max_blocks + it.p0 + p0 + lane];
+                    const bool ok = lane < np && blk >= 0 && blk < a.num_blocks;
+                    const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+                    if (lane < np && !ok) set_error(err, TQ_DEVERR_BLOCK);
+                    if (lane == 0) {
+                        smask[s] = mask;
+                        mbar_expect_tx(B(&full[s]), (uint32_t)__popc(mask) * L.page_bytes);
+                    }
+                    __syncwarp();
+                    if (ok)
+                        bulk_copy(smem_u32(ring + s * sl.tile + (size_t)lane * L.page_bytes),
+                                  a.cache + ((int64_t)blk * a.heads + it.g) * L.page_bytes, L.page_bytes, B(&full[s]));
+                }
             }
-        }
-        // copies still in flight must land before the block exits
-        if (lane == 0) {
-            bool d2 = false;
-            for (int k = max(0, tseq - S); k < tseq; ++k) ws_wait(B(&full[k % S]), (k / S) & 1, d2, err);
-            if (nimg > 0) ws_wait(B(ifull), (nimg - 1) & 1, d2, err);
-        }
-    } else if (warp == 9) {
-        // --------------------------------------------------- MMA issue
-        if (lane == 0) {
+            // copies still in flight must land before the block exits
+            if (lane == 0) {
+                bool d2 = false;
+                for (int k = max(0, tseq - S); k < tseq; ++k) ws_wait(B(&full[k % S]), (k / S) & 1, d2, err);
+                if (nimg > 0) ws_wait(B(ifull), (nimg - 1) & 1, d2, err);
+            }
+        } else if (warp == 9 && lane == 0) {
+            // ----------------------------------------------- MMA issue
             const uint32_t idesc_s = fp8_idesc(kXpCols);
-            const uint32_t idesc_pv = xp_pv_idesc(kXpHeads);
+            const uint32_t idesc_pv = xp_pv_idesc(2 * kXpHeads);
             const uint32_t sbo = 8u * (uint32_t)(npl * D);
             const uint32_t vhi = smem_u32(smem + sl.vhi), vlo = smem_u32(smem + sl.vlo);
-            const uint32_t phi = smem_u32(smem + sl.phi), plo = smem_u32(smem + sl.plo);
+            const uint32_t pb = smem_u32(smem + sl.phi);  // [P_hi | P_lo]: 8 column groups
             const uint32_t dO = tmem + kXpColO;
             int tseq = 0, ki = 0;
             int pv_t = -1, pv_first = 0, pv_item = 0;  // the tile whose P V is still to issue
@@ -443,11 +452,9 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 tc_fence_after();
 #pragma unroll 1
                 for (int kk = 0; kk < kXpTileTok / 16; ++kk) {
-                    const uint64_t ah = xp_mn_desc(vhi + 256 * kk), al = xp_mn_desc(vlo + 256 * kk);
-                    const uint64_t bh = xp_mn_desc(phi + 256 * kk), bl = xp_mn_desc(plo + 256 * kk);
-                    xp_mma_ss(dO, ah, bh, idesc_pv, (pv_first && kk == 0) ? 0u : 1u);
-                    xp_mma_ss(dO, ah, bl, idesc_pv, 1u);
-                    xp_mma_ss(dO, al, bh, idesc_pv, 1u);
+                    const uint64_t bd = xp_mn_desc(pb + 256 * kk);
+                    xp_mma_ss(dO, xp_mn_desc(vhi + 256 * kk), bd, idesc_pv, (pv_first && kk == 0) ? 0u : 1u);
+                    xp_mma_ss(dO, xp_mn_desc(vlo + 256 * kk), bd, idesc_pv, 1u);
                 }
                 tc_commit(B(pvdone));
             };
@@ -474,95 +481,113 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
         }
     } else if (warp < 4) {
         // ------------------------------------- key and value operands
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kXpRegsWork));
         const int pj = tid >> 4, r = tid & 15;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const bool qjl = L.k_qjl;
         uint8_t* vh = smem + sl.vhi;
         uint8_t* vl = smem + sl.vlo;
-        int tseq = 0;
-        for (int k = 0; k < nk; ++k) {
-            const XpItem it = items[k];
-            if (it.n_tiles == 0) continue;
-            for (int t = 0; t < it.n_tiles; ++t, ++tseq) {
-                const int s = tseq % S;
-                ws_wait(B(&full[s]), (tseq / S) & 1, dead, err);
-                const int np = min(kTilePages, it.n_pages - t * kTilePages);
-                const int pos = it.tok0 + (t * kTilePages + pj) * kBlock + r;
-                const bool valid = pj < np && pos < it.tok1 && ((smask[s] >> pj) & 1);
-                const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
-                {
-                    uint32_t kw[KB][NW], sw[NW];
+        // the key operands of tile u (item k, tile t of it): they go into the
+        // single A buffer once the score MMAs of tile u - 1 are done
+        auto key_operands = [&](int u, int t) {
+            const int s = u % S;
+            ws_wait(B(&full[s]), (u / S) & 1, dead, err);
+            const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
+            uint32_t kw[KB][NW], sw[NW];
 #pragma unroll
-                    for (int p = 0; p < KB; ++p) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(pg + L.k_codes + (p * kBlock + r) * (D / 8));
-                        kw[p][0] = u.x;
-                        kw[p][1] = u.y;
-                        kw[p][2] = u.z;
-                        kw[p][3] = u.w;
-                    }
-                    {
-                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                        if (qjl) u = *reinterpret_cast<const uint4*>(pg + L.k_signs + r * (D / 8));
-                        sw[0] = u.x;
-                        sw[1] = u.y;
-                        sw[2] = u.z;
-                        sw[3] = u.w;
-                    }
-                    if (tseq >= 1) ws_wait(B(mdone), (tseq - 1) & 1, dead, err);  // A operand free
-                    tc_fence_after();
-                    const uint32_t abase = tmem + lane_base + kXpColA;
-#pragma unroll
-                    for (int P = 0; P <= NPK; ++P) {
-                        if (P == NPK && !qjl) break;
-                        uint32_t a32[32];
-#pragma unroll
-                        for (int w = 0; w < NW; ++w) {
-                            uint32_t x = 0;
-                            if (P < NPK) {
-#pragma unroll
-                                for (int p = 0; p < KB; ++p)
-                                    if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w];
-                            } else {
-                                x = sw[w];
-                            }
-                            a32[8 * w + 0] = bit_operand<0>(x);
-                            a32[8 * w + 1] = bit_operand<1>(x);
-                            a32[8 * w + 2] = bit_operand<2>(x);
-                            a32[8 * w + 3] = bit_operand<3>(x);
-                            a32[8 * w + 4] = bit_operand<4>(x);
-                            a32[8 * w + 5] = bit_operand<5>(x);
-                            a32[8 * w + 6] = bit_operand<6>(x);
-                            a32[8 * w + 7] = bit_operand<7>(x);
-                        }
-                        tmem_st32(abase + P * NCOL, a32);
-                    }
-                    tc_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B(aready));
-                }
-                // the token's value row, dequantised, as fp16 high and low parts
-                if (tseq >= 1) ws_wait(B(pvdone), (tseq - 1) & 1, dead, err);  // value operand free
-                xp_value_row<G32, VB>(pg, r, valid, L, vcent, vh, vl, tid);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(B(vready));
-                    mbar_arrive(B(&empty[s]));
-                }
+            for (int p = 0; p < KB; ++p) {
+                const uint4 v4 = *reinterpret_cast<const uint4*>(pg + L.k_codes + (p * kBlock + r) * (D / 8));
+                kw[p][0] = v4.x;
+                kw[p][1] = v4.y;
+                kw[p][2] = v4.z;
+                kw[p][3] = v4.w;
             }
+            {
+                uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+                if (qjl) v4 = *reinterpret_cast<const uint4*>(pg + L.k_signs + r * (D / 8));
+                sw[0] = v4.x;
+                sw[1] = v4.y;
+                sw[2] = v4.z;
+                sw[3] = v4.w;
+            }
+            (void)t;
+            if (u >= 1) ws_wait(B(mdone), (u - 1) & 1, dead, err);  // A operand free
+            tc_fence_after();
+            const uint32_t abase = tmem + lane_base + kXpColA;
+#pragma unroll
+            for (int P = 0; P <= NPK; ++P) {
+                if (P == NPK && !qjl) break;
+                uint32_t a32[32];
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    uint32_t x = 0;
+                    if (P < NPK) {
+#pragma unroll
+                        for (int p = 0; p < KB; ++p)
+                            if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w];
+                    } else {
+                        x = sw[w];
+                    }
+                    a32[8 * w + 0] = bit_operand<0>(x);
+                    a32[8 * w + 1] = bit_operand<1>(x);
+                    a32[8 * w + 2] = bit_operand<2>(x);
+                    a32[8 * w + 3] = bit_operand<3>(x);
+                    a32[8 * w + 4] = bit_operand<4>(x);
+                    a32[8 * w + 5] = bit_operand<5>(x);
+                    a32[8 * w + 6] = bit_operand<6>(x);
+                    a32[8 * w + 7] = bit_operand<7>(x);
+                }
+                tmem_st32(abase + P * NCOL, a32);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B(aready));
+        };
+        // tiles in order; the key operands of the next tile go before the
+        // values of this one, so that the next score MMAs overlap the value
+        // expansion and the P V of this tile
+        int k = 0, t = 0, u = 0;
+        while (k < nk && items[k].n_tiles == 0) ++k;
+        if (k < nk) key_operands(0, 0);
+        while (k < nk) {
+            const XpItem it = items[k];
+            int k2 = k, t2 = t + 1;
+            if (t2 == it.n_tiles) {
+                t2 = 0;
+                ++k2;
+                while (k2 < nk && items[k2].n_tiles == 0) ++k2;
+            }
+            if (k2 < nk) key_operands(u + 1, t2);
+            // the token's value row, dequantised, as fp16 high and low parts
+            const int s = u % S;
+            const int np = min(kTilePages, it.n_pages - t * kTilePages);
+            const int pos = it.tok0 + (t * kTilePages + pj) * kBlock + r;
+            const bool valid = pj < np && pos < it.tok1 && ((smask[s] >> pj) & 1);
+            const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
+            if (u >= 1) ws_wait(B(pvdone), (u - 1) & 1, dead, err);  // value operand free
+            xp_value_row<G32, VB>(pg, r, valid, L, vcent, vh, vl, tid);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(B(vready));
+                mbar_arrive(B(&empty[s]));
+            }
+            k = k2;
+            t = t2;
+            ++u;
         }
     } else {
         // ------------------------------------------------------ consumers
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kXpRegsWork));
         const int ctid = tid - 128, cw = warp - 4;
         const int pj = ctid >> 4, r = ctid & 15;
         const uint32_t lane_base = (uint32_t)(32 * cw) << 16;
         const bool qjl = L.k_qjl;
-        uint8_t* ph = smem + sl.phi;
-        uint8_t* pl = smem + sl.plo;
-        float* tmax = red;                          // [2][4][32]
-        float* lsum_s = red + 2 * 4 * kXpHeads;     // [4][32]
-        int tseq = 0, ki = 0;
+        uint8_t* pbuf = smem + sl.phi;              // [P_hi | P_lo]
+        float* tmax = red;                          // [2][32 heads][4 warps]
+        float* lsum_s = red + 2 * 4 * kXpHeads;     // [4 warps][32 heads]
+        int tseq = 0;
         for (int k = 0; k < nk; ++k) {
             const XpItem it = items[k];
             if (it.n_tiles == 0) continue;
@@ -598,30 +623,43 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 ws_wait(B(mdone), tseq & 1, dead, err);
                 tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < kXpHeads / 4; ++q) {
-                    uint32_t kc[16], sg[16];
-                    tmem_ld16(tmem + lane_base + 16 * q, kc);
-                    if (qjl) tmem_ld16(tmem + lane_base + kXpCols + 16 * q, sg);
+                for (int q = 0; q < kXpHeads / 8; ++q) {
+                    // 8 heads (two images): 32 key and 32 sign columns
+                    uint32_t kc[32], sg[32];
+                    tmem_ld32(tmem + lane_base + 32 * q, kc);
+                    if (qjl) tmem_ld32(tmem + lane_base + kXpCols + 32 * q, sg);
                     tc_wait_ld();
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j = 4 * q + h;
+                    for (int h = 0; h < 8; ++h) {
+                        const int j = 8 * q + h;
                         const float4 cst = *reinterpret_cast<const float4*>(icst + 4 * j);
                         float v = n16 * (cst.x + piece_sum(&kc[kPieces * h]) * cst.z);
                         if (qjl) v += rho * (cst.y + piece_sum(&sg[kPieces * h]) * cst.w);
-                        sc[j] = (valid && q < it.n) ? v : -INFINITY;  // head j = 4 q + h of entry q
+                        sc[j] = (valid && (j >> 2) < it.n) ? v : -INFINITY;  // head j of entry j / 4
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B(dfree));
 
-                // ---------------- tile maxima and the CTA-wide lazy reference
+                // ---------------- tile maxima: a transposed butterfly leaves the
+                // warp's maximum of head `lane` in lane `lane`
                 float* tm = tmax + (tseq & 1) * 4 * kXpHeads;
+                {
+                    float v[kXpHeads];
 #pragma unroll
-                for (int j = 0; j < kXpHeads; ++j) {
-                    const float m = warp_max(sc[j]);
-                    if (lane == 0) tm[cw * kXpHeads + j] = m;
+                    for (int j = 0; j < kXpHeads; ++j) v[j] = sc[j];
+#pragma unroll
+                    for (int w = kXpHeads / 2; w >= 1; w >>= 1) {
+                        const bool up = (lane & w) != 0;
+#pragma unroll
+                        for (int j = 0; j < w; ++j) {
+                            const float send = up ? v[j] : v[j + w];
+                            const float keep = up ? v[j + w] : v[j];
+                            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+                        }
+                    }
+                    tm[lane * 4 + cw] = v[0];
                 }
                 named_sync(1, 128);
                 // every consumer thread takes the same decisions (the maxima and
@@ -629,7 +667,8 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 bool any = false;
 #pragma unroll
                 for (int j = 0; j < kXpHeads; ++j) {
-                    const float mt = fmaxf(fmaxf(tm[j], tm[kXpHeads + j]), fmaxf(tm[2 * kXpHeads + j], tm[3 * kXpHeads + j]));
+                    const float4 m4 = *reinterpret_cast<const float4*>(tm + 4 * j);
+                    const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
                     if (t == 0) mref[j] = mt;
                     else any |= mt > mref[j] + kRescaleSlack;
                 }
@@ -638,26 +677,29 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 if (tseq >= 1) ws_wait(B(pvdone), (tseq - 1) & 1, dead, err);
                 if (any) {
                     tc_fence_after();
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + kXpColO, o);
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(tmem + lane_base + kXpColO, o0);
+                    tmem_ld32(tmem + lane_base + kXpColO + kXpHeads, o1);
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < kXpHeads; ++j) {
-                        const float mt =
-                            fmaxf(fmaxf(tm[j], tm[kXpHeads + j]), fmaxf(tm[2 * kXpHeads + j], tm[3 * kXpHeads + j]));
+                        const float4 m4 = *reinterpret_cast<const float4*>(tm + 4 * j);
+                        const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
                         if (mt > mref[j] + kRescaleSlack) {
                             const float alpha = mref[j] == -INFINITY ? 0.f : fast_exp2(mref[j] - mt);
                             mref[j] = mt;
                             lp[j] *= alpha;
-                            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                            o0[j] = __float_as_uint(__uint_as_float(o0[j]) * alpha);
+                            o1[j] = __float_as_uint(__uint_as_float(o1[j]) * alpha);
                         }
                     }
-                    tmem_st32(tmem + lane_base + kXpColO, o);
+                    tmem_st32(tmem + lane_base + kXpColO, o0);
+                    tmem_st32(tmem + lane_base + kXpColO + kXpHeads, o1);
                     tc_wait_st();
                     tc_fence_before();
                 }
 
-                // ---------------- probability operands (fp16 high and low parts)
+                // ---------------- probability operands (fp16 high | low parts)
 #pragma unroll
                 for (int c = 0; c < kXpHeads / 8; ++c) {
                     uint32_t hi[4], lo[4];
@@ -670,8 +712,9 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                         lp[j + 1] += p1;
                         split_f16x2(p0, p1, hi[u], lo[u]);
                     }
-                    *reinterpret_cast<uint4*>(ph + xp_mn_off(ctid, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(pl + xp_mn_off(ctid, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c + kXpHeads / 8)) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
                 fence_async_smem();
                 __syncwarp();
@@ -686,8 +729,9 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
             }
             ws_wait(B(pvdone), (tseq - 1) & 1, dead, err);
             tc_fence_after();
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + kXpColO, o);
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tmem + lane_base + kXpColO, o0);
+            tmem_ld32(tmem + lane_base + kXpColO + kXpHeads, o1);
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -700,7 +744,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 if (e < it.n) {
                     const int64_t row =
                         ((int64_t)(it.t0 + e) * a.q_heads + it.g * a.group + it.hgi * hc + (j & 3)) * S_ + it.c;
-                    a.ws_acc[row * D + i] = __uint_as_float(o[j]);
+                    a.ws_acc[row * D + i] = __uint_as_float(o0[j]) + __uint_as_float(o1[j]);
                 }
             }
             named_sync(1, 128);  // row sums published
@@ -711,7 +755,8 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                     if (lane == j) m = mref[j];
                 const int j = lane, e = j >> 2;
                 if (e < it.n) {
-                    const float l = (lsum_s[j] + lsum_s[kXpHeads + j]) + (lsum_s[2 * kXpHeads + j] + lsum_s[3 * kXpHeads + j]);
+                    const float l =
+                        (lsum_s[j] + lsum_s[kXpHeads + j]) + (lsum_s[2 * kXpHeads + j] + lsum_s[3 * kXpHeads + j]);
                     const int64_t row =
                         ((int64_t)(it.t0 + e) * a.q_heads + it.g * a.group + it.hgi * hc + (j & 3)) * S_ + it.c;
                     a.ws_ml[row * 2] = m;
@@ -719,9 +764,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 }
             }
             named_sync(1, 128);  // icst and the row sums are free for the next item
-            ++ki;
         }
-        (void)ki;
     }
     tc_fence_before();
     __syncthreads();
