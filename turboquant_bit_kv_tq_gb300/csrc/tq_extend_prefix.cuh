@@ -59,18 +59,26 @@ constexpr int kXpVBytes = kXpTileTok * 128 * 2;  // one fp16 piece of the value 
 constexpr int kXpPBytes = kXpTileTok * kXpHeads * 2;  // one fp16 piece of the probability operand
 
 // Byte offset of the 16-byte row (token t, 8-element group c) in the MN-major
-// no-swizzle layout of a [128 tokens x 8c elements] fp16 operand: core
-// matrices of 8 tokens x 8 elements (128 B, tokens 16 B apart), K-adjacent
-// core matrices 128 B apart, element groups 2048 B apart.
-__host__ __device__ constexpr uint32_t xp_mn_off(int t, int c) { return (uint32_t)c * 2048u + (uint32_t)t * 16u; }
+// no-swizzle layout of a [128 tokens x 8 ng elements] fp16 operand: core
+// matrices of 8 tokens x 8 elements (128 B, tokens 16 B apart), the ng
+// element groups of 8 tokens side by side (128 B apart), blocks of 8 tokens
+// ng * 128 B apart.  The tensor cores read a K step's groups as one
+// contiguous run.
+__host__ __device__ constexpr uint32_t xp_mn_off(int t, int c, int ng) {
+    return (uint32_t)(t >> 3) * (uint32_t)(ng * 128) + (uint32_t)c * 128u + (uint32_t)(t & 7) * 16u;
+}
 
 // MN-major shared-memory descriptor of such an operand.  For MN-major
 // operands without swizzling the leading-byte-offset field holds the step
-// between K-adjacent core matrices (128 B here) and the stride-byte-offset
-// field the step between MN-adjacent ones (2048 B), the reverse of their
+// between K-adjacent core matrices (ng * 128 B here) and the stride-byte-offset
+// field the step between MN-adjacent ones (128 B), the reverse of their
 // K-major roles (measured: of the four assignments for A and B only this one
 // reproduces an integer-valued product).
-__device__ __forceinline__ uint64_t xp_mn_desc(uint32_t addr) { return smem_desc(addr, 128, 2048); }
+__device__ __forceinline__ uint64_t xp_mn_desc(uint32_t addr, int ng) {
+    return smem_desc(addr, (uint32_t)(128 * ng), 128);
+}
+constexpr int kXpVGroups = 16;  // value operand: 128 coordinates
+constexpr int kXpPGroups = 8;   // probability operand: 32 heads high | 32 heads low
 
 // kind::f16 instruction descriptor: fp32 accumulation, fp16 A and B, both
 // MN-major, M = 128, N = n
@@ -130,7 +138,7 @@ __host__ __device__ inline XpLayout xp_layout(int page_bytes, int bimg_bytes) {
     l.smask = off;
     off = up(off + (size_t)kXpStages * 4);
     l.bars = off;
-    off = up(off + (size_t)(2 * kXpStages + 9) * 8);
+    off = up(off + (size_t)(2 * kXpStages + 11) * 8);
     l.tslot = off;
     off = up(off + 16);
     l.total = off;
@@ -153,17 +161,28 @@ __host__ __device__ inline int xp_block_tokens(int nhg) { return kXpImgs / nhg; 
 template <int KB, bool KU>
 tq_status dispatch_extend_prefix(const DecodeArgs& a, cudaStream_t s, int grid);
 
+// (x, y) as fp16 high parts (the fp32 values cut to 11 significant bits, a
+// logic operation, then exact in fp16 at normal magnitudes) and fp16
+// roundings of the exact remainders: one conversion per value
+__device__ __forceinline__ void xp_split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const float hx = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    const float hy = __uint_as_float(__float_as_uint(y) & 0xFFFFE000u);
+    hi = pack_f16x2(hx, hy);
+    lo = pack_f16x2(x - hx, y - hy);
+}
+
 // fp16 high and low parts of eight values, as the two 16-byte operand rows
 __device__ __forceinline__ void xp_store8(uint8_t* vh, uint8_t* vl, uint32_t off, const float (&v)[8]) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) split_f16x2(v[2 * u], v[2 * u + 1], h[u], l[u]);
+    for (int u = 0; u < 4; ++u) xp_split2(v[2 * u], v[2 * u + 1], h[u], l[u]);
     *reinterpret_cast<uint4*>(vh + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(vl + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Dequantised value row of page row r (token t of the tile) into the value
-// operand: element group c holds coordinates 8c .. 8c + 7.  Group-32 values:
+// Dequantised value row of page row r (token t of the tile), coordinates
+// 64 ch .. 64 ch + 63, into the value operand: element group c holds
+// coordinates 8c .. 8c + 7.  Group-32 values:
 // v = zero + scale * code in fp32 (the product is exact; one rounding), with
 // the code read as 2^23 + code * 2^(w*n) from the float bits (w-bit field n of
 // a 16-bit window) and the 2^(-w*n) folded into the scale; the field of
@@ -174,9 +193,11 @@ __device__ __forceinline__ void xp_store8(uint8_t* vh, uint8_t* vl, uint32_t off
 // from the bit planes.  A row that is not a valid token gets zeros.
 template <bool G32, int VB>
 __device__ __forceinline__ void xp_value_row(const uint8_t* pg, int r, bool valid, const Layout& L,
-                                             const float* vcent, uint8_t* vh, uint8_t* vl, int t) {
+                                             const float* vcent, uint8_t* vh, uint8_t* vl, int t, int ch) {
     constexpr int D = 128;
     constexpr float kMagic = 8388608.f;  // 2^23
+    // loops over groups are not unrolled: this code shares the instruction
+    // cache with the consumers' and is short that way
     if constexpr (G32) {
         constexpr int NWD = D * VB / 32;  // 32-bit words of the code row
         uint32_t w[NWD];
@@ -189,18 +210,21 @@ __device__ __forceinline__ void xp_value_row(const uint8_t* pg, int r, bool vali
             w[4 * q + 2] = u.z;
             w[4 * q + 3] = u.w;
         }
-        const uint4 mt = *reinterpret_cast<const uint4*>(pg + L.v_meta + r * L.v_meta_row);
-        const uint32_t mw[4] = {mt.x, mt.y, mt.z, mt.w};
-#pragma unroll
-        for (int M = 0; M < 4; ++M) {
-            const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&mw[M]));
+        const uint32_t* meta = reinterpret_cast<const uint32_t*>(pg + L.v_meta + r * L.v_meta_row);
+#pragma unroll 1
+        for (int M = 2 * ch; M < 2 * ch + 2; ++M) {
+            const uint32_t mw = meta[M];
+            const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&mw));
             const float s = valid ? sz.x : 0.f, z = valid ? sz.y : 0.f;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int c = 4 * M + jj;
                 float v[8];
                 if constexpr (VB == 4) {
-                    const uint32_t x = __byte_perm(w[4 * jj + M / 2], w[4 * jj + 2 + M / 2], (M & 1) ? 0x7632 : 0x5410);
+                    const bool odd = (M & 1) != 0, up = M >= 2;
+                    const uint32_t wa = up ? w[4 * jj + 1] : w[4 * jj];
+                    const uint32_t wb = up ? w[4 * jj + 3] : w[4 * jj + 2];
+                    const uint32_t x = __byte_perm(wa, wb, odd ? 0x7632u : 0x5410u);
                     const uint32_t xh = x >> 16;
 #pragma unroll
                     for (int n = 0; n < 4; ++n) {
@@ -219,31 +243,29 @@ __device__ __forceinline__ void xp_value_row(const uint8_t* pg, int r, bool vali
                         v[n] = fmaf(f, sn, z);
                     }
                 }
-                xp_store8(vh, vl, xp_mn_off(t, c), v);
+                xp_store8(vh, vl, xp_mn_off(t, c, kXpVGroups), v);
             }
         }
     } else {
-        uint32_t pw[VB][4];
-#pragma unroll
-        for (int pp = 0; pp < VB; ++pp) {
-            const uint4 u = *reinterpret_cast<const uint4*>(pg + L.v_codes + (pp * kBlock + r) * (D / 8));
-            pw[pp][0] = u.x;
-            pw[pp][1] = u.y;
-            pw[pp][2] = u.z;
-            pw[pp][3] = u.w;
-        }
         const float nv = valid ? __half2float(*reinterpret_cast<const __half*>(pg + L.v_meta + 2 * r)) : 0.f;
+#pragma unroll 1
+        for (int cw4 = 2 * ch; cw4 < 2 * ch + 2; ++cw4) {
+            uint32_t pw[VB];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            float v[8];
+            for (int pp = 0; pp < VB; ++pp)
+                pw[pp] = *reinterpret_cast<const uint32_t*>(pg + L.v_codes + (pp * kBlock + r) * (D / 8) + 4 * cw4);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t code = 0;
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[8];
 #pragma unroll
-                for (int pp = 0; pp < VB; ++pp) code |= ((pw[pp][c >> 2] >> (8 * (c & 3) + q)) & 1u) << pp;
-                v[q] = nv * vcent[code];
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t code = 0;
+#pragma unroll
+                    for (int pp = 0; pp < VB; ++pp) code |= ((pw[pp] >> (8 * cc + q)) & 1u) << pp;
+                    v[q] = nv * vcent[code];
+                }
+                xp_store8(vh, vl, xp_mn_off(t, 4 * cw4 + cc, kXpVGroups), v);
             }
-            xp_store8(vh, vl, xp_mn_off(t, c), v);
         }
     }
 }
@@ -340,10 +362,11 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
     uint64_t* aready = ifull + 2;         // key operands stored (4 score warps)
     uint64_t* mdone = ifull + 3;          // score MMAs done (commit)
     uint64_t* dfree = ifull + 4;          // scores read (4 consumer warps)
-    uint64_t* vready = ifull + 5;         // value operands stored (4 score warps)
-    uint64_t* pready = ifull + 6;         // probability operands stored (4 consumer warps)
-    uint64_t* pvdone = ifull + 7;         // P V MMAs done (commit)
-    uint64_t* oread = ifull + 8;          // output accumulator read (4 consumer warps)
+    // the value operand and its P V go in two token halves (tokens 0-63, 64-127)
+    uint64_t* vready = ifull + 5;         // [half] value operands stored (4 score warps)
+    uint64_t* pready = ifull + 7;         // probability operands stored (4 consumer warps)
+    uint64_t* pvdone = ifull + 8;         // [half] P V MMAs of the half done (commit; half 1: all)
+    uint64_t* oread = ifull + 10;         // output accumulator read (4 consumer warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + sl.tslot);
     XpItem* items = reinterpret_cast<XpItem*>(smem + sl.items);
     uint32_t* smask = reinterpret_cast<uint32_t*>(smem + sl.smask);
@@ -365,9 +388,11 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
         mbar_init(B(aready), 4);
         mbar_init(B(mdone), 1);
         mbar_init(B(dfree), 4);
-        mbar_init(B(vready), 4);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(B(&vready[h]), 4);
+            mbar_init(B(&pvdone[h]), 1);
+        }
         mbar_init(B(pready), 4);
-        mbar_init(B(pvdone), 1);
         mbar_init(B(oread), 4);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -446,17 +471,22 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
             int tseq = 0, ki = 0;
             int pv_t = -1, pv_first = 0, pv_item = 0;  // the tile whose P V is still to issue
             auto issue_pv = [&]() {
-                ws_wait(B(vready), pv_t & 1, dead, err);
                 ws_wait(B(pready), pv_t & 1, dead, err);
                 if (pv_first && pv_item >= 1) ws_wait(B(oread), (pv_item - 1) & 1, dead, err);
-                tc_fence_after();
 #pragma unroll 1
-                for (int kk = 0; kk < kXpTileTok / 16; ++kk) {
-                    const uint64_t bd = xp_mn_desc(pb + 256 * kk);
-                    xp_mma_ss(dO, xp_mn_desc(vhi + 256 * kk), bd, idesc_pv, (pv_first && kk == 0) ? 0u : 1u);
-                    xp_mma_ss(dO, xp_mn_desc(vlo + 256 * kk), bd, idesc_pv, 1u);
+                for (int h = 0; h < 2; ++h) {
+                    ws_wait(B(&vready[h]), pv_t & 1, dead, err);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
+                        // K step kk: tokens 16 kk .. 16 kk + 15, two blocks of 8
+                        const uint64_t bd = xp_mn_desc(pb + 2 * 128 * kXpPGroups * kk, kXpPGroups);
+                        const uint32_t ao = 2 * 128 * kXpVGroups * kk;
+                        xp_mma_ss(dO, xp_mn_desc(vhi + ao, kXpVGroups), bd, idesc_pv, (pv_first && kk == 0) ? 0u : 1u);
+                        xp_mma_ss(dO, xp_mn_desc(vlo + ao, kXpVGroups), bd, idesc_pv, 1u);
+                    }
+                    tc_commit(B(&pvdone[h]));
                 }
-                tc_commit(B(pvdone));
             };
             for (int k = 0; k < nk; ++k) {
                 const XpItem it = items[k];
@@ -514,20 +544,16 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
             if (u >= 1) ws_wait(B(mdone), (u - 1) & 1, dead, err);  // A operand free
             tc_fence_after();
             const uint32_t abase = tmem + lane_base + kXpColA;
-#pragma unroll
-            for (int P = 0; P <= NPK; ++P) {
-                if (P == NPK && !qjl) break;
+#pragma unroll 1
+            for (int P = 0; P < npl; ++P) {
+                // plane P < NPK: XOR of the code bits in subset P; P = NPK: signs
+                const uint32_t sub = P < NPK ? (uint32_t)plane_subset(KB, P) : 0u;
                 uint32_t a32[32];
 #pragma unroll
                 for (int w = 0; w < NW; ++w) {
-                    uint32_t x = 0;
-                    if (P < NPK) {
+                    uint32_t x = P < NPK ? 0u : sw[w];
 #pragma unroll
-                        for (int p = 0; p < KB; ++p)
-                            if ((plane_subset(KB, P) >> p) & 1) x ^= kw[p][w];
-                    } else {
-                        x = sw[w];
-                    }
+                    for (int p = 0; p < KB; ++p) x ^= ((sub >> p) & 1u) ? kw[p][w] : 0u;
                     a32[8 * w + 0] = bit_operand<0>(x);
                     a32[8 * w + 1] = bit_operand<1>(x);
                     a32[8 * w + 2] = bit_operand<2>(x);
@@ -559,20 +585,25 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 while (k2 < nk && items[k2].n_tiles == 0) ++k2;
             }
             if (k2 < nk) key_operands(u + 1, t2);
-            // the token's value row, dequantised, as fp16 high and low parts
+            // the tile's value rows, dequantised, as fp16 high and low parts:
+            // tokens 0-63, then 64-127, two threads per token (coordinate
+            // halves ch), so that the first half's P V overlaps the second's
             const int s = u % S;
             const int np = min(kTilePages, it.n_pages - t * kTilePages);
-            const int pos = it.tok0 + (t * kTilePages + pj) * kBlock + r;
-            const bool valid = pj < np && pos < it.tok1 && ((smask[s] >> pj) & 1);
-            const uint8_t* pg = ring + s * sl.tile + pj * L.page_bytes;
-            if (u >= 1) ws_wait(B(pvdone), (u - 1) & 1, dead, err);  // value operand free
-            xp_value_row<G32, VB>(pg, r, valid, L, vcent, vh, vl, tid);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(B(vready));
-                mbar_arrive(B(&empty[s]));
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int tok = 64 * h + (tid >> 1), ch = tid & 1;
+                const int pj2 = tok >> 4, r2 = tok & 15;
+                const int pos = it.tok0 + (t * kTilePages + pj2) * kBlock + r2;
+                const bool valid = pj2 < np && pos < it.tok1 && ((smask[s] >> pj2) & 1);
+                const uint8_t* pg = ring + s * sl.tile + pj2 * L.page_bytes;
+                if (u >= 1) ws_wait(B(&pvdone[h]), (u - 1) & 1, dead, err);  // this half of the operand free
+                xp_value_row<G32, VB>(pg, r2, valid, L, vcent, vh, vl, tok, ch);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B(&vready[h]));
             }
+            if (lane == 0) mbar_arrive(B(&empty[s]));
             k = k2;
             t = t2;
             ++u;
@@ -674,7 +705,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 }
                 // the previous tile's P V must be done before the output
                 // accumulator is rescaled or the probability operand rewritten
-                if (tseq >= 1) ws_wait(B(pvdone), (tseq - 1) & 1, dead, err);
+                if (tseq >= 1) ws_wait(B(&pvdone[1]), (tseq - 1) & 1, dead, err);
                 if (any) {
                     tc_fence_after();
                     uint32_t o0[32], o1[32];
@@ -710,10 +741,11 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                         const float p1 = sc[j + 1] == -INFINITY ? 0.f : fast_exp2(sc[j + 1] - mref[j + 1]);
                         lp[j] += p0;
                         lp[j + 1] += p1;
-                        split_f16x2(p0, p1, hi[u], lo[u]);
+                        xp_split2(p0, p1, hi[u], lo[u]);
                     }
-                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c + kXpHeads / 8)) =
+                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c, kXpPGroups)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(pbuf + xp_mn_off(ctid, c + kXpHeads / 8, kXpPGroups)) =
                         make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
                 fence_async_smem();
@@ -727,7 +759,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 const float l = warp_sum(lp[j]);
                 if (lane == 0) lsum_s[cw * kXpHeads + j] = l;
             }
-            ws_wait(B(pvdone), (tseq - 1) & 1, dead, err);
+            ws_wait(B(&pvdone[1]), (tseq - 1) & 1, dead, err);
             tc_fence_after();
             uint32_t o0[32], o1[32];
             tmem_ld32(tmem + lane_base + kXpColO, o0);
