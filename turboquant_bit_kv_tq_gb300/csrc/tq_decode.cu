@@ -23,9 +23,10 @@ static DecodeGeom ws_geom(const DecodeGeom& g, const Layout& L, bool k_uniform) 
 
 template <int D>
 static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) {
-    const size_t prep_smem = prep_smem_bytes<D>(a.group);
-    constexpr size_t kPrepMax = prep_smem_bytes<D>(kMaxG);  // the largest head group's need
-    if (prep_smem > kPrepMax) return TQ_ERR_UNSUPPORTED;
+    if (a.group > kMaxG) return TQ_ERR_UNSUPPORTED;
+    // the most virtual heads a prep CTA takes (S^T of d = 256 leaves room for 16)
+    constexpr int kPrepV = D == 128 ? kPrepMaxV : kMaxG;
+    constexpr size_t kPrepMax = prep_smem_bytes<D>(kPrepV);
     // per-device set-up (the first call on a device does it; before any capture)
     int sms = 0;
     {
@@ -42,6 +43,8 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
                     xp_layout(a.lay.page_bytes, gw.bimg_bytes).total <= 227 * 1024;
     if (xp) {
         a.gm = gw;
+        // the query prep takes a query block's entries per CTA (S^T staged once)
+        a.prep_entries = xp_block_tokens(gw.nhg);
     } else if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel
@@ -84,7 +87,10 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         // in stream order (overlapping it with a preceding store measured
         // slower)
         a.pdl = ev0 == nullptr && ev1 == nullptr;
-        const cudaError_t e = launch_pdl(false, prep_kernel<D>, dim3(a.heads, a.batch), dim3(kPrepThreads), prep_smem, s, a);
+        if (a.prep_entries < 1 || a.prep_entries * a.group > kPrepV) a.prep_entries = 1;
+        const size_t prep_smem = prep_smem_bytes<D>(a.prep_entries * a.group);
+        const dim3 pgrid(a.heads, (a.batch + a.prep_entries - 1) / a.prep_entries);
+        const cudaError_t e = launch_pdl(false, prep_kernel<D>, pgrid, dim3(kPrepThreads), prep_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {

@@ -74,6 +74,7 @@ struct DecodeArgs {
     const int4* xblocks = nullptr;
     const int32_t* xcounts = nullptr;
     int xblocks_max = 0;  // the plan's capacity (an upper bound of the block count)
+    int prep_entries = 1;  // batch entries per query-prep CTA
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -185,27 +186,40 @@ __device__ __forceinline__ void mma_fp8_ts(uint32_t d, uint32_t a, uint64_t bdes
 //   2 * (S q)_c * bit_weight(c%8) * 2^sigmaQ        (sign plane P = npk)
 // for coordinate c = 32*(col/8) + 8*e + col%8: the coordinate that byte e of
 // tensor-memory column col of plane P holds in the split kernel.
+// One CTA serves prep_entries consecutive batch entries of one KV head (1 for
+// decode; a block of extend's new tokens): their E x G query heads are handled
+// as "virtual heads" v = e G + h, with S^T staged once.  Every head's
+// arithmetic is the same for any entry count.
+constexpr int kPrepMaxV = 32;  // virtual heads per CTA at most
 template <int D>
-__host__ __device__ constexpr size_t prep_smem_bytes(int G) {
-    return (size_t)D * D * 2 + (size_t)3 * G * D * 4 + 2 * kMaxG * 4 + 16;
+__host__ __device__ constexpr size_t prep_smem_bytes(int GV) {
+    return (size_t)D * D * 2 + (size_t)3 * GV * D * 4 + 2 * kPrepMaxV * 4 + 16;
 }
 
-constexpr int kPrepThreads = 512;  // one CTA per (sequence, KV head): its phases are short serial chains
+constexpr int kPrepThreads = 512;  // its phases are short serial chains
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     pdl_launch_dependents();  // the split kernel's prologue may start
-    const int g = blockIdx.x, b = blockIdx.y;
-    if (b >= a.batch) return;
+    const int g = blockIdx.x, E = a.prep_entries, b0 = blockIdx.y * E;
+    const int ne = min(E, a.batch - b0);
+    if (ne <= 0) return;
     // an extend entry with no compressed prefix uses none of this (its exact
     // part reads the raw queries)
-    if (a.chunk_attn && a.seq_lens[b] <= 0) return;
-    const int G = a.group, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    if (a.chunk_attn) {
+        bool any = false;
+        for (int e = 0; e < ne; ++e) any |= a.seq_lens[b0 + e] > 0;
+        if (!any) return;
+    }
+    const int G = a.group, GV = ne * G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5,
+              nwarps = blockDim.x >> 5;
+    // global query-head row of virtual head v
+    auto hrow = [&](int v) { return (int64_t)(b0 + v / G) * a.q_heads + (int64_t)g * G + v % G; };
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t* st = reinterpret_cast<uint16_t*>(smem);           // S^T bf16 [D][D]
-    float* qv = reinterpret_cast<float*>(smem + (size_t)D * D * 2);  // [G][D]
-    float* rq = qv + G * D;                                     // [G][D]
-    float* sq = rq + G * D;                                     // [G][D]
-    float* sig = sq + G * D;                                    // [kMaxG][2] = 2^sigmaK, 2^sigmaQ
+    float* qv = reinterpret_cast<float*>(smem + (size_t)D * D * 2);  // [GV][D]
+    float* rq = qv + GV * D;                                    // [GV][D]
+    float* sq = rq + GV * D;                                    // [GV][D]
+    float* sig = sq + GV * D;                                   // [kPrepMaxV][2] = 2^sigmaK, 2^sigmaQ
     uint64_t* bar = reinterpret_cast<uint64_t*>(sig + 2 * kMaxG);
     if (tid == 0) {
         mbar_init(smem_u32(bar), 1);
@@ -213,13 +227,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
         mbar_expect_tx(smem_u32(bar), D * D * 2);
         bulk_copy(smem_u32(st), a.dp.st_bf16, D * D * 2, smem_u32(bar));
     }
-    const int64_t hbase = (int64_t)b * a.q_heads + (int64_t)g * G;
     // the queries, the rotation signs and the key codebook's Walsh terms load
     // together (one memory latency), the S^T copy meanwhile
     __shared__ float s_signs[D], s_kw[9];
-    for (int e = tid; e < G * D; e += blockDim.x)
-        qv[e] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[hbase * D + e]
-                                          : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[hbase * D + e]);
+    for (int e = tid; e < GV * D; e += blockDim.x) {
+        const int64_t src = hrow(e / D) * D + e % D;
+        qv[e] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[src]
+                                          : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[src]);
+    }
     for (int e = tid; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
     __syncthreads();
@@ -228,9 +243,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // are made: [head][0..2] sum, sum over i % 8 = 7, max of |v| bit_weight(i % 8)
     // of R q (one entry per head) and of S q (one entry per warp of the head)
     constexpr int kSqWarps = D / 64;  // warps per head in the S q phase
-    __shared__ float red_r[kMaxG][3], red_s[kMaxG][kSqWarps][3];
+    __shared__ float red_r[kPrepMaxV][3], red_s[kPrepMaxV][kSqWarps][3];
     // R q by an in-warp Hadamard transform (one warp per head)
-    for (int h = warp; h < G; h += nwarps) {
+    for (int h = warp; h < GV; h += nwarps) {
         float x[D / 32];
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) x[k] = qv[h * D + lane + 32 * k] * s_signs[lane + 32 * k];
@@ -261,7 +276,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
         constexpr int NP = D / 2;            // column pairs
         constexpr int HS = kPrepThreads / NP;  // heads covered per pass (8 at d=128, 4 at d=256)
         const int jp = tid % NP, h0 = tid / NP;
-        for (int h = h0; h < G; h += HS) {
+        for (int h = h0; h < GV; h += HS) {
             float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};  // two partial sums per column
             if (s_ok) {
                 const float4* q4 = reinterpret_cast<const float4*>(qv + h * D);
@@ -296,12 +311,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
-    float* dst = a.ws_q + hbase * 3 * D;
-    for (int e = tid; e < G * D; e += blockDim.x) {
+    for (int e = tid; e < GV * D; e += blockDim.x) {
         const int h = e / D, i = e % D;
-        dst[h * 3 * D + i] = rq[e];
-        dst[h * 3 * D + D + i] = sq[e];
-        dst[h * 3 * D + 2 * D + i] = qv[e] * f;
+        float* dst = a.ws_q + hrow(h) * 3 * D;
+        dst[i] = rq[e];
+        dst[D + i] = sq[e];
+        dst[2 * D + i] = qv[e] * f;
     }
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
         bmax = fmaxf(bmax, fabsf(kw[1 + p]));
         bsum += kw[1 + p];
     }
-    for (int h = tid; h < G; h += blockDim.x) {
+    for (int h = tid; h < GV; h += blockDim.x) {
         const float s_rq = red_r[h][0], s_rq7 = red_r[h][1], m_rq = red_r[h][2] * bmax;
         float s_sq = 0.f, s_sq7 = 0.f, m_sq = 0.f;
 #pragma unroll
@@ -329,7 +344,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
             };
             auto pow2 = [](int e) { return __uint_as_float((uint32_t)(127 + e) << 23); };
             const int ek = max(-120, min(120, scale_exp(m_rq))), eq = max(-120, min(120, scale_exp(m_sq)));
-            float* c = a.ws_cst + (hbase + h) * 4;
+            float* c = a.ws_cst + hrow(h) * 4;
             c[0] = kw[0] * s_rq + 0.5f * bsum * s_rq7;
             c[1] = -s_sq + s_sq7;
             c[2] = pow2(-ek);
@@ -345,45 +360,54 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     const int kt = gm.npl * D;           // K extent (bytes per row)
     const uint32_t sbo = 8u * kt;        // byte step between 8-row groups
     const int hrows = (gm.n_cols + kPieces - 1) / kPieces;  // head row blocks (incl. padding)
-    const int units = gm.nhg * hrows * gm.npl * (D / 4);
-    uint8_t* img0 = a.ws_bimg + ((int64_t)b * a.heads + g) * gm.nhg * gm.bimg_bytes;
+    // a work unit is (entry, head group, 16-byte K chunk j, head row block hl,
+    // fastest): the kPieces rows of head hl over K bytes 16j .. 16j + 15 are
+    // 64 contiguous bytes of the image, and consecutive units fill whole lines
+    const int nchunk = kt / 16;
+    const int units = ne * gm.nhg * nchunk * hrows;
     for (int u = tid; u < units; u += blockDim.x) {
         int x = u;
-        const int col = x % (D / 4);
-        x /= D / 4;
-        const int P = x % gm.npl;
-        x /= gm.npl;
-        const int hl = x % hrows, hgi = x / hrows;
-        uint32_t word[kPieces];
+        const int hl = x % hrows;
+        x /= hrows;
+        const int j = x % nchunk;
+        x /= nchunk;
+        const int hgi = x % gm.nhg, ent = x / gm.nhg;
+        const int P = (16 * j) / D, col0 = ((16 * j) % D) / 4;
+        uint32_t word[kPieces][4];
 #pragma unroll
-        for (int k = 0; k < kPieces; ++k) word[k] = 0;
+        for (int k = 0; k < kPieces; ++k)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) word[k][cc] = 0;
         if (hl < gm.hc) {
-            const int h = hgi * gm.hc + hl;
+            const int h = ent * G + hgi * gm.hc + hl;  // virtual head
             const bool sign_plane = P == gm.npk;
             const float beta = sign_plane ? 2.f : kw[1 + P];
             const float* src = sign_plane ? sq + h * D : rq + h * D;
             const float sc = sig[2 * h + (sign_plane ? 1 : 0)];
-            const float bw = bit_weight(col & 7);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = 32 * (col >> 3) + 8 * e + (col & 7);
-                float y = beta * src[c] * bw * sc;
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = col0 + cc;
+                const float bw = bit_weight(col & 7);
 #pragma unroll
-                for (int k = 0; k < kPieces; ++k) {
-                    const uint8_t pk = float_to_e4m3(y);
-                    word[k] |= (uint32_t)pk << (8 * e);
-                    y = (y - e4m3_to_float(pk)) * 16.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 32 * (col >> 3) + 8 * e + (col & 7);
+                    float y = beta * src[c] * bw * sc;
+#pragma unroll
+                    for (int k = 0; k < kPieces; ++k) {
+                        const uint8_t pk = float_to_e4m3(y);
+                        word[k][cc] |= (uint32_t)pk << (8 * e);
+                        y = (y - e4m3_to_float(pk)) * 16.f;
+                    }
                 }
             }
         }
-        const int kk0 = P * D + 4 * col;
-        uint8_t* img = img0 + (size_t)hgi * gm.bimg_bytes;
+        uint8_t* img = a.ws_bimg + (((int64_t)(b0 + ent) * a.heads + g) * gm.nhg + hgi) * gm.bimg_bytes;
 #pragma unroll
         for (int k = 0; k < kPieces; ++k) {
             const int n = kPieces * hl + k;
             if (n < gm.n_cols)
-                *reinterpret_cast<uint32_t*>(img + (n & 7) * 16 + (n >> 3) * sbo + (kk0 >> 4) * 128 + (kk0 & 15)) =
-                    word[k];
+                *reinterpret_cast<uint4*>(img + (n & 7) * 16 + (n >> 3) * sbo + j * 128) =
+                    make_uint4(word[k][0], word[k][1], word[k][2], word[k][3]);
         }
     }
 }
