@@ -93,6 +93,11 @@ CASES = [
     ("k4_lloyd_fallback_kernel", "llama8b_gqa4_b16_8k", dict(k_bits=4), [100, 7], [9, 4], 4),
     ("mse_values_chunk", "llama8b_gqa4_b16_8k", dict(v_mode="mse", v_bits=3), [64, 0], [20, 11], 4),
     ("empty_chunk_first", "llama8b_gqa4_b16_8k", {}, [50, 30, 9], [0, 5, 2], 4),
+    # the prefix kernel's other instances: 2-bit keys with 2-bit group-32
+    # values, 3-bit uniform keys with 4-bit MSE values, keys without QJL
+    ("k2_g32v2", "llama8b_gqa4_b16_8k", dict(k_bits=2, v_bits=2), [200, 64], [11, 6], 4),
+    ("uniform_k3_mse_v4", "llama8b_gqa4_b16_8k", dict(k_codebook="uniform", v_mode="mse", v_bits=4), [150], [13], 4),
+    ("no_qjl_keys", "llama8b_gqa4_b16_8k", dict(k_qjl=False), [90, 33], [9, 17], 2),
 ]
 
 
@@ -107,6 +112,26 @@ def test_extend_parity(case):
     _assert_close(got, ref)
     assert c.device_error() == 0
     assert np.abs(ref).max() > 0.1
+
+
+def test_extend_invalid_prefix_block_is_flagged():
+    # a block-table entry of sequence 1's prefix out of range: flagged, its
+    # page skipped; sequence 0 (and its new tokens) are unaffected
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [70, 70], [5, 4])
+    c = e.make_cache(2)
+    bad = e.table.copy()
+    bad[1, 1] = e.num_blocks + 3
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q = torch.from_numpy(np.ascontiguousarray(e.Q)).to("cuda", dt)
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda", torch.bfloat16)  # noqa: E731
+    out = c.extend(q, torch.from_numpy(bad).cuda(), torch.tensor(e.prefix, dtype=torch.int32, device="cuda"),
+                   torch.from_numpy(e.cu).cuda(), bf(e.ck), bf(e.cv), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert c.device_error() & tq.TQ_DEVERR_BLOCK
+    got = out.cpu().numpy()
+    _assert_close(got[:5], e.oracle()[:5])
+    assert np.isfinite(got).all()
 
 
 def test_extend_rows_outside_every_chunk_are_zero_and_flagged():
