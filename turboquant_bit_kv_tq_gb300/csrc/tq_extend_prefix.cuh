@@ -15,9 +15,9 @@
 //            head for the whole CTA (a tile maximum across the 4 consumer
 //            warps); rescaling the output accumulator in tensor memory is rare
 //   P V      a second tcgen05 contraction, D[128 coordinates x 64] in
-//            tensor memory: A = the tile's dequantised values (fp16 high and
+//            tensor memory: A = the tile's dequantised values (bf16 high and
 //            low parts, MN-major: token-major rows as the thread that owns a
-//            token writes them), B = [P_hi | P_lo], the probabilities' fp16
+//            token writes them), B = [P_hi | P_lo], the probabilities' bf16
 //            high and low parts side by side (MN-major, N = 64); the two
 //            column halves add up at the end; fp32 accumulation
 // Every (new token, query head) of the item gets the split's partial
@@ -55,11 +55,11 @@ constexpr int kXpTmemCols = 512;
 constexpr int kXpColA = 2 * kXpCols;       // A operand: npl planes x 32 columns
 constexpr int kXpColO = 448;               // P V accumulator: 64 columns (probability high | low part)
 constexpr int kXpTileTok = kTilePages * kBlock;  // 128 prefix tokens per tile
-constexpr int kXpVBytes = kXpTileTok * 128 * 2;  // one fp16 piece of the value operand
-constexpr int kXpPBytes = kXpTileTok * kXpHeads * 2;  // one fp16 piece of the probability operand
+constexpr int kXpVBytes = kXpTileTok * 128 * 2;  // one bf16 piece of the value operand
+constexpr int kXpPBytes = kXpTileTok * kXpHeads * 2;  // one bf16 piece of the probability operand
 
 // Byte offset of the 16-byte row (token t, 8-element group c) in the MN-major
-// no-swizzle layout of a [128 tokens x 8 ng elements] fp16 operand: core
+// no-swizzle layout of a [128 tokens x 8 ng elements] 16-bit operand: core
 // matrices of 8 tokens x 8 elements (128 B, tokens 16 B apart), the ng
 // element groups of 8 tokens side by side (128 B apart), blocks of 8 tokens
 // ng * 128 B apart.  The tensor cores read a K step's groups as one
@@ -80,10 +80,11 @@ __device__ __forceinline__ uint64_t xp_mn_desc(uint32_t addr, int ng) {
 constexpr int kXpVGroups = 16;  // value operand: 128 coordinates
 constexpr int kXpPGroups = 8;   // probability operand: 32 heads high | 32 heads low
 
-// kind::f16 instruction descriptor: fp32 accumulation, fp16 A and B, both
+// kind::f16 instruction descriptor: fp32 accumulation, bf16 A and B, both
 // MN-major, M = 128, N = n
 __host__ __device__ constexpr uint32_t xp_pv_idesc(int n) {
-    return (1u << 4) | (1u << 15) | (1u << 16) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((128u >> 4) << 24);
 }
 
 // D[128 x N] (+)= A[128 x 16] B[16 x N], both operands in shared memory
@@ -161,17 +162,18 @@ __host__ __device__ inline int xp_block_tokens(int nhg) { return kXpImgs / nhg; 
 template <int KB, bool KU>
 tq_status dispatch_extend_prefix(const DecodeArgs& a, cudaStream_t s, int grid);
 
-// (x, y) as fp16 high parts (the fp32 values cut to 11 significant bits, a
-// logic operation, then exact in fp16 at normal magnitudes) and fp16
-// roundings of the exact remainders: one conversion per value
+// (x, y) as bf16 high parts (the top 16 bits of each fp32 value) and bf16
+// low parts (the top 16 bits of the exact remainders): ~16 significant bits
+// together, from logic operations and byte permutes (no conversions)
 __device__ __forceinline__ void xp_split2(float x, float y, uint32_t& hi, uint32_t& lo) {
-    const float hx = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    const float hy = __uint_as_float(__float_as_uint(y) & 0xFFFFE000u);
-    hi = pack_f16x2(hx, hy);
-    lo = pack_f16x2(x - hx, y - hy);
+    const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
+    hi = __byte_perm(xb, yb, 0x7632u);
+    const float lx = x - __uint_as_float(xb & 0xFFFF0000u);
+    const float ly = y - __uint_as_float(yb & 0xFFFF0000u);
+    lo = __byte_perm(__float_as_uint(lx), __float_as_uint(ly), 0x7632u);
 }
 
-// fp16 high and low parts of eight values, as the two 16-byte operand rows
+// bf16 high and low parts of eight values, as the two 16-byte operand rows
 __device__ __forceinline__ void xp_store8(uint8_t* vh, uint8_t* vl, uint32_t off, const float (&v)[8]) {
     uint32_t h[4], l[4];
 #pragma unroll
@@ -585,7 +587,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                 while (k2 < nk && items[k2].n_tiles == 0) ++k2;
             }
             if (k2 < nk) key_operands(u + 1, t2);
-            // the tile's value rows, dequantised, as fp16 high and low parts:
+            // the tile's value rows, dequantised, as bf16 high and low parts:
             // tokens 0-63, then 64-127, two threads per token (coordinate
             // halves ch), so that the first half's P V overlaps the second's
             const int s = u % S;
@@ -730,7 +732,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) extend_prefix_kernel(DecodeArgs
                     tc_fence_before();
                 }
 
-                // ---------------- probability operands (fp16 high | low parts)
+                // ---------------- probability operands (bf16 high | low parts)
 #pragma unroll
                 for (int c = 0; c < kXpHeads / 8; ++c) {
                     uint32_t hi[4], lo[4];
