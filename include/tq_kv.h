@@ -285,13 +285,22 @@ tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype,
  *   cu_q         device int32 [batch+1], non-decreasing, cu_q[0] = 0,
  *                cu_q[batch] = n_tokens.  A row of q that no chunk holds gets
  *                out = 0 and sets TQ_DEVERR_CHUNK; every row a chunk names
- *                lies in [0, n_tokens).
+ *                lies in [0, n_tokens).  A cu_q that decreases or leaves
+ *                [0, n_tokens] also sets TQ_DEVERR_CHUNK; the rows it names
+ *                are clamped into [0, n_tokens) and their outputs are then
+ *                unspecified.
  *   new_k/new_v  device bf16 [n_tokens][H_kv][d], 16-byte aligned
  *   scale, out_dtype as for tq_decode_attention; out device [n_tokens][H_q][d]
- * Each token is one entry of the decode grid: n_tokens <= max_batch, and a
- * chunk may hold at most tail_cap tokens (tail_cap >= 1; a longer chunk is
- * clamped and sets TQ_DEVERR_TAIL).  Uses the cache's workspace, like
- * tq_decode_attention.  n_tokens == 0 is a no-op.
+ * Each token is one entry of the workspace (its split partials, as in the
+ * decode): n_tokens <= max_batch, and a chunk may hold at most tail_cap
+ * tokens (tail_cap >= 1; a longer chunk is clamped and sets TQ_DEVERR_TAIL).
+ * At d = 128 with head groups of four query heads and at most six score
+ * planes, blocks of a chunk's new tokens (8 at 4 query heads per KV head, 4 at
+ * 8) share one tensor-core pass over every prefix tile; other configurations
+ * run the decode kernels over one entry per new token.  The results agree to
+ * the decode's error bar either way.  A prefix block id outside
+ * [0, num_blocks) is skipped and sets TQ_DEVERR_BLOCK.  Uses the cache's
+ * workspace, like tq_decode_attention.  n_tokens == 0 is a no-op.
  */
 tq_status tq_extend_attention(const tq_cache* cache, const void* q, int q_dtype, const void* cache_buf,
                               const int32_t* block_table, const int32_t* prefix_lens, const int32_t* cu_q,
