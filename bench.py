@@ -87,11 +87,18 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# the sources the decode split kernels are compiled from and launched by: a
+# change to any of them makes a traffic record stale (other kernels' files,
+# e.g. the store's or extend's prefix kernel, do not)
+_SPLIT_SOURCES = ("tq_decode_ws.cuh", "tq_decode_kernels.cuh", "tq_device.cuh", "tq_internal.h", "tq_decode.cu",
+                  "tq_host.cpp")
+
+
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "turboquant_bit_kv_tq_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+        if name in _SPLIT_SOURCES or name.startswith("tq_decode_split_"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
