@@ -39,6 +39,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "tq_device.cuh"
 
@@ -268,46 +269,68 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
             red_r[h][2] = m0;
         }
     }
-    // S q from the shared copy of S^T: thread (column pair j, j + 1; head h),
-    // 32-bit loads of S^T pairs and 128-bit loads of four query elements
+    // S q from the shared copy of S^T: thread (column pair j, j + 1; a block
+    // of HPT heads), 32-bit loads of S^T pairs (each serving the block's
+    // heads) and 128-bit loads of four query elements.  HPT = 4 when one pass
+    // of single heads would not cover the CTA's heads (a query block of
+    // extend), 1 otherwise; every head's sums run in the same order either way.
     bool s_ok = mbar_wait(smem_u32(bar), 0, a.dp.err);
     const float kq = f * sqrtf(1.5707963267948966f) / (float)D;
-    {
-        constexpr int NP = D / 2;            // column pairs
-        constexpr int HS = kPrepThreads / NP;  // heads covered per pass (8 at d=128, 4 at d=256)
-        const int jp = tid % NP, h0 = tid / NP;
-        for (int h = h0; h < GV; h += HS) {
-            float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};  // two partial sums per column
-            if (s_ok) {
-                const float4* q4 = reinterpret_cast<const float4*>(qv + h * D);
-#pragma unroll 4
-                for (int i4 = 0; i4 < D / 4; ++i4) {
-                    const float4 qq = q4[i4];
-                    const float qa[4] = {qq.x, qq.y, qq.z, qq.w};
+    auto sq_pass = [&](auto hpt_c) {
+        constexpr int HPT = decltype(hpt_c)::value;
+        constexpr int NP = D / 2;                 // column pairs
+        constexpr int HS = kPrepThreads / NP;     // head blocks covered per pass
+        const int jp = tid % NP, b0h = tid / NP;  // (warp-uniform b0h)
+        for (int hb = b0h; hb * HPT < GV; hb += HS) {
+            float s0[HPT][2], s1[HPT][2];  // two partial sums per column and head
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t pr = *reinterpret_cast<const uint32_t*>(st + (4 * i4 + u) * D + 2 * jp);
-                        s0[u & 1] = fmaf(__uint_as_float(pr << 16), qa[u], s0[u & 1]);
-                        s1[u & 1] = fmaf(__uint_as_float(pr & 0xFFFF0000u), qa[u], s1[u & 1]);
+            for (int hh = 0; hh < HPT; ++hh) s0[hh][0] = s0[hh][1] = s1[hh][0] = s1[hh][1] = 0.f;
+            if (s_ok) {
+#pragma unroll 2
+                for (int i4 = 0; i4 < D / 4; ++i4) {
+                    uint32_t pr[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) pr[u] = *reinterpret_cast<const uint32_t*>(st + (4 * i4 + u) * D + 2 * jp);
+#pragma unroll
+                    for (int hh = 0; hh < HPT; ++hh) {
+                        const int h = hb * HPT + hh;
+                        if (h < GV) {
+                            const float4 qq = reinterpret_cast<const float4*>(qv + h * D)[i4];
+                            const float qa[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                s0[hh][u & 1] = fmaf(__uint_as_float(pr[u] << 16), qa[u], s0[hh][u & 1]);
+                                s1[hh][u & 1] = fmaf(__uint_as_float(pr[u] & 0xFFFF0000u), qa[u], s1[hh][u & 1]);
+                            }
+                        }
                     }
                 }
             }
-            const float v0 = (s0[0] + s0[1]) * kq, v1 = (s1[0] + s1[1]) * kq;
-            sq[h * D + 2 * jp] = v0;
-            sq[h * D + 2 * jp + 1] = v1;
-            // columns 2jp (i % 8 even) and 2jp + 1 (i % 8 = 7 when jp % 4 = 3)
-            float sum = warp_sum(v0 + v1);
-            float s7 = warp_sum((jp & 3) == 3 ? v1 : 0.f);
-            float mx = warp_max(fmaxf(fabsf(v0) * fabsf(bit_weight((2 * jp) & 7)),
-                                      fabsf(v1) * fabsf(bit_weight((2 * jp + 1) & 7))));
-            if (lane == 0) {
-                const int wh = (jp >> 5);  // this warp's place among the head's warps
-                red_s[h][wh][0] = sum;
-                red_s[h][wh][1] = s7;
-                red_s[h][wh][2] = mx;
+#pragma unroll
+            for (int hh = 0; hh < HPT; ++hh) {
+                const int h = hb * HPT + hh;
+                if (h >= GV) break;
+                const float v0 = (s0[hh][0] + s0[hh][1]) * kq, v1 = (s1[hh][0] + s1[hh][1]) * kq;
+                sq[h * D + 2 * jp] = v0;
+                sq[h * D + 2 * jp + 1] = v1;
+                // columns 2jp (i % 8 even) and 2jp + 1 (i % 8 = 7 when jp % 4 = 3)
+                float sum = warp_sum(v0 + v1);
+                float s7 = warp_sum((jp & 3) == 3 ? v1 : 0.f);
+                float mx = warp_max(fmaxf(fabsf(v0) * fabsf(bit_weight((2 * jp) & 7)),
+                                          fabsf(v1) * fabsf(bit_weight((2 * jp + 1) & 7))));
+                if (lane == 0) {
+                    const int wh = (jp >> 5);  // this warp's place among the head's warps
+                    red_s[h][wh][0] = sum;
+                    red_s[h][wh][1] = s7;
+                    red_s[h][wh][2] = mx;
+                }
             }
         }
-    }
+    };
+    if (GV > kPrepThreads / (D / 2))
+        sq_pass(std::integral_constant<int, 4>{});
+    else
+        sq_pass(std::integral_constant<int, 1>{});
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
@@ -388,16 +411,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
             for (int cc = 0; cc < 4; ++cc) {
                 const int col = col0 + cc;
                 const float bw = bit_weight(col & 7);
+                float y[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 32 * (col >> 3) + 8 * e + (col & 7);
-                    float y = beta * src[c] * bw * sc;
+                for (int e = 0; e < 4; ++e) y[e] = beta * src[32 * (col >> 3) + 8 * e + (col & 7)] * bw * sc;
+                // the pieces of bytes (0, 1) and (2, 3) in packed conversions:
+                // the same roundings as one value at a time
 #pragma unroll
-                    for (int k = 0; k < kPieces; ++k) {
-                        const uint8_t pk = float_to_e4m3(y);
-                        word[k][cc] |= (uint32_t)pk << (8 * e);
-                        y = (y - e4m3_to_float(pk)) * 16.f;
+                for (int k = 0; k < kPieces; ++k) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const __nv_fp8x2_storage_t pk =
+                            __nv_cvt_float2_to_fp8x2(make_float2(y[e], y[e + 1]), __NV_SATFINITE, __NV_E4M3);
+                        w |= (uint32_t)pk << (8 * e);
+                        const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pk, __NV_E4M3)));
+                        y[e] = (y[e] - back.x) * 16.f;
+                        y[e + 1] = (y[e + 1] - back.y) * 16.f;
                     }
+                    word[k][cc] = w;
                 }
             }
         }
