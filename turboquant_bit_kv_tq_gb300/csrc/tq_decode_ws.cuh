@@ -236,7 +236,7 @@ struct WsIssuer {
         while (c_k < nk && items[c_k].n_tiles == 0) ++c_k;
     }
 
-    // warp-uniform wait: lane 0 waits (bounded), the others take its verdict
+    // warp-uniform wait: lane 0 waits (bounded), the others take its outcome
     __device__ bool wait_uniform(uint64_t* bar, uint32_t par, bool block, int lane) {
         int ok = 1;
         if (lane == 0) {
