@@ -295,8 +295,8 @@ tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype,
  * decode): n_tokens <= max_batch, and a chunk may hold at most tail_cap
  * tokens (tail_cap >= 1; a longer chunk is clamped and sets TQ_DEVERR_TAIL).
  * At d = 128 with head groups of four query heads and at most six score
- * planes, blocks of a chunk's new tokens (8 at 4 query heads per KV head, 4 at
- * 8) share one tensor-core pass over every prefix tile; other configurations
+ * planes, blocks of 8 new tokens of a chunk (and one head group of four query
+ * heads) share one tensor-core pass over every prefix tile; other configurations
  * run the decode kernels over one entry per new token.  The results agree to
  * the decode's error bar either way.  A prefix block id outside
  * [0, num_blocks) is skipped and sets TQ_DEVERR_BLOCK.  Uses the cache's

@@ -43,8 +43,9 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
                     xp_layout(a.lay.page_bytes, gw.bimg_bytes).total <= 227 * 1024;
     if (xp) {
         a.gm = gw;
-        // the query prep takes a query block's entries per CTA (S^T staged once)
-        a.prep_entries = xp_block_tokens(gw.nhg);
+        // the query prep takes as many entries per CTA as its virtual-head
+        // limit allows (S^T staged once for them)
+        a.prep_entries = std::max(1, std::min(xp_block_tokens(), kPrepMaxV / a.group));
     } else if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel
@@ -395,7 +396,7 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
     // kernel (launch_decode runs it when the score planes fit)
     const DecodeGeom gw = ws_geom(a.gm, a.lay, a.k_uniform);
     if (xp_supported(gw, d)) {
-        const int tpb = xp_block_tokens(gw.nhg);
+        const int tpb = xp_block_tokens();
         a.xcounts = tail_base + B;
         a.xblocks = reinterpret_cast<const int4*>(tail_base + B + 4);
         a.xblocks_max = std::min(n_tokens, (n_tokens + tpb - 1) / tpb + batch);

@@ -4,8 +4,8 @@
 // [Roadmap] §4.1: in an extend (prefill) call every new token attends to its
 // sequence's whole compressed prefix, so the new tokens of a chunk share every
 // prefix tile.  A work item is one query block (up to 8 consecutive new tokens
-// of one sequence at G = 4, 4 at G = 8: 32 query heads of one KV head), one KV
-// head and one prefix split.  The CTA streams the split as 128-token tiles
+// of one sequence, one head group of four query heads: 32 query heads), one
+// KV head and one prefix split.  The CTA streams the split as 128-token tiles
 // and contracts each tile against all 32 query heads at once:
 //   scores   the decode's fp8 bit-plane contraction (key code planes and the
 //            QJL sign plane as exact e4m3 A operands in tensor memory), with
@@ -153,8 +153,10 @@ inline bool xp_supported(const DecodeGeom& gm, int d) {
     return d == 128 && gm.hc == 4 && gm.nth == 1 && gm.n_cols == 16 && gm.npl * (d / 4) <= kXpColO - kXpColA;
 }
 
-// new tokens per query block
-__host__ __device__ inline int xp_block_tokens(int nhg) { return kXpImgs / nhg; }
+// new tokens per query block: one query image per token and head group, and
+// an item takes one head group, so a block of kXpImgs tokens fills the
+// item's kXpImgs images whatever the group size
+__host__ __device__ inline int xp_block_tokens() { return kXpImgs; }
 
 // the prefix kernels of one key configuration (all value modes), compiled in
 // their own translation units: KB-bit keys, KU = uniform codebook with its KB
