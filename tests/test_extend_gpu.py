@@ -114,6 +114,24 @@ def test_extend_parity(case):
     assert np.abs(ref).max() > 0.1
 
 
+def test_extend_many_sequences():
+    # 70 sequences (the query-block plan's scan spans three warps), chunks of
+    # 0..11 tokens and prefixes of 0..90 tokens (some empty), 2-block splits:
+    # many blocks and items per CTA
+    w = wl.config("llama8b_gqa4_b16_8k")
+    rng = np.random.default_rng(21)
+    B = 70
+    prefix = [int(x) for x in rng.integers(0, 91, B)]
+    chunk = [int(x) for x in rng.integers(0, 12, B)]
+    for b in rng.choice(B, 6, replace=False):
+        prefix[b] = 0
+    e = Extend(w, prefix, chunk)
+    c = e.make_cache(2)
+    got = e.run(c)
+    _assert_close(got, e.oracle())
+    assert c.device_error() == 0
+
+
 def test_extend_invalid_prefix_block_is_flagged():
     # a block-table entry of sequence 1's prefix out of range: flagged, its
     # page skipped; sequence 0 (and its new tokens) are unaffected
