@@ -601,13 +601,15 @@ def _store_workload(torch, tq, wl, device, steps, warmup, flush, peak, with_boun
     return line, cases
 
 
-def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4, split_blocks=128):
-    """Extend (prefill) attention on the 8B shape (context line): batch
-    sequences, each with `prefix` compressed tokens and `chunk` new exact
-    tokens that attend causally among themselves."""
+def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, chunk=256, batch=4, split_blocks=128,
+                     shape="llama8b_gqa4_b16_8k"):
+    """Extend (prefill) attention on the 8B shape (context line; the 70B shape
+    with shape="llama70b_gqa8_b4_ragged131k_hybrid"): batch sequences, each
+    with `prefix` compressed tokens and `chunk` new exact tokens that attend
+    causally among themselves."""
     import numpy as np
 
-    w = wl.scaled(wl.config("llama8b_gqa4_b16_8k"), batch=batch, seq_lens=[prefix] * batch)
+    w = wl.scaled(wl.config(shape), batch=batch, seq_lens=[prefix] * batch, tail=0)
     table, num_blocks = wl.block_table(w)
     T = batch * chunk
     c = tq.TQCache(device=device, **{**wl.cache_config_kwargs(w, num_blocks=num_blocks, max_blocks=table.shape[1],
@@ -640,7 +642,8 @@ def _extend_workload(torch, tq, wl, device, steps, warmup, flush, prefix=4096, c
         raise RuntimeError("device error during the extend workload")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     attended = T * prefix + batch * chunk * (chunk + 1) // 2
-    return {"workload": f"llama8b_gqa4 extend: {batch} seqs x {prefix}-token compressed prefix + {chunk} new tokens",
+    tag = "llama8b_gqa4" if shape.startswith("llama8b") else "llama70b_gqa8"
+    return {"workload": f"{tag} extend: {batch} seqs x {prefix}-token compressed prefix + {chunk} new tokens",
             "new_tokens_per_s": T / (ms * 1e-3), "attended_kv_tokens_per_s": attended / (ms * 1e-3), "ms": ms,
             "split_blocks": split_blocks, "calls": steps}
 
@@ -732,7 +735,7 @@ def run_ours(args):
     del c, st
     torch.cuda.empty_cache()
 
-    extra = store_line = cases = extend_line = None
+    extra = store_line = cases = extend_line = extend_line8 = None
     if rank == 0 and not args.no_decode_workloads and args.workload == DEFAULT_WORKLOAD:
         extra = [_decode_workload(torch, tq, wl, wl.config(name), device, max(5, min(args.steps, 20)),
                                   max(3, args.warmup), flush, peak, peak_kind) for name in EXTRA_DECODES]
@@ -741,6 +744,8 @@ def run_ours(args):
                                             with_boundary_cases=not args.no_boundary_cases)
     if not args.no_extend_workload and rank == 0:
         extend_line = _extend_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush)
+        extend_line8 = _extend_workload(torch, tq, wl, device, max(3, min(args.steps, 20)), 3, flush,
+                                        shape="llama70b_gqa8_b4_ragged131k_hybrid")
 
     if rank == 0:
         cpu = None
@@ -781,6 +786,7 @@ def run_ours(args):
             "store_workload": store_line,
             "boundary_cases": cases,
             "extend_workload": extend_line,
+            "extend_workload_gqa8": extend_line8,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
