@@ -379,9 +379,14 @@ def run_reference(args):
 # --------------------------------------------------------------- our arm
 def _split_blocks(w, override=0):
     """Blocks per decode split: longer splits for long contexts; a short one
-    (a few work items in all) needs short splits to spread over the SMs."""
+    (a few work items in all) needs short splits to spread over the SMs.  Each
+    CTA takes a contiguous run of equal numbers of splits, so the choice sets
+    the balance: measured on the 8B-shaped decode (16 x 8192 tokens), 80-block
+    splits (three per CTA) took the split kernel 72.3 us against 74.2 at 32
+    and 80.7 at 56; on the d=256 and 70B-shaped decodes 64 was best or within
+    noise of the best."""
     longest = max(w.seq_lens)
-    return override or (64 if longest > 16384 else 32 if longest > 2048 else 8)
+    return override or (64 if longest > 16384 else 80 if longest > 4096 else 32 if longest > 2048 else 8)
 
 
 def _setup_decode(w, split_blocks, torch, tq, wl, device):

@@ -6,6 +6,7 @@ and relative-L2 1e-3 (fp32 output)."""
 import numpy as np
 import pytest
 
+import bench
 import parity
 import turboquant_bit_kv_tq_gb300 as tq
 from oracle import paged
@@ -336,19 +337,22 @@ def _sampled_full_size(name, picks, split_blocks, changes=None):
 
 
 def test_decode_full_size_llama8b_sampled():
-    _sampled_full_size("llama8b_gqa4_b16_8k", [(0, 0), (9, 5), (15, 7)], split_blocks=32)
+    _sampled_full_size("llama8b_gqa4_b16_8k", [(0, 0), (9, 5), (15, 7)],
+                       split_blocks=bench._split_blocks(wl.config("llama8b_gqa4_b16_8k")))
 
 
 def test_decode_full_size_d256_sampled():
-    _sampled_full_size("d256_gqa8_b8_32k", [(3, 1), (7, 3)], split_blocks=64)
+    _sampled_full_size("d256_gqa8_b8_32k", [(3, 1), (7, 3)],
+                       split_blocks=bench._split_blocks(wl.config("d256_gqa8_b8_32k")))
 
 
 def test_decode_full_size_llama8b_uniform_k4_sampled():
-    _sampled_full_size("llama8b_gqa4_b16_8k", [(2, 1), (12, 6)], split_blocks=32,
+    _sampled_full_size("llama8b_gqa4_b16_8k", [(2, 1), (12, 6)],
+                       split_blocks=bench._split_blocks(wl.config("llama8b_gqa4_b16_8k")),
                        changes=dict(k_bits=4, k_codebook="uniform"))
 
 
 def test_decode_full_size_hybrid131k_sampled():
     w = wl.config("llama70b_gqa8_b4_ragged131k_hybrid")
     longest = int(np.argmax(w.seq_lens))
-    _sampled_full_size("llama70b_gqa8_b4_ragged131k_hybrid", [(longest, 2)], split_blocks=64)
+    _sampled_full_size("llama70b_gqa8_b4_ragged131k_hybrid", [(longest, 2)], split_blocks=bench._split_blocks(w))
