@@ -132,6 +132,40 @@ def test_extend_many_sequences():
     assert c.device_error() == 0
 
 
+def test_extend_cuda_graph_replay_with_new_lengths():
+    # the grid depends only on the token and sequence counts (the query-block
+    # plan is made on the device): capture once, replay with changed prefix
+    # lengths and chunk boundaries
+    w = wl.config("llama8b_gqa4_b16_8k")
+    e = Extend(w, [120, 40, 77], [5, 9, 6])
+    c = e.make_cache(2, tail_cap=12)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q = torch.from_numpy(np.ascontiguousarray(e.Q)).to("cuda", dt)
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda", torch.bfloat16)  # noqa: E731
+    nk, nv = bf(e.ck), bf(e.cv)
+    tab = torch.from_numpy(e.table).cuda()
+    pl = torch.tensor(e.prefix, dtype=torch.int32, device="cuda")
+    cu = torch.from_numpy(e.cu).cuda()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c.extend(q, tab, pl, cu, nk, nv, out=out, stream=s)  # warm-up outside capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c.extend(q, tab, pl, cu, nk, nv, out=out, stream=s)
+    for new_prefix, new_cu in (([120, 40, 77], [0, 5, 14, 20]), ([30, 0, 77], [0, 5, 14, 20]),
+                               ([120, 16, 1], [0, 10, 14, 20])):
+        pl.copy_(torch.tensor(new_prefix, dtype=torch.int32))
+        cu.copy_(torch.tensor(new_cu, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        assert c.device_error() == 0
+        ref = paged.extend_attention(e.cache, e.P, e.Q.astype(np.float64), e.table, new_prefix,
+                                     np.asarray(new_cu, np.int32), e.ck, e.cv)
+        _assert_close(out.cpu().numpy(), ref)
+
+
 def test_extend_invalid_prefix_block_is_flagged():
     # a block-table entry of sequence 1's prefix out of range: flagged, its
     # page skipped; sequence 0 (and its new tokens) are unaffected
