@@ -334,13 +334,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
-    for (int e = tid; e < GV * D; e += blockDim.x) {
-        const int h = e / D, i = e % D;
-        float* dst = a.ws_q + hrow(h) * 3 * D;
-        dst[i] = rq[e];
-        dst[D + i] = sq[e];
-        dst[2 * D + i] = qv[e] * f;
-    }
+    // the scaled query for the exact tail's scores (row 2 of the head's
+    // workspace rows; the tail split reads nothing else of them, and extend's
+    // exact part reads the raw queries)
+    if (a.tail_cap > 0 && !a.chunk_attn)
+        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * 3 * D + 2 * D + e % D] = qv[e] * f;
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
     const float* kw = s_kw;
