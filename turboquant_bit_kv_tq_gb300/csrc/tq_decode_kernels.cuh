@@ -176,7 +176,8 @@ __device__ __forceinline__ void mma_fp8_ts(uint32_t d, uint32_t a, uint64_t bdes
         : "memory");
 }
 // ------------------------------------------------------------------ prep
-// ws_q[b][h] = { R q * f, S q * f * sqrt(pi/2)/d, q * f },  f = scale*log2(e);
+// ws_q[b][h] = q * f (when a hybrid tail reads it), f = scale*log2(e); R q * f
+// and S q * f * sqrt(pi/2)/d stay in shared memory for what follows:
 // ws_cst[b][h] = { C_h, Q_h, 2^-sigmaK, 2^-sigmaQ } with
 //   C_h = alpha sum_i (Rq)_i + 1/2 sum_P beta_P sum_{i%8=7} (Rq)_i
 //   Q_h = -sum_j (Sq)_j + sum_{j%8=7} (Sq)_j
@@ -334,11 +335,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
-    // the scaled query for the exact tail's scores (row 2 of the head's
-    // workspace rows; the tail split reads nothing else of them, and extend's
-    // exact part reads the raw queries)
+    // the scaled query for the exact tail's scores (extend's exact part reads
+    // the raw queries)
     if (a.tail_cap > 0 && !a.chunk_attn)
-        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * 3 * D + 2 * D + e % D] = qv[e] * f;
+        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * D + e % D] = qv[e] * f;
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
     const float* kw = s_kw;
@@ -736,7 +736,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
     float* pr = qs + G * D;                      // [G][kTile]
     float* sm_m = pr + G * kTile;                // [G]
     for (int e = tid; e < G * D; e += blockDim.x)
-        qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + e / D) * 3 * D + 2 * D + e % D];
+        qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + e / D) * D + e % D];
     int tl = a.tail_lens ? a.tail_lens[b] : 0;
     if (tl < 0 || tl > a.tail_cap) {
         if (tid == 0 && g == 0) set_error(a.dp.err, TQ_DEVERR_TAIL);

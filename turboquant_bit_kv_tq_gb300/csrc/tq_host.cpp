@@ -133,7 +133,7 @@ WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     WorkspaceLayout w;
     size_t off = 0;
     w.q = off;
-    off = up256(off + bh * 3 * d * 4);
+    off = up256(off + bh * d * 4);
     w.bimg = off;
     off = up256(off + size_t(c.max_batch) * c.num_kv_heads * gm.nhg * gm.bimg_bytes);
     w.cst = off;
