@@ -85,13 +85,14 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         // the split (and tail) and combine kernels launch programmatically
         // (each one's prologue overlaps the previous kernel's tail) unless
         // profiling events sit between the launches; the query prep launches
-        // in stream order (overlapping it with a preceding store measured
-        // slower)
+        // programmatically too, but waits for its predecessor before any read
+        // (that hides the launch gap; running it beside a preceding store
+        // measured slower)
         a.pdl = ev0 == nullptr && ev1 == nullptr;
         if (a.prep_entries < 1 || a.prep_entries * a.group > kPrepV) a.prep_entries = 1;
         const size_t prep_smem = prep_smem_bytes<D>(a.prep_entries * a.group);
         const dim3 pgrid(a.heads, (a.batch + a.prep_entries - 1) / a.prep_entries);
-        const cudaError_t e = launch_pdl(false, prep_kernel<D>, pgrid, dim3(kPrepThreads), prep_smem, s, a);
+        const cudaError_t e = launch_pdl(true, prep_kernel<D>, pgrid, dim3(kPrepThreads), prep_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {

@@ -201,6 +201,9 @@ __host__ __device__ constexpr size_t prep_smem_bytes(int GV) {
 constexpr int kPrepThreads = 512;  // its phases are short serial chains
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
+    // launched programmatically: the preceding kernel (the step's store, or
+    // whatever wrote the queries) must be complete before anything is read
+    pdl_wait();
     pdl_launch_dependents();  // the split kernel's prologue may start
     const int g = blockIdx.x, E = a.prep_entries, b0 = blockIdx.y * E;
     const int ne = min(E, a.batch - b0);

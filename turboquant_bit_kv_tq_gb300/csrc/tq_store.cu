@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(StoreBulkLayout<D>::kWarps * 32) store_kernel(
 // The sums run over i in the same order as store_kernel's.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
+    // a programmatically launched successor (the decode's query prep) may be
+    // scheduled now; it waits for this grid to finish before it reads anything
+    pdl_launch_dependents();
     constexpr int PER = D / 32;
     constexpr int kChunk = 16;  // uint4 (8 bf16) loads of an S row held at once
     __shared__ __align__(16) float r_s[D];
