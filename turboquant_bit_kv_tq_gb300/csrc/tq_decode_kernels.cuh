@@ -176,6 +176,22 @@ __device__ __forceinline__ void mma_fp8_ts(uint32_t d, uint32_t a, uint64_t bdes
         : "memory");
 }
 // ------------------------------------------------------------------ prep
+__device__ __forceinline__ void mma_bf16f32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two 8x8 b16 matrices from shared memory, transposed: lanes 0-7 give the row
+// addresses (16 bytes each, 16-byte aligned) of the first, lanes 8-15 of the
+// second; r0/r1 then hold a k-major [16 x 8] block as an mma B fragment.
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 // ws_q[b][h] = q * f (when a hybrid tail reads it), f = scale*log2(e); R q * f
 // and S q * f * sqrt(pi/2)/d stay in shared memory for what follows:
 // ws_cst[b][h] = { C_h, Q_h, 2^-sigmaK, 2^-sigmaQ } with
@@ -193,9 +209,12 @@ __device__ __forceinline__ void mma_fp8_ts(uint32_t d, uint32_t a, uint64_t bdes
 // as "virtual heads" v = e G + h, with S^T staged once.  Every head's
 // arithmetic is the same for any entry count.
 constexpr int kPrepMaxV = 32;  // virtual heads per CTA at most
+// the staged queries' row pitch is D + kPrepQPad floats, so that the eight
+// rows of an mma A fragment fall on different banks
+constexpr int kPrepQPad = 8;
 template <int D>
 __host__ __device__ constexpr size_t prep_smem_bytes(int GV) {
-    return (size_t)D * D * 2 + (size_t)3 * GV * D * 4 + 2 * kPrepMaxV * 4 + 16;
+    return (size_t)D * D * 2 + (size_t)3 * GV * D * 4 + (size_t)GV * kPrepQPad * 4 + 2 * kPrepMaxV * 4 + 16;
 }
 
 constexpr int kPrepThreads = 512;  // its phases are short serial chains
@@ -221,8 +240,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     auto hrow = [&](int v) { return (int64_t)(b0 + v / G) * a.q_heads + (int64_t)g * G + v % G; };
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t* st = reinterpret_cast<uint16_t*>(smem);           // S^T bf16 [D][D]
-    float* qv = reinterpret_cast<float*>(smem + (size_t)D * D * 2);  // [GV][D]
-    float* rq = qv + GV * D;                                    // [GV][D]
+    constexpr int QS = D + kPrepQPad;                           // row pitch of qv
+    float* qv = reinterpret_cast<float*>(smem + (size_t)D * D * 2);  // [GV][QS]
+    float* rq = qv + GV * QS;                                   // [GV][D]
     float* sq = rq + GV * D;                                    // [GV][D]
     float* sig = sq + GV * D;                                   // [kPrepMaxV][2] = 2^sigmaK, 2^sigmaQ
     uint64_t* bar = reinterpret_cast<uint64_t*>(sig + 2 * kMaxG);
@@ -237,23 +257,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     __shared__ float s_signs[D], s_kw[9];
     for (int e = tid; e < GV * D; e += blockDim.x) {
         const int64_t src = hrow(e / D) * D + e % D;
-        qv[e] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[src]
+        qv[(e / D) * QS + e % D] = a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[src]
                                           : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[src]);
     }
     for (int e = tid; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
     __syncthreads();
     const float f = a.scale_log2e;
-    // per-head sums and maxima for the constants below, taken where the values
-    // are made: [head][0..2] sum, sum over i % 8 = 7, max of |v| bit_weight(i % 8)
-    // of R q (one entry per head) and of S q (one entry per warp of the head)
-    constexpr int kSqWarps = D / 64;  // warps per head in the S q phase
+    // per-head sums and maxima for the constants below: [head][0..2] sum, sum
+    // over i % 8 = 7, max of |v| bit_weight(i % 8) of R q (one entry per head)
+    // and of S q (one entry per warp of the head, on the one-pass S q path;
+    // the tensor-core path takes them in the constants phase)
+    constexpr int kSqWarps = D / 64;  // warps per head in the one-pass S q
     __shared__ float red_r[kPrepMaxV][3], red_s[kPrepMaxV][kSqWarps][3];
     // R q by an in-warp Hadamard transform (one warp per head)
     for (int h = warp; h < GV; h += nwarps) {
         float x[D / 32];
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) x[k] = qv[h * D + lane + 32 * k] * s_signs[lane + 32 * k];
+        for (int k = 0; k < D / 32; ++k) x[k] = qv[h * QS + lane + 32 * k] * s_signs[lane + 32 * k];
         fwht_warp<D / 32>(x, lane);
         const float bw = fabsf(bit_weight(lane & 7));  // i % 8 = lane % 8 for i = lane + 32 k
         float s0 = 0.f, m0 = 0.f;
@@ -273,13 +294,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
             red_r[h][2] = m0;
         }
     }
-    // S q from the shared copy of S^T: thread (column pair j, j + 1; a block
-    // of HPT heads), 32-bit loads of S^T pairs (each serving the block's
-    // heads) and 128-bit loads of four query elements.  HPT = 4 when one pass
-    // of single heads would not cover the CTA's heads (a query block of
-    // extend), 1 otherwise; every head's sums run in the same order either way.
+    // S q.  When one pass of single heads covers the CTA's heads (decode's
+    // head groups at d = 128): thread (column pair j, j + 1; head), 32-bit
+    // loads of S^T pairs and 128-bit loads of four query elements, with the
+    // head's sums taken in the same pass.  Otherwise (more heads, d = 256)
+    // on the tensor cores, sums in the constants phase.
     bool s_ok = mbar_wait(smem_u32(bar), 0, a.dp.err);
     const float kq = f * sqrtf(1.5707963267948966f) / (float)D;
+    const bool sq_tc = GV > kPrepThreads / (D / 2);
     auto sq_pass = [&](auto hpt_c) {
         constexpr int HPT = decltype(hpt_c)::value;
         constexpr int NP = D / 2;                 // column pairs
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
                     for (int hh = 0; hh < HPT; ++hh) {
                         const int h = hb * HPT + hh;
                         if (h < GV) {
-                            const float4 qq = reinterpret_cast<const float4*>(qv + h * D)[i4];
+                            const float4 qq = reinterpret_cast<const float4*>(qv + h * QS)[i4];
                             const float qa[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
@@ -331,17 +353,74 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
             }
         }
     };
-    if (GV > kPrepThreads / (D / 2))
-        sq_pass(std::integral_constant<int, 4>{});
-    else
-        sq_pass(std::integral_constant<int, 1>{});
+    if (!sq_tc) sq_pass(std::integral_constant<int, 1>{});
+    if (sq_tc && s_ok) {
+        // tensor cores: sq[h][j] = kq sum_i q[h][i] S^T[i][j] with bf16 operands
+        // and fp32 accumulation (a bf16 query is exact in one part, an fp32
+        // query is split into three bf16 parts); warp w takes the 8-column
+        // blocks nt = w, w + nwarps, ... of every head
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const int nparts = a.q_dtype == TQ_DTYPE_F32 ? 3 : 1;
+        static_assert(kPrepMaxV <= 32, "two 16-head row tiles at most");
+        for (int nt = warp; nt < D / 8; nt += nwarps) {
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 2
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t b0, b1;
+                ldsm_x2_trans(b0, b1, smem_u32(st + (16 * ks + (lane & 15)) * D + 8 * nt));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    if (16 * mt >= GV) break;
+                    // A rows: heads 16 mt + g8 and 16 mt + g8 + 8; columns
+                    // 16 ks + 2 t4 (+1, +8, +9)
+                    float xa[2][4];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int h = 16 * mt + g8 + 8 * r;
+                        const float* qr = qv + h * QS + 16 * ks + 2 * t4;
+                        const bool in = h < GV;
+                        xa[r][0] = in ? qr[0] : 0.f;
+                        xa[r][1] = in ? qr[1] : 0.f;
+                        xa[r][2] = in ? qr[8] : 0.f;
+                        xa[r][3] = in ? qr[9] : 0.f;
+                    }
+                    for (int part = 0; part < nparts; ++part) {
+                        const uint32_t af[4] = {pack_bf16x2(xa[0][0], xa[0][1]), pack_bf16x2(xa[1][0], xa[1][1]),
+                                                pack_bf16x2(xa[0][2], xa[0][3]), pack_bf16x2(xa[1][2], xa[1][3])};
+                        mma_bf16f32(c[mt], af, b0, b1);
+                        if (part + 1 < nparts) {
+                            // the remainders for the next part
+#pragma unroll
+                            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const uint32_t w2 = af[2 * e + r];
+                                    xa[r][2 * e] -= __uint_as_float(w2 << 16);
+                                    xa[r][2 * e + 1] -= __uint_as_float(w2 & 0xFFFF0000u);
+                                }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int h = 16 * mt + g8 + 8 * r;
+                    if (h < GV) {
+                        sq[h * D + 8 * nt + 2 * t4] = c[mt][2 * r] * kq;
+                        sq[h * D + 8 * nt + 2 * t4 + 1] = c[mt][2 * r + 1] * kq;
+                    }
+                }
+        }
+    }
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
     // the scaled query for the exact tail's scores (extend's exact part reads
     // the raw queries)
     if (a.tail_cap > 0 && !a.chunk_attn)
-        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * D + e % D] = qv[e] * f;
+        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * D + e % D] = qv[(e / D) * QS + e % D] * f;
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
     const float* kw = s_kw;
@@ -350,15 +429,29 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
         bmax = fmaxf(bmax, fabsf(kw[1 + p]));
         bsum += kw[1 + p];
     }
-    for (int h = tid; h < GV; h += blockDim.x) {
-        const float s_rq = red_r[h][0], s_rq7 = red_r[h][1], m_rq = red_r[h][2] * bmax;
+    for (int h = warp; h < GV; h += nwarps) {
+        // S q's sum, sum over j % 8 = 7 and max of |v| bit_weight(j % 8)
         float s_sq = 0.f, s_sq7 = 0.f, m_sq = 0.f;
+        if (sq_tc) {
 #pragma unroll
-        for (int w = 0; w < kSqWarps; ++w) {
-            s_sq += red_s[h][w][0];
-            s_sq7 += red_s[h][w][1];
-            m_sq = fmaxf(m_sq, red_s[h][w][2]);
+            for (int k = 0; k < D / 32; ++k) {
+                const float v = sq[h * D + lane + 32 * k];  // j % 8 = lane % 8
+                s_sq += v;
+                m_sq = fmaxf(m_sq, fabsf(v) * fabsf(bit_weight(lane & 7)));
+            }
+            s_sq7 = warp_sum((lane & 7) == 7 ? s_sq : 0.f);
+            s_sq = warp_sum(s_sq);
+            m_sq = warp_max(m_sq);
+        } else {
+#pragma unroll
+            for (int w = 0; w < kSqWarps; ++w) {
+                s_sq += red_s[h][w][0];
+                s_sq7 += red_s[h][w][1];
+                m_sq = fmaxf(m_sq, red_s[h][w][2]);
+            }
         }
+        if (lane != 0) continue;
+        const float s_rq = red_r[h][0], s_rq7 = red_r[h][1], m_rq = red_r[h][2] * bmax;
         m_sq *= 2.f;
         {
             // operand scales 2^e with 2^e m <= 224 (e4m3 holds up to 448): e is
@@ -462,12 +555,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
 constexpr int kChunkRows = 16;
 constexpr int kChunkKeys = 64;
 constexpr int kChunkMaxWarps = 8;
-
-__device__ __forceinline__ void mma_bf16f32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
