@@ -126,8 +126,8 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
     }
     if (st != TQ_OK) return st;
     if (ev1) cudaEventRecord((cudaEvent_t)ev1, s);
-    return cuda_status(launch_pdl(a.pdl, combine_kernel<D>, dim3(a.q_heads, a.batch), dim3(128),
-                                  (size_t)a.sp.n_splits * sizeof(float), s, a));
+    return cuda_status(launch_pdl(a.pdl, a.sp.n_splits <= 8 ? combine_kernel<D, 8> : combine_kernel<D, 32>,
+                                  dim3(a.q_heads, a.batch), dim3(128), (size_t)a.sp.n_splits * sizeof(float), s, a));
 }
 
 tq_status launch_decode(const DecodeArgs& a, cudaStream_t s, void* ev0, void* ev1) {

@@ -1545,7 +1545,9 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
 }
 
 // --------------------------------------------------------------- combine
-template <int D>
+// kPre: splits whose partials load beside the (m, l) pairs (8 when a row has
+// at most 8 splits: fewer registers, more CTAs per SM; else 32)
+template <int D, int kPre>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     pdl_launch_dependents();
     pdl_wait();  // the split partials
@@ -1560,7 +1562,6 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the first kPre splits' partials load now, beside the (m, l) pairs,
     // instead of after the two reductions below
-    constexpr int kPre = 32;
     const float* src = a.ws_acc + base * D + tid;
     float pre[kPre][kPerThread];
 #pragma unroll
@@ -1592,6 +1593,12 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
             const float ws = __shfl_sync(0xffffffffu, w, s);
 #pragma unroll
             for (int p = 0; p < kPerThread; ++p) acc[p] = ws > 0.f ? fmaf(ws, pre[s][p], acc[p]) : acc[p];
+        }
+        for (int s = kPre; s < S; ++s) {
+            const float ws = __shfl_sync(0xffffffffu, w, s);
+#pragma unroll
+            for (int p = 0; p < kPerThread; ++p)
+                if (ws > 0.f) acc[p] = fmaf(ws, src[(int64_t)s * D + 128 * p], acc[p]);
         }
     } else {
         float M = -INFINITY;
