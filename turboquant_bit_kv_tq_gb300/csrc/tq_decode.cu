@@ -46,6 +46,7 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         // the query prep takes as many entries per CTA as its virtual-head
         // limit allows (S^T staged once for them)
         a.prep_entries = std::max(1, std::min(xp_block_tokens(), kPrepMaxV / a.group));
+        a.prep_late_release = true;
     } else if (ws_fits(gw, D)) {
         // persistent warp-specialized split kernel: two CTAs per SM, the
         // deepest ring that fits; the exact tail runs as its own kernel

@@ -76,6 +76,9 @@ struct DecodeArgs {
     const int32_t* xcounts = nullptr;
     int xblocks_max = 0;  // the plan's capacity (an upper bound of the block count)
     int prep_entries = 1;  // batch entries per query-prep CTA
+    // the query prep releases its dependents at its end rather than at its
+    // start (before the extend prefix kernel, which takes a whole SM)
+    bool prep_late_release = false;
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // launched programmatically: the preceding kernel (the step's store, or
     // whatever wrote the queries) must be complete before anything is read
     pdl_wait();
-    pdl_launch_dependents();  // the split kernel's prologue may start
+    if (!a.prep_late_release) pdl_launch_dependents();  // the split kernel's prologue may start
     const int g = blockIdx.x, E = a.prep_entries, b0 = blockIdx.y * E;
     const int ne = min(E, a.batch - b0);
     if (ne <= 0) return;
@@ -535,6 +538,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
                     make_uint4(word[k][0], word[k][1], word[k][2], word[k][3]);
         }
     }
+    if (a.prep_late_release) pdl_launch_dependents();
 }
 
 // ------------------------------------------------- extend: exact chunk part

@@ -363,15 +363,10 @@ __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
     const int64_t t = w / a.heads;
     const int h = (int)(w - t * a.heads);
     const int64_t slot = a.slots[t];
-    if (slot < 0 || slot >= a.num_slots) {
-        if (slot != -1 && threadIdx.x == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
-        return;
-    }
-    const int row = (int)(slot & 15);
-    uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
     const bool qjl = L.k_qjl;
-    // every load of the encoding at once: the input vector (warp 0: key,
-    // warp 1: value), the tables, and this warp's first S rows
+    // every load of the encoding at once, the slot's among them (none of the
+    // others depends on it): the input vector (warp 0: key, warp 1: value),
+    // the tables, and this warp's first S rows
     float x[PER];
     if (warp < 2) {
         const Tin* in = static_cast<const Tin*>(warp == 0 ? a.k : a.v) + w * D;
@@ -390,6 +385,13 @@ __global__ void __launch_bounds__(D) store_small_kernel(StoreArgs a) {
 #pragma unroll
         for (int q = 0; q < kChunk; ++q) sv[q] = __ldg(srow + q);
     }
+    // a skipped or bad slot ends the block (uniformly: the slot is per block)
+    if (slot < 0 || slot >= a.num_slots) {
+        if (slot != -1 && threadIdx.x == 0 && h == 0) set_error(a.dp.err, TQ_DEVERR_SLOT);
+        return;
+    }
+    const int row = (int)(slot & 15);
+    uint8_t* page = a.cache + ((slot >> 4) * a.heads + h) * (int64_t)L.page_bytes;
     __syncthreads();
     if (warp == 0) {
         // ------------------------------------------------------------ key
