@@ -112,6 +112,9 @@ CASES = [
     ("single_head_full", "single_head_d128_1k", {}, [1024], None, 0, 8),
     ("gqa4_ragged", "llama8b_gqa4_b16_8k", {}, [0, 1, 15, 16, 17, 300], None, 0, 4),
     ("d256_gqa8", "d256_gqa8_b8_32k", {}, [1, 33, 700], None, 0, 8),
+    # fp32 queries with eight heads per prep CTA at d=256: the prep's S q on
+    # tensor cores, the query in three bf16 parts
+    ("d256_gqa8_f32q", "d256_gqa8_b8_32k", dict(dtype="f32"), [65, 300], None, 0, 8),
     ("hybrid_gqa8", "llama70b_gqa8_b4_ragged131k_hybrid", {}, [15, 16, 500, 0], [0, 5, 128, 3], 128, 4),
     ("mse3_tail", "d256_gqa8_b8_32k", dict(v_bits=3, k_bits=4, tail=32), [40, 0], [7, 32], 32, 1),
     ("g32v2_k2", "llama8b_gqa4_b16_8k", dict(v_bits=2, k_bits=2), [129, 64], None, 0, 2),

@@ -88,6 +88,9 @@ CASES = [
     ("uniform_k4_gqa8", "llama70b_gqa8_b4_ragged131k_hybrid", dict(k_bits=4, k_codebook="uniform", tail=0),
      [64, 500], [12, 2], 8),
     ("f32_single_head", "single_head_d128_1k", {}, [1024], [8], 8),
+    # fp32 queries in the prefix kernel's query blocks (32 virtual heads per
+    # prep CTA: S q on tensor cores, the query in three bf16 parts)
+    ("gqa4_f32_queries", "llama8b_gqa4_b16_8k", dict(dtype="f32"), [200, 70], [9, 12], 4),
     ("prefill_only", "llama8b_gqa4_b16_8k", {}, [0, 0], [16, 3], 4),
     ("prefill_long_chunks", "llama8b_gqa4_b16_8k", {}, [0, 5], [150, 77], 4),
     ("k4_lloyd_fallback_kernel", "llama8b_gqa4_b16_8k", dict(k_bits=4), [100, 7], [9, 4], 4),
