@@ -97,7 +97,9 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {
-        const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
+        const size_t tail_smem = tail_smem_bytes<D>(a.group);
+        const tq_status fs = ensure_dynamic_smem((const void*)tail_kernel<D>, (int)tail_smem_bytes<D>(kMaxG), "tail_kernel");
+        if (fs != TQ_OK) return fs;
         const cudaError_t e = launch_pdl(a.pdl, tail_kernel<D>, dim3(a.heads, a.batch), dim3(128), tail_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }

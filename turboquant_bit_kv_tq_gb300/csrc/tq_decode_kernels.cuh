@@ -47,6 +47,13 @@ namespace tq {
 
 constexpr int kTile = 128;  // tail split: tokens per smem tile
 constexpr int kMaxG = 16;
+constexpr int kTailV = 64;  // tail split: value rows staged in shared memory at a time
+// shared memory of the exact tail split: scaled queries, scores, maxima and
+// the staged value rows (bf16)
+template <int D>
+__host__ __device__ constexpr size_t tail_smem_bytes(int G) {
+    return (size_t)G * D * 4 + (size_t)G * kTile * 4 + kMaxG * 4 + (size_t)kTailV * D * 2;
+}
 constexpr int kWarpsPerGroup = 4;
 
 struct DecodeArgs {
@@ -829,6 +836,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
     float* qs = reinterpret_cast<float*>(smem);  // [G][D] = q * f
     float* pr = qs + G * D;                      // [G][kTile]
     float* sm_m = pr + G * kTile;                // [G]
+    uint16_t* vst = reinterpret_cast<uint16_t*>(sm_m + kMaxG);  // [kTailV][D] staged values (bf16)
     for (int e = tid; e < G * D; e += blockDim.x)
         qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + e / D) * D + e % D];
     int tl = a.tail_lens ? a.tail_lens[b] : 0;
@@ -861,6 +869,8 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
             float s[kMaxG];
 #pragma unroll
             for (int h = 0; h < kMaxG; ++h) s[h] = 0.f;
+            // (unrolled: the row's loads issue together)
+#pragma unroll
             for (int i8 = 0; i8 < D / 8; ++i8) {
                 const uint4 u = __ldg(krow + i8);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -913,19 +923,30 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
 #pragma unroll
             for (int p = 0; p < kPerThread; ++p) acc[h][p] *= alpha;
         }
-        if (tid < 128) {
+        // values, a thread per coordinate, from kTailV-row chunks staged in
+        // shared memory with 16-byte loads (one memory latency per chunk)
+        for (int c0 = 0; c0 < n_tok; c0 += kTailV) {
+            const int nc = min(kTailV, n_tok - c0);
+            for (int e = tid; e < nc * (D / 8); e += blockDim.x) {
+                const int t = e / (D / 8), c8 = e % (D / 8);
+                reinterpret_cast<uint4*>(vst)[e] =
+                    __ldg(reinterpret_cast<const uint4*>(a.tail_v + tail_off(tt + c0 + t)) + c8);
+            }
+            __syncthreads();
+            if (tid < 128) {
 #pragma unroll
-            for (int p = 0; p < kPerThread; ++p) {
-                const int i = tid + 128 * p;
-                for (int t = 0; t < n_tok; ++t) {
-                    const float v = bf16_bits_to_float(a.tail_v[tail_off(tt + t) + i]);
+                for (int p = 0; p < kPerThread; ++p) {
+                    const int i = tid + 128 * p;
+                    for (int t = 0; t < nc; ++t) {
+                        const float v = bf16_bits_to_float(vst[t * D + i]);
 #pragma unroll
-                    for (int h = 0; h < kMaxG; ++h)
-                        if (h < G) acc[h][p] = fmaf(pr[h * kTile + t], v, acc[h][p]);
+                        for (int h = 0; h < kMaxG; ++h)
+                            if (h < G) acc[h][p] = fmaf(pr[h * kTile + c0 + t], v, acc[h][p]);
+                    }
                 }
             }
+            __syncthreads();  // the staged rows are consumed
         }
-        __syncthreads();
     }
     // MSE values are combined in the rotated space: acc <- R acc = H D acc / sqrt(d)
     if (a.lay.v_mode == TQ_V_MSE) {
@@ -1726,7 +1747,7 @@ tq_status dispatch_split(const DecodeArgs& a, cudaStream_t s, size_t smem, int g
 template <int D>
 inline tq_status split_config(const DecodeArgs& a, int* stages, size_t* smem) {
     const int nsets = a.lay.v_mode == TQ_V_G32 ? D / 32 : (1 << (a.lay.v_bits - 1));
-    const size_t tail_smem = (size_t)a.group * D * 4 + (size_t)a.group * kTile * 4 + kMaxG * 4;
+    const size_t tail_smem = tail_smem_bytes<D>(a.group);
     const size_t limits[2] = {112 * 1024, 226 * 1024};
     for (size_t lim : limits)
         for (int st = 4; st >= 2; --st) {
