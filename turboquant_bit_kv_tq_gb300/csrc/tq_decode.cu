@@ -97,10 +97,10 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (grid > 0 && a.tail_cap > 0 && !a.chunk_attn) {
-        const size_t tail_smem = tail_smem_bytes<D>(a.group);
-        const tq_status fs = ensure_dynamic_smem((const void*)tail_kernel<D>, (int)tail_smem_bytes<D>(kMaxG), "tail_kernel");
-        if (fs != TQ_OK) return fs;
-        const cudaError_t e = launch_pdl(a.pdl, tail_kernel<D>, dim3(a.heads, a.batch), dim3(128), tail_smem, s, a);
+        // one query head per CTA
+        const size_t tail_smem = tail_smem_bytes<D>(1);
+        const cudaError_t e =
+            launch_pdl(a.pdl, tail_kernel<D>, dim3(a.heads, a.batch, a.group), dim3(128), tail_smem, s, a);
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (ev0) cudaEventRecord((cudaEvent_t)ev0, s);

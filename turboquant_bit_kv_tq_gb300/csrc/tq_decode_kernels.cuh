@@ -829,16 +829,17 @@ __global__ void __launch_bounds__(32 * kChunkMaxWarps) chunk_attn_kernel(DecodeA
 // Exact bf16 tail tokens on CUDA cores (scores by (token, head), values by
 // coordinate); partial in the same form as the compressed splits.
 template <int D>
-__device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
+__device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem, int h0, int NH) {
     constexpr int kPerThread = D / 128;
+    // query heads h0 .. h0 + NH - 1 of the group
     const int G = a.group, tid = threadIdx.x;
     const int chunk = a.sp.n_chunks;
-    float* qs = reinterpret_cast<float*>(smem);  // [G][D] = q * f
-    float* pr = qs + G * D;                      // [G][kTile]
-    float* sm_m = pr + G * kTile;                // [G]
+    float* qs = reinterpret_cast<float*>(smem);  // [NH][D] = q * f
+    float* pr = qs + NH * D;                     // [NH][kTile]
+    float* sm_m = pr + NH * kTile;               // [NH]
     uint16_t* vst = reinterpret_cast<uint16_t*>(sm_m + kMaxG);  // [kTailV][D] staged values (bf16)
-    for (int e = tid; e < G * D; e += blockDim.x)
-        qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + e / D) * D + e % D];
+    for (int e = tid; e < NH * D; e += blockDim.x)
+        qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + h0 + e / D) * D + e % D];
     int tl = a.tail_lens ? a.tail_lens[b] : 0;
     if (tl < 0 || tl > a.tail_cap) {
         if (tid == 0 && g == 0) set_error(a.dp.err, TQ_DEVERR_TAIL);
@@ -860,7 +861,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
     };
     for (int tt = 0; tt < tl; tt += kTile) {
         const int n_tok = min(kTile, tl - tt);
-        for (int e = tid; e < G * kTile; e += blockDim.x) pr[e] = -INFINITY;
+        for (int e = tid; e < NH * kTile; e += blockDim.x) pr[e] = -INFINITY;
         __syncthreads();
         // a thread per token: one pass over its key row (16-byte loads) for
         // every head of the group
@@ -882,7 +883,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
                 }
 #pragma unroll
                 for (int h = 0; h < kMaxG; ++h) {
-                    if (h < G) {
+                    if (h < NH) {
                         const float* qh = qs + h * D + 8 * i8;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) s[h] = fmaf(qh[e], kf[e], s[h]);
@@ -891,12 +892,12 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
             }
 #pragma unroll
             for (int h = 0; h < kMaxG; ++h)
-                if (h < G) pr[h * kTile + t] = s[h];
+                if (h < NH) pr[h * kTile + t] = s[h];
         }
         __syncthreads();
         {
             const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-            for (int h = warp; h < G; h += nw) {
+            for (int h = warp; h < NH; h += nw) {
                 float mx = -INFINITY;
                 for (int t = lane; t < kTile; t += 32) mx = fmaxf(mx, pr[h * kTile + t]);
                 mx = warp_max(mx);
@@ -904,7 +905,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
             }
         }
         __syncthreads();
-        for (int e = tid; e < G * kTile; e += blockDim.x) {
+        for (int e = tid; e < NH * kTile; e += blockDim.x) {
             const float sv = pr[e];
             pr[e] = sv == -INFINITY ? 0.f : exp2f(sv - sm_m[e / kTile]);
         }
@@ -913,7 +914,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         // state in registers)
 #pragma unroll
         for (int h = 0; h < kMaxG; ++h) {
-            if (h >= G) continue;
+            if (h >= NH) continue;
             const float m_new = sm_m[h];
             const float alpha = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
             float psum = 0.f;
@@ -941,7 +942,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
                         const float v = bf16_bits_to_float(vst[t * D + i]);
 #pragma unroll
                         for (int h = 0; h < kMaxG; ++h)
-                            if (h < G) acc[h][p] = fmaf(pr[h * kTile + c0 + t], v, acc[h][p]);
+                            if (h < NH) acc[h][p] = fmaf(pr[h * kTile + c0 + t], v, acc[h][p]);
                     }
                 }
             }
@@ -955,7 +956,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         if (tid < 128)
 #pragma unroll
             for (int h = 0; h < kMaxG; ++h)
-                if (h < G)
+                if (h < NH)
 #pragma unroll
                     for (int p = 0; p < kPerThread; ++p)
                         buf[h * D + tid + 128 * p] = acc[h][p] * a.dp.signs[tid + 128 * p];
@@ -963,7 +964,7 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
         if (tid < 128)
 #pragma unroll
             for (int h = 0; h < kMaxG; ++h)
-                if (h < G)
+                if (h < NH)
 #pragma unroll
                     for (int p = 0; p < kPerThread; ++p) {
                         const int i = tid + 128 * p;
@@ -975,8 +976,8 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem) {
     if (tid < 128)
 #pragma unroll
         for (int h = 0; h < kMaxG; ++h) {
-            if (h >= G) continue;
-            const int64_t idx = ((int64_t)b * a.q_heads + g * G + h) * a.sp.n_splits + chunk;
+            if (h >= NH) continue;
+            const int64_t idx = ((int64_t)b * a.q_heads + g * G + h0 + h) * a.sp.n_splits + chunk;
 #pragma unroll
             for (int p = 0; p < kPerThread; ++p) a.ws_acc[idx * D + tid + 128 * p] = acc[h][p];
             if (tid == 0) {
@@ -1069,7 +1070,7 @@ __global__ void __launch_bounds__(128, 2) split_kernel(DecodeArgs a) {
     if (a.tail_cap > 0 && chunk == a.sp.n_chunks) {
         // all G heads of the tail in one CTA (extend's chunk kernel may have
         // written it already)
-        if (hgi == 0 && !a.chunk_attn) tail_split<D>(a, g, b, smem);
+        if (hgi == 0 && !a.chunk_attn) tail_split<D>(a, g, b, smem, 0, a.group);
         return;
     }
     const Layout& L = a.lay;

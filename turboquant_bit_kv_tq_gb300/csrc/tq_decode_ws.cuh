@@ -983,15 +983,17 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
     if (warp == 0) tmem_dealloc(tmem, kWsTmemCols);
 }
 
-// Exact hybrid-tail tokens of every (KV head, sequence) as split n_chunks.
+// Exact hybrid-tail tokens of every (KV head, sequence, query head) as split
+// n_chunks: one query head per CTA, so that the short tail spreads over the
+// SMs (the key and value rows are read once per query head, from L2)
 template <int D>
 __global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
     pdl_launch_dependents();
     pdl_wait();  // the query prep's results
     extern __shared__ __align__(16) uint8_t smem[];
-    const int g = blockIdx.x, b = blockIdx.y;
-    if (b >= a.batch) return;
-    tail_split<D>(a, g, b, smem);
+    const int g = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+    if (b >= a.batch || h >= a.group) return;
+    tail_split<D>(a, g, b, smem, h, 1);
 }
 
 template <int D, int KB, bool KU, bool G32, int VB, int NTH>
