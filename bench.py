@@ -2,8 +2,9 @@
 """Throughput of the TurboQuant KV-cache hot path on GB300.
 
 One step = one decode step of one attention layer for the whole batch: the
-fused store of every sequence's new token (tq_store) followed by decode
-attention over the compressed paged cache (tq_decode_attention), on seeded
+fused store of every sequence's new token followed by decode attention over
+the compressed paged cache, in one tq_store_decode_attention call (the same
+results as tq_store then tq_decode_attention), on seeded
 synthetic data with the workload's shapes.  Default workload: the
 Llama-3.1-8B-shaped decode layer (32 query / 8 KV heads, d=128, batch 16,
 8,192-token contexts, 3-bit keys + QJL, 4-bit group-32 values).
@@ -439,9 +440,8 @@ def _setup_decode(w, split_blocks, torch, tq, wl, device):
 
 
 def _step(c, st, stream):
-    c.store(st["new_k"], st["new_v"], st["new_slots"], stream=stream)
-    c.decode(st["q"], st["table"], st["lens"], out=st["out"], tail_k=st.get("tail_k"), tail_v=st.get("tail_v"),
-             tail_lens=st.get("tail_lens"), stream=stream)
+    c.store_decode(st["new_k"], st["new_v"], st["new_slots"], st["q"], st["table"], st["lens"], out=st["out"],
+                   tail_k=st.get("tail_k"), tail_v=st.get("tail_v"), tail_lens=st.get("tail_lens"), stream=stream)
 
 
 def _events(torch, n, stream):
@@ -771,7 +771,7 @@ def run_ours(args):
                        "l2": "flushed: 256 MiB buffer written between timed steps (outside the events)",
                        "clocks": "sampled every 50 ms over the timed steps plus untimed steps of the same "
                                  "load up to 0.6 s",
-                       "step": "tq_store of each sequence's new token + tq_decode_attention",
+                       "step": "tq_store_decode_attention: each sequence's new token stored, then the decode",
                        "timing": "value: K steps without profiling events; roofline: the split kernel's "
                                  "CUDA-event durations over K more steps with events around it"},
             "roofline": roof,

@@ -268,6 +268,26 @@ tq_status tq_decode_attention(const tq_cache* cache, const void* q, int q_dtype,
                               int out_dtype, void* stream);
 
 /*
+ * One decode step of the fused path ([Paged]: the new token's K/V are
+ * compressed into the paged cache and the decode then reads the cache): the
+ * same results, bit for bit, as tq_store(k, v, in_dtype, num_tokens,
+ * slot_mapping) followed by tq_decode_attention(q, ...) on the same stream.
+ * Arguments, layouts and errors are those of the two calls; every argument
+ * of both is checked before anything launches, so an error status means
+ * nothing was enqueued.  num_tokens == 0 stores nothing.
+ * Ordering: q (like k and v) must be final when the call's first kernel
+ * starts, i.e. written by work that precedes the call in the stream and that
+ * finishes in plain stream order.  With num_tokens > 0 the decode's query
+ * pass then reads q while the store kernel runs; it writes nothing before the
+ * store completes.
+ */
+tq_status tq_store_decode_attention(const tq_cache* cache, const void* k, const void* v, int in_dtype,
+                                    int64_t num_tokens, const int64_t* slot_mapping, const void* q, int q_dtype,
+                                    void* cache_buf, const int32_t* block_table, const int32_t* seq_lens,
+                                    const void* tail_k, const void* tail_v, const int32_t* tail_lens, float scale,
+                                    int batch, void* out, int out_dtype, void* stream);
+
+/*
  * Extend (prefill) attention over the compressed paged cache ([Roadmap] §4.1:
  * the extend kernel, like the decode kernel, reads the compressed pool
  * directly).  Sequence b < batch brings n_b = cu_q[b+1] - cu_q[b] new tokens:

@@ -22,7 +22,7 @@ __all__ = [
     "tq_make_qjl_matrix", "tq_cache_sizes", "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params",
     "tq_store", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_set_profile_events",
     "tq_get_device_error", "tq_set_store_small_max", "tq_extend_attention", "TQ_DEVERR_CHUNK", "TQCache",
-    "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT", "tq_check_wait_timeout",
+    "TQ_PROF_STORE", "TQ_PROF_DECODE_SPLIT", "tq_check_wait_timeout", "tq_store_decode_attention",
 ]
 
 TQ_DTYPE_F32, TQ_DTYPE_BF16 = 0, 1
@@ -38,6 +38,7 @@ EXPORTED = [
     "tq_cache_create", "tq_cache_destroy", "tq_cache_export_params", "tq_store", "tq_decode_attention",
     "tq_set_profile_events", "tq_get_device_error", "tq_decode_attention_noalloc", "tq_last_cuda_error",
     "tq_set_store_small_max", "tq_make_uniform_codebook", "tq_extend_attention", "tq_check_wait_timeout",
+    "tq_store_decode_attention",
 ]
 TQ_PROF_STORE, TQ_PROF_DECODE_SPLIT = 0, 1
 
@@ -118,6 +119,8 @@ def load_library():
             "tq_get_device_error": (i32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
             "tq_set_store_small_max": (i32, [i64]),
             "tq_check_wait_timeout": (i32, [_P, ctypes.c_uint32, _P]),
+            "tq_store_decode_attention": (
+                i32, [_P, _P, _P, i32, i64, _P, _P, i32, _P, _P, _P, _P, _P, _P, ctypes.c_float, i32, _P, i32, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -269,6 +272,26 @@ def tq_decode_attention(handle, q, cache, block_table, seq_lens, out, tail_k=Non
         _dtype_code(out) | (TQ_OUT_ROTATED if rotated else 0), _stream_ptr(stream)), "tq_decode_attention")
 
 
+def tq_store_decode_attention(handle, k, v, slot_mapping, q, cache, block_table, seq_lens, out, tail_k=None,
+                              tail_v=None, tail_lens=None, scale=0.0, stream=None, rotated=False):
+    """tq_store(k, v, slot_mapping) then tq_decode_attention(q, ...) in one
+    call; k and v may have zero tokens (nothing is stored)."""
+    import torch
+
+    if k.dtype != v.dtype or k.shape != v.shape:
+        raise ValueError("k and v must have the same shape and dtype")
+    if tail_k is not None:
+        _dev(tail_k, "tail_k", torch.bfloat16)
+        _dev(tail_v, "tail_v", torch.bfloat16)
+    _check(load_library().tq_store_decode_attention(
+        handle, _dev(k, "k"), _dev(v, "v"), _dtype_code(k), k.shape[0],
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(q, "q"), _dtype_code(q), _dev(cache, "cache"),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(tail_k, "tail_k"), _dev(tail_v, "tail_v"), _dev(tail_lens, "tail_lens", torch.int32), float(scale),
+        q.shape[0], _dev(out, "out"), _dtype_code(out) | (TQ_OUT_ROTATED if rotated else 0), _stream_ptr(stream)),
+        "tq_store_decode_attention")
+
+
 def tq_decode_attention_noalloc(handle, q, cache, block_table, seq_lens, out, tail_k=None, tail_v=None,
                                 tail_lens=None, scale=0.0, stream=None):
     """tq_decode_attention with its scratch in the library's static device
@@ -364,6 +387,16 @@ class TQCache:
             out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
         tq_decode_attention(self.handle, q, self.cache, block_table, seq_lens, out, tail_k, tail_v, tail_lens,
                             scale, stream, rotated)
+        return out
+
+    def store_decode(self, k, v, slot_mapping, q, block_table, seq_lens, out=None, tail_k=None, tail_v=None,
+                     tail_lens=None, scale=0.0, stream=None, out_dtype=None, rotated=False):
+        import torch
+
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
+        tq_store_decode_attention(self.handle, k, v, slot_mapping, q, self.cache, block_table, seq_lens, out,
+                                  tail_k, tail_v, tail_lens, scale, stream, rotated)
         return out
 
     def extend(self, q, block_table, prefix_lens, cu_q, new_k, new_v, out=None, scale=0.0, stream=None,

@@ -206,6 +206,32 @@ extern "C" tq_status tq_decode_attention(const tq_cache* c, const void* q, int q
     return launch_decode(a, (cudaStream_t)stream, e0, e1);
 }
 
+extern "C" tq_status tq_store_decode_attention(const tq_cache* c, const void* k, const void* v, int in_dtype,
+                                               int64_t num_tokens, const int64_t* slot_mapping, const void* q,
+                                               int q_dtype, void* cache_buf, const int32_t* block_table,
+                                               const int32_t* seq_lens, const void* tail_k, const void* tail_v,
+                                               const int32_t* tail_lens, float scale, int batch, void* out,
+                                               int out_dtype, void* stream) {
+    // both calls' arguments are checked before either launches
+    DecodeArgs a;
+    tq_status st = decode_args(c, q, q_dtype, cache_buf, block_table, seq_lens, tail_k, tail_v, tail_lens, scale,
+                               batch, out, out_dtype, &a);
+    if (st != TQ_OK) return st;
+    if (num_tokens < 0) return TQ_ERR_INVALID_ARG;
+    if (num_tokens > 0) {
+        if (!k || !v || !slot_mapping) return TQ_ERR_INVALID_ARG;
+        if (in_dtype != TQ_DTYPE_F32 && in_dtype != TQ_DTYPE_BF16) return TQ_ERR_INVALID_ARG;
+        if (((uintptr_t)k & 3) || ((uintptr_t)v & 3)) return TQ_ERR_MISALIGNED;
+        st = tq_store(c, k, v, in_dtype, num_tokens, slot_mapping, cache_buf, stream);
+        if (st != TQ_OK) return st;
+        // the store kernel, launched in plain stream order, began after the
+        // queries' writer had finished: the query prep may read them at once
+        a.q_early = true;
+    }
+    void *e0 = c->prof_start[TQ_PROF_DECODE_SPLIT], *e1 = c->prof_stop[TQ_PROF_DECODE_SPLIT];
+    return launch_decode(a, (cudaStream_t)stream, e0, e1);
+}
+
 namespace tq {
 
 // One thread waits for phase 0 of a shared-memory mbarrier that expects one

@@ -86,6 +86,12 @@ struct DecodeArgs {
     // the query prep releases its dependents at its end rather than at its
     // start (before the extend prefix kernel, which takes a whole SM)
     bool prep_late_release = false;
+    // the query prep's predecessor is a store kernel launched without the
+    // programmatic attribute, so everything that wrote the queries finished
+    // before it began: the prep loads its queries and tables before its wait
+    // (the wait still comes before any write, and its completion then implies
+    // the store's, which the split kernel relies on)
+    bool q_early = false;
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
     int64_t num_blocks;
@@ -231,18 +237,27 @@ constexpr int kPrepThreads = 512;  // its phases are short serial chains
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // launched programmatically: the preceding kernel (the step's store, or
-    // whatever wrote the queries) must be complete before anything is read
-    pdl_wait();
-    if (!a.prep_late_release) pdl_launch_dependents();  // the split kernel's prologue may start
+    // whatever wrote the queries) must be complete before anything is read,
+    // unless q_early says the queries were complete before that kernel began
+    if (!a.q_early) pdl_wait();
+    // the split kernel's prologue may start (with q_early once the store is
+    // done: its CTAs would otherwise sit beside the store's)
+    if (!a.prep_late_release && !a.q_early) pdl_launch_dependents();
     const int g = blockIdx.x, E = a.prep_entries, b0 = blockIdx.y * E;
     const int ne = min(E, a.batch - b0);
-    if (ne <= 0) return;
+    if (ne <= 0) {
+        if (a.q_early) pdl_wait();
+        return;
+    }
     // an extend entry with no compressed prefix uses none of this (its exact
     // part reads the raw queries)
     if (a.chunk_attn) {
         bool any = false;
         for (int e = 0; e < ne; ++e) any |= a.seq_lens[b0 + e] > 0;
-        if (!any) return;
+        if (!any) {
+            if (a.q_early) pdl_wait();
+            return;
+        }
     }
     const int G = a.group, GV = ne * G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5,
               nwarps = blockDim.x >> 5;
@@ -272,6 +287,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     }
     for (int e = tid; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
+    if (a.q_early) {
+        pdl_wait();  // the store, before any write
+        if (!a.prep_late_release) pdl_launch_dependents();
+    }
     __syncthreads();
     const float f = a.scale_log2e;
     // per-head sums and maxima for the constants below: [head][0..2] sum, sum
