@@ -88,9 +88,9 @@ struct DecodeArgs {
     bool prep_late_release = false;
     // the query prep's predecessor is a store kernel launched without the
     // programmatic attribute, so everything that wrote the queries finished
-    // before it began: the prep loads its queries and tables before its wait
-    // (the wait still comes before any write, and its completion then implies
-    // the store's, which the split kernel relies on)
+    // before it began: the prep loads its queries and computes R q and S q
+    // before its wait (which still comes before any write; its completion
+    // then implies the store's, which the split kernel relies on)
     bool q_early = false;
     float scale_log2e;  // softmax scale * log2(e)
     int batch;
@@ -287,10 +287,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     }
     for (int e = tid; e < D; e += blockDim.x) s_signs[e] = a.dp.signs[e];
     if (tid < 9) s_kw[tid] = a.dp.k_walsh[tid];
-    if (a.q_early) {
-        pdl_wait();  // the store, before any write
-        if (!a.prep_late_release) pdl_launch_dependents();
-    }
     __syncthreads();
     const float f = a.scale_log2e;
     // per-head sums and maxima for the constants below: [head][0..2] sum, sum
@@ -446,6 +442,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
     // a copy that never completed must land before the block exits
     if (!s_ok) mbar_wait(smem_u32(bar), 0, a.dp.err);
     __syncthreads();
+    if (a.q_early) {
+        pdl_wait();  // the store, before any write
+        if (!a.prep_late_release) pdl_launch_dependents();
+    }
     // the scaled query for the exact tail's scores (extend's exact part reads
     // the raw queries)
     if (a.tail_cap > 0 && !a.chunk_attn)
