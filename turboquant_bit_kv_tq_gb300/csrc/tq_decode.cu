@@ -80,6 +80,9 @@ static tq_status launch_dim(DecodeArgs a, cudaStream_t s, void* ev0, void* ev1) 
                                    chunk_smem_bytes(), s>>>(a);
             const tq_status st = cuda_status(cudaGetLastError());
             if (st != TQ_OK) return st;
+            // it began after the queries' writer had finished: the prep may
+            // read them beside it
+            a.q_early = true;
         }
     }
     {

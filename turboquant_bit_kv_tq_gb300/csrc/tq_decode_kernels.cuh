@@ -624,6 +624,9 @@ __host__ __device__ constexpr size_t chunk_smem_bytes() {
 template <int D>
 __global__ void __launch_bounds__(32 * kChunkMaxWarps) chunk_attn_kernel(DecodeArgs a) {
     static_assert(D == 128, "the chunk kernel holds a 128-wide output row in registers");
+    // launched in plain stream order; the query prep after it (q_early) may
+    // compute beside it and waits for it before its first write
+    pdl_launch_dependents();
     constexpr int KP = D * 2 + 16;  // staged row pitch (bytes): conflict-free fragment loads
     constexpr int NKS = D / 16, NSB = kChunkKeys / 8, NOB = D / 8;
     extern __shared__ __align__(16) uint8_t smem[];
