@@ -187,7 +187,6 @@ tq_status decode_args(const tq_cache* c, const void* q, int q_dtype, const void*
     a->lay = c->lay;
     a->dp = c->dp;
     a->gm = c->geom;
-    a->ws_q = c->ws_q;
     a->ws_bimg = c->ws_bimg;
     a->ws_cst = c->ws_cst;
     a->ws_acc = c->ws_acc;
@@ -420,7 +419,6 @@ extern "C" tq_status tq_extend_attention(const tq_cache* c, const void* q, int q
     a.lay = c->lay;
     a.dp = c->dp;
     a.gm = c->geom;
-    a.ws_q = c->ws_q;
     a.ws_bimg = c->ws_bimg;
     a.ws_cst = c->ws_cst;
     a.ws_acc = c->ws_acc;

@@ -103,7 +103,6 @@ struct DecodeArgs {
     Layout lay;
     DeviceParams dp;
     DecodeGeom gm;
-    float* ws_q;
     uint8_t* ws_bimg;
     float* ws_cst;
     float* ws_acc;
@@ -208,7 +207,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-// ws_q[b][h] = q * f (when a hybrid tail reads it), f = scale*log2(e); R q * f
+// f = scale*log2(e); R q * f
 // and S q * f * sqrt(pi/2)/d stay in shared memory for what follows:
 // ws_cst[b][h] = { C_h, Q_h, 2^-sigmaK, 2^-sigmaQ } with
 //   C_h = alpha sum_i (Rq)_i + 1/2 sum_P beta_P sum_{i%8=7} (Rq)_i
@@ -446,10 +445,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeArgs a) {
         pdl_wait();  // the store, before any write
         if (!a.prep_late_release) pdl_launch_dependents();
     }
-    // the scaled query for the exact tail's scores (extend's exact part reads
-    // the raw queries)
-    if (a.tail_cap > 0 && !a.chunk_attn)
-        for (int e = tid; e < GV * D; e += blockDim.x) a.ws_q[hrow(e / D) * D + e % D] = qv[(e / D) * QS + e % D] * f;
     // per-head constants and operand scales (one warp per head)
     const DecodeGeom gm = a.gm;
     const float* kw = s_kw;
@@ -860,8 +855,14 @@ __device__ void tail_split(const DecodeArgs& a, int g, int b, uint8_t* smem, int
     float* pr = qs + NH * D;                     // [NH][kTile]
     float* sm_m = pr + NH * kTile;               // [NH]
     uint16_t* vst = reinterpret_cast<uint16_t*>(sm_m + kMaxG);  // [kTailV][D] staged values (bf16)
-    for (int e = tid; e < NH * D; e += blockDim.x)
-        qs[e] = a.ws_q[((int64_t)b * a.q_heads + g * G + h0 + e / D) * D + e % D];
+    // the query times f, read from the caller's queries (the same product
+    // as the query prep's, which this kernel does not wait for)
+    for (int e = tid; e < NH * D; e += blockDim.x) {
+        const int64_t src = ((int64_t)b * a.q_heads + g * G + h0 + e / D) * D + e % D;
+        qs[e] = (a.q_dtype == TQ_DTYPE_F32 ? static_cast<const float*>(a.q)[src]
+                                           : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[src])) *
+                a.scale_log2e;
+    }
     int tl = a.tail_lens ? a.tail_lens[b] : 0;
     if (tl < 0 || tl > a.tail_cap) {
         if (tid == 0 && g == 0) set_error(a.dp.err, TQ_DEVERR_TAIL);

@@ -54,7 +54,6 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache* c, const void* 
     const tq_status sa = scratch_address(&ws);
     if (sa != TQ_OK) return sa;
     // every scratch byte read below is written earlier by the same call
-    a.ws_q = reinterpret_cast<float*>(ws + wl.q);
     a.ws_bimg = ws + wl.bimg;
     a.ws_cst = reinterpret_cast<float*>(ws + wl.cst);
     a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);

@@ -989,11 +989,14 @@ __global__ void __launch_bounds__(kWsThreads, kWsCtasPerSm) split_ws_kernel(Deco
 template <int D>
 __global__ void __launch_bounds__(128) tail_kernel(DecodeArgs a) {
     pdl_launch_dependents();
-    pdl_wait();  // the query prep's results
     extern __shared__ __align__(16) uint8_t smem[];
     const int g = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
-    if (b >= a.batch || h >= a.group) return;
-    tail_split<D>(a, g, b, smem, h, 1);
+    // it reads only the caller's inputs, final once the query prep (its
+    // predecessor) has started, and writes only its own partials, so it runs
+    // beside the prep; it waits for the prep at its end because the split
+    // kernel after it waits only on it
+    if (b < a.batch && h < a.group) tail_split<D>(a, g, b, smem, h, 1);
+    pdl_wait();
 }
 
 template <int D, int KB, bool KU, bool G32, int VB, int NTH>

@@ -132,8 +132,6 @@ WorkspaceLayout workspace_layout(const tq_cache_config& c) {
     const size_t bh = size_t(c.max_batch) * c.num_q_heads, d = c.head_dim;
     WorkspaceLayout w;
     size_t off = 0;
-    w.q = off;
-    off = up256(off + bh * d * 4);
     w.bimg = off;
     off = up256(off + size_t(c.max_batch) * c.num_kv_heads * gm.nhg * gm.bimg_bytes);
     w.cst = off;
@@ -634,7 +632,6 @@ tq_status tq_cache_create(const tq_cache_config* cfg, void* params_dev, void* wo
     const WorkspaceLayout wl = workspace_layout(*cfg);
     uint8_t* ws = (uint8_t*)workspace_dev;
     h->geom = decode_geom(*cfg);
-    h->ws_q = (float*)(ws + wl.q);
     h->ws_bimg = (uint8_t*)(ws + wl.bimg);
     h->ws_cst = (float*)(ws + wl.cst);
     h->ws_acc = (float*)(ws + wl.acc);

@@ -82,11 +82,10 @@ struct DecodeGeom {
 DecodeGeom decode_geom(const tq_cache_config& c);
 
 struct WorkspaceLayout {
-    // q: [B][Hq][d] fp32 (the query times scale log2 e, for the exact tail);
     // bimg: [B][Hkv][nhg][bimg_bytes] (score operands); cst: [B][Hq][4] fp32; acc: [B][Hq][S][d]; ml: [B][Hq][S][2];
     // ext: 4 x [B] int32 (extend attention's per-token lengths and rows), then
     // 4 int32 and [B] int4 (the extend prefix kernel's query blocks)
-    size_t q, bimg, cst, acc, ml, ext, total;
+    size_t bimg, cst, acc, ml, ext, total;
 };
 
 // TQ_OK for cudaSuccess; otherwise records the runtime's message for
@@ -119,7 +118,6 @@ struct tq_cache {
     tq::Splits splits;
     tq::DeviceParams dp;
     tq::DecodeGeom geom;
-    float* ws_q;
     uint8_t* ws_bimg;
     float* ws_cst;
     float* ws_acc;
