@@ -142,3 +142,23 @@ def test_extend_binding_checks_shapes_before_any_call():
         tq.tq_extend_attention(None, q, None, table[:1], pl, cu, kv, kv, out)
     with pytest.raises(ValueError):  # CPU tensors never reach the library
         tq.tq_extend_attention(None, q, torch.zeros(16, dtype=torch.uint8), table, pl, cu, kv, kv, out)
+
+
+def test_store_decode_entry_checks_arguments_before_any_launch():
+    torch = pytest.importorskip("torch")
+    lib = tq.load_library()
+    # a null cache handle is refused before anything reaches CUDA
+    st = lib.tq_store_decode_attention(None, None, None, tq.TQ_DTYPE_BF16, 0, None, None, tq.TQ_DTYPE_BF16, None,
+                                       None, None, None, None, None, 0.0, 1, None, tq.TQ_DTYPE_F32, None)
+    assert st == -1  # TQ_ERR_INVALID_ARG
+    # the binding checks shapes and devices first
+    k = torch.zeros((2, 8, 128), dtype=torch.bfloat16)
+    q = torch.zeros((2, 32, 128), dtype=torch.bfloat16)
+    slots = torch.zeros(2, dtype=torch.int64)
+    table = torch.zeros((2, 4), dtype=torch.int32)
+    lens = torch.zeros(2, dtype=torch.int32)
+    out = torch.zeros((2, 32, 128))
+    with pytest.raises(ValueError):  # k and v differ
+        tq.tq_store_decode_attention(None, k, k[:1], slots, q, None, table, lens, out)
+    with pytest.raises(ValueError):  # CPU tensors never reach the library
+        tq.tq_store_decode_attention(None, k, k, slots, q, torch.zeros(16, dtype=torch.uint8), table, lens, out)
